@@ -1,0 +1,418 @@
+#!/usr/bin/env python
+"""Benchmark of the W8A8 projection path on one GB300 (replicas for N > 1).
+
+A step is one pass of the whole workload's hot path over one batch: every
+activation quantizer call and every projection GEMM (with its fused epilogue;
+LoRA adds where the workload has them).  Default workload: the INT8 MLP of
+one 27B-shaped layer at 1,502 tokens (packed gate/up 5120 -> 2 x 17408 with the
+fused SwiGLU epilogue, then down 17408 -> 5120).
+
+Printed (rank 0, one JSON line): whole-step W8A8 GEMM throughput in TOPS
+(2*M*N*K per projection, counted once), the end-to-end figure through the
+C ABI with host buffers, the roofline of the dominant kernel from CUDA events
+recorded on its stream, the quantizer's GB/s, clocks sampled during the timed
+region, and the CPU oracle timed on a bounded sample on the host cores.
+``--impl reference`` times that oracle as the reference arm instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import clef_synth as S  # noqa: E402
+
+METRIC = "W8A8 linear TOPS & % of GB300 dense INT8/FP8 peak; quantizer GB/s vs HBM"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="clef", choices=["clef", "reference"])
+    ap.add_argument("--config", type=int, default=1, help="workload index (0-4)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mp = json.load(f)
+        return mp["hbm_gbs"], mp["bf16_tflops"], mp.get("bf16_tflops_sustained"), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+
+def _par(fn, n, threads):
+    from concurrent.futures import ThreadPoolExecutor
+    chunk = max(1, -(-n // threads))
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        parts = list(ex.map(lambda a: fn(a, min(n, a + chunk)), range(0, n, chunk)))
+    return tuple(np.concatenate([p[i] for p in parts]) for i in range(len(parts[0]))) \
+        if isinstance(parts[0], tuple) else np.concatenate(parts)
+
+
+def oracle_weights(cfg, weights, threads):
+    """The oracle's own quantisation of every weight (set-up, not timed)."""
+    import oracle as O
+    qfn = (lambda x: O.quant_fp8(x)) if cfg.scheme == "fp8" else O.quant_int8_h128
+    return {name: _par(lambda a, b: qfn(W[a:b]), W.shape[0], threads) for name, (W, _) in weights.items()}
+
+
+def oracle_sample(cfg, acts, weights, qw, lora, rows, threads):
+    """Run the oracle over `rows` (row indices) of the workload; returns
+    (seconds, algorithmic GEMM ops covered)."""
+    import oracle as O
+
+    def par(fn, n):
+        return _par(fn, n, threads)
+
+    fp8 = cfg.scheme == "fp8"
+    qfn = (lambda x: O.quant_fp8(x)) if fp8 else O.quant_int8_h128
+    R = len(rows)
+    xs = {name: np.ascontiguousarray(x[rows]) for name, x in acts.items()}
+    t0 = time.perf_counter()
+
+    def run_rows(a, b):
+        q = {name: qfn(x[a:b]) for name, x in xs.items()}
+        h = None
+        out = None
+        for p in cfg.projections:
+            wq, ws = qw[p.name]
+            bias = weights[p.name][1]
+            qx, sx = qfn(h) if p.chained else q[p.act]
+            if p.kind == "gateup":
+                if lora:
+                    y = (O.fp8_linear if fp8 else O.int8_linear)(qx, sx, wq, ws, bias)
+                    N = p.N
+                    x = xs[p.act][a:b]
+                    y[:, :N] = O.lora_add(x, *lora[p.name + "/gate"], y[:, :N])
+                    y[:, N:] = O.lora_add(x, *lora[p.name + "/up"], y[:, N:])
+                    h = O.swiglu_bf16(y)
+                elif fp8:
+                    h = O.fp8_gateup_swiglu(qx, sx, wq, ws, bias)
+                else:
+                    h = O.int8_gateup_swiglu(qx, sx, wq, ws, bias)
+                out = h
+            else:
+                out = (O.fp8_linear if fp8 else O.int8_linear)(qx, sx, wq, ws, bias)
+                if lora and p.name in lora:
+                    A, B = lora[p.name]
+                    out = O.lora_add(xs[p.act][a:b] if not p.chained else h, A, B, out)
+        return (out,)
+
+    par(run_rows, R)
+    dt = time.perf_counter() - t0
+    ops = sum(p.ops(R) for p in cfg.projections)
+    return dt, ops
+
+
+def cpu_threads():
+    return max(1, os.cpu_count() or 1)
+
+
+def sample_rows(cfg, n):
+    rng = np.random.default_rng(1234)
+    return np.sort(rng.choice(cfg.M, size=min(n, cfg.M), replace=False))
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    cfg = S.CONFIGS[args.config]
+    acts, weights, lora = S.layer_inputs(cfg, seed=0)
+    threads = cpu_threads()
+    per_step_rows = threads  # one row per host thread per step
+    rows = sample_rows(cfg, per_step_rows)
+    qw = oracle_weights(cfg, weights, threads)
+    for _ in range(args.warmup):
+        oracle_sample(cfg, acts, weights, qw, lora, rows, threads)
+    times, ops = [], 0
+    for _ in range(args.steps):
+        dt, ops = oracle_sample(cfg, acts, weights, qw, lora, rows, threads)
+        times.append(dt)
+    tot = sum(times)
+    value = ops * args.steps / tot / 1e12
+    sample = f"{len(rows)} of {cfg.M} token rows per step through every projection of {cfg.name}"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8" if cfg.scheme == "fp8" else "int8", "data": "synthetic",
+        "config": workload_config(cfg),
+        "cpu_baseline": {"value": value, "unit": "TOPS", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(cfg):
+    d = {"workload": cfg.name, "tokens": cfg.M, "scheme": cfg.scheme,
+         "projections": {p.name: [p.K, p.weight_rows] for p in cfg.projections},
+         "l2": "flushed between steps (256 MiB write, outside the per-step events)"}
+    if cfg.lora_rank:
+        d["lora_rank"] = cfg.lora_rank
+    return d
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+    import w8a8_quantized_projections_gb300 as clef
+    from w8a8_quantized_projections_gb300.layer import QuantizedLayer
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    cfg = S.CONFIGS[args.config]
+    hbm_gbs, bf16_peak, bf16_sust, peak_src = peaks()
+
+    # replicas: each rank works on its own batch (seeded by rank), weights shared by seed
+    acts_np, weights_np, lora_np = S.layer_inputs(cfg, seed=0)
+    if rank:
+        acts_np = {n: S.activation(rank, f"{cfg.name}/act/{n}", cfg.M, x.shape[1]) for n, x in acts_np.items()}
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    weights = {k: (bf(W), bf(b)) for k, (W, b) in weights_np.items()}
+    lora = {k: (bf(A), bf(B)) for k, (A, B) in lora_np.items()}
+    acts = {k: bf(x) for k, x in acts_np.items()}
+    layer = QuantizedLayer(cfg, weights, lora or None, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        layer.step(acts)
+    torch.cuda.synchronize(dev)
+    assert clef.poll_status() == 0
+
+    # ---- device-timed steps (inputs resident in HBM)
+    events = {}
+    step_ev = []
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        layer.step(acts, events=events)
+        s1.record(stream)
+        step_ev.append((s0, s1))
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    status = clef.poll_status()
+    if status:
+        raise RuntimeError(f"device status word reported {status}")
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    t_sum = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([t_sum], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_sum = float(t.item())
+    ops_step = cfg.gemm_ops()
+    value = ops_step * args.steps * world / t_sum / 1e12
+
+    # per-kernel times
+    kt = {}
+    for key, lst in events.items():
+        kt[key] = [a.elapsed_time(b) / 1e3 for a, b in lst]
+    gemm_keys = [k for k in kt if k[0] == "gemm"]
+    proj = {p.name: p for p in cfg.projections}
+    dom = max(gemm_keys, key=lambda k: sum(kt[k]))
+    dom_p = proj[dom[1]]
+    dom_t = statistics.mean(kt[dom])
+    dom_ops = dom_p.ops(cfg.M)
+    achieved = dom_ops / dom_t / 1e12
+    q_bytes = 0
+    q_time = 0.0
+    for key, lst in kt.items():
+        if key[0] != "quant":
+            continue
+        K = acts_np[key[1]].shape[1] if key[1] in acts_np else proj_input_K(cfg, key[1])
+        q_bytes += (3 * cfg.M * K + 4 * cfg.M) * len(lst)
+        q_time += sum(lst)
+    q_gbs = q_bytes / q_time / 1e9 if q_time else None
+    gemm_time = sum(sum(kt[k]) for k in gemm_keys)
+    gemm_tops = ops_step * args.steps / gemm_time / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t_sum / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8" if cfg.scheme == "fp8" else "int8", "data": "synthetic",
+        "config": workload_config(cfg),
+        "roofline": {
+            "kernel": f"{'fp8' if cfg.scheme == 'fp8' else 'w8a8'} {dom_p.name} GEMM "
+                      f"({cfg.M}x{dom_p.weight_rows}x{dom_p.K})",
+            "bound": "tensor", "achieved": achieved,
+            "peak": bf16_peak * (2.0 if cfg.scheme == "fp8" else 1.0),
+            "unit": "TFLOP/s",
+            "frac": achieved / (bf16_peak * (2.0 if cfg.scheme == "fp8" else 1.0)),
+            "traffic": None,
+            "peak_source": (f"{peak_src} bf16 dense burst x2 (fp8 nominal ratio)" if cfg.scheme == "fp8"
+                            else f"{peak_src} bf16 dense burst (INT8 runs exactly on the fp16 tensor "
+                                 f"pipe: sm_103a has no tcgen05 integer MMA)"),
+        },
+        "gemm_only_tops": gemm_tops,
+        "quantizer": {"achieved": q_gbs, "unit": "GB/s", "peak": hbm_gbs,
+                      "frac": (q_gbs / hbm_gbs) if q_gbs else None,
+                      "bytes_per_element": 3, "bytes_per_row": 4},
+        "kernel_ms": {f"{k[0]}:{k[1]}": 1e3 * statistics.mean(v) for k, v in kt.items()},
+        "gpu_launches": layer.launches_per_step() * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+
+    # ---- end to end through the C ABI with host buffers
+    if not args.no_e2e:
+        line["e2e"] = e2e(args, layer, acts, acts_np, cfg, dev, stream, world, torch)
+
+    # ---- CPU oracle on a bounded sample (rank 0, N = 1)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = cpu_threads()
+        rows = sample_rows(cfg, 4 * threads)
+        qw = oracle_weights(cfg, weights_np, threads)
+        dt, ops = oracle_sample(cfg, acts_np, weights_np, qw, lora_np, rows, threads)
+        line["cpu_baseline"] = {"value": ops / dt / 1e12, "unit": "TOPS", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"{len(rows)} of {cfg.M} token rows through every projection "
+                                          f"of {cfg.name} ({dt:.1f} s)"}
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def proj_input_K(cfg, act):
+    for p in cfg.projections:
+        if p.act == act:
+            return p.K
+    raise KeyError(act)
+
+
+def e2e(args, layer, acts, acts_np, cfg, dev, stream, world, torch):
+    """Same metric with host buffers: each step copies its activations in from
+    pinned host memory and the step's final output back, inside the timing."""
+    host_in = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).pin_memory()
+               for k, v in acts_np.items()}
+    last = cfg.projections[-1].name
+    out_dev = layer.out[last]
+    host_out = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
+    dev_in = {k: torch.empty_like(v) for k, v in acts.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    for _ in range(2):
+        for k in dev_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        layer.step(dev_in)
+        host_out.copy_(out_dev, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        for k in dev_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        layer.step(dev_in)
+        host_out.copy_(out_dev, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t = e0.elapsed_time(e1) / 1e3
+    return {"value": cfg.gemm_ops() * args.steps * world / t / 1e12, "unit": "TOPS",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+if __name__ == "__main__":
+    main()

@@ -25,6 +25,10 @@ Generator (stated so that it can be re-implemented anywhere):
 """
 from __future__ import annotations
 
+import os
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 from .configs import CONFIGS, Config, Projection  # noqa: F401
@@ -73,6 +77,46 @@ def normals(seed: int, name: str, n: int, start: int = 0) -> np.ndarray:
     return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
 
 
+_tls = threading.local()
+_BASE = None
+
+
+def _normals_ws(sseed: np.uint64, start: int, n: int) -> np.ndarray:
+    """Same values as ``normals`` for an already-derived stream seed, computed
+    in place in a per-thread workspace (fresh pages are slow to fault in)."""
+    global _BASE
+    if _BASE is None:
+        _BASE = np.arange(2 * _CHUNK, dtype=np.uint64)
+    ws = getattr(_tls, "ws", None)
+    if ws is None:
+        ws = _tls.ws = (np.empty(2 * _CHUNK, np.uint64), np.empty(2 * _CHUNK, np.uint64),
+                        np.empty(_CHUNK, np.float64), np.empty(_CHUNK, np.float64))
+    z, t, u1, u2 = ws
+    z, t, u1, u2 = z[:2 * n], t[:2 * n], u1[:n], u2[:n]
+    with np.errstate(over="ignore"):
+        np.add(_BASE[:2 * n], np.uint64(2 * start + 1), out=z)      # counter i
+        np.multiply(z, _GOLDEN, out=z)
+        np.add(z, sseed, out=z)
+        for sh, mul in ((30, _M1), (27, _M2)):
+            np.right_shift(z, np.uint64(sh), out=t)
+            np.bitwise_xor(z, t, out=z)
+            np.multiply(z, mul, out=z)
+        np.right_shift(z, np.uint64(31), out=t)
+        np.bitwise_xor(z, t, out=z)
+        np.right_shift(z, np.uint64(11), out=z)
+    u1[:] = z[0::2]
+    u2[:] = z[1::2]
+    u1 += 1.0
+    u1 *= 2.0 ** -53
+    u2 *= 2.0 ** -53
+    np.log(u1, out=u1)
+    u1 *= -2.0
+    np.sqrt(u1, out=u1)
+    u2 *= 2.0 * np.pi
+    np.cos(u2, out=u2)
+    return u1 * u2
+
+
 def f64_to_bf16_bits(v: np.ndarray) -> np.ndarray:
     """Round fp64 values to bf16 storage (via fp32, both steps nearest-even)."""
     f = np.ascontiguousarray(v, dtype=np.float32).view(np.uint32)
@@ -114,12 +158,23 @@ def normal_bf16(seed: int, name: str, shape, std: float = 1.0,
         mult = np.ones(K, dtype=np.float64)
         mult[outlier_channels(seed, name, K, outliers)] = outlier_scale
         cols = mult
-    for a in range(0, n, _CHUNK):
+    sseed = np.uint64(stream_seed(seed, name))
+
+    def fill(a):
         b = min(n, a + _CHUNK)
-        v = normals(seed, name, b - a, start=a) * std
+        v = _normals_ws(sseed, a, b - a)
+        v *= std
         if cols is not None:
-            v = v * cols[np.arange(a, b, dtype=np.int64) % shape[-1]]
+            v *= cols[np.arange(a, b, dtype=np.int64) % shape[-1]]
         out[a:b] = f64_to_bf16_bits(v)
+
+    starts = range(0, n, _CHUNK)
+    if n > _CHUNK:
+        with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, starts))
+    else:
+        for a in starts:
+            fill(a)
     return out.reshape(shape)
 
 
@@ -142,3 +197,37 @@ def lora_pair(seed: int, name: str, r: int, K: int, N: int):
     """LoRA factors A ``[r][K]`` and B ``[N][r]``, entries N(0, 0.01^2)."""
     return (normal_bf16(seed, name + "/A", (r, K), 0.01),
             normal_bf16(seed, name + "/B", (N, r), 0.01))
+
+
+def layer_inputs(cfg: Config, seed: int = 0, rows: slice | None = None):
+    """Seeded inputs of one workload: activations, weights (+bias) and LoRA pairs.
+
+    Returns (acts, weights, lora) as numpy bf16-bit arrays:
+    acts[name] = [M][K] (chained inputs are produced by the path itself and are
+    absent); weights[proj] = (W [rows][K], bias [rows]) with gate/up packed gate
+    rows first; lora[proj] = (A [r][K], B [N][r]) and, for gate/up,
+    lora[proj + "/gate"], lora[proj + "/up"].  Every tensor has its own named
+    sub-stream, so any subset can be regenerated alone.
+    """
+    acts = {}
+    for name, K in cfg.activations():
+        acts[name] = activation(seed, f"{cfg.name}/act/{name}", cfg.M, K)
+    weights, lora = {}, {}
+    for p in cfg.projections:
+        if p.kind == "gateup":
+            W = np.concatenate([weight(seed, f"{cfg.name}/w/{p.name}/gate", p.N, p.K),
+                                weight(seed, f"{cfg.name}/w/{p.name}/up", p.N, p.K)])
+            b = np.concatenate([bias(seed, f"{cfg.name}/b/{p.name}/gate", p.N),
+                                bias(seed, f"{cfg.name}/b/{p.name}/up", p.N)])
+        else:
+            W = weight(seed, f"{cfg.name}/w/{p.name}", p.N, p.K)
+            b = bias(seed, f"{cfg.name}/b/{p.name}", p.N)
+        weights[p.name] = (W, b)
+        if cfg.lora_rank:
+            r = cfg.lora_rank
+            if p.kind == "gateup":
+                lora[p.name + "/gate"] = lora_pair(seed, f"{cfg.name}/lora/{p.name}/gate", r, p.K, p.N)
+                lora[p.name + "/up"] = lora_pair(seed, f"{cfg.name}/lora/{p.name}/up", r, p.K, p.N)
+            else:
+                lora[p.name] = lora_pair(seed, f"{cfg.name}/lora/{p.name}", r, p.K, p.N)
+    return acts, weights, lora

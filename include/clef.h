@@ -1,0 +1,202 @@
+/*
+ * clef.h -- C ABI of the GB300 (sm_103a) W8A8 quantized projection library.
+ *
+ * The library computes the quantized decoder linear projections of a
+ * Clef-style single-pass decision backbone: a per-token activation
+ * quantizer (block-128 Walsh-Hadamard rotation, absmax scale, symmetric INT8
+ * codes; FP8-e4m3 dynamic variant), W8A8 GEMMs whose epilogues fuse the
+ * row x column scales, the bias and, for packed gate/up weights, the SwiGLU
+ * product, and the runtime LoRA add.  Every step runs in hand-written CUDA
+ * kernels on the caller's stream.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers are DEVICE pointers to memory the caller owns; the library
+ *    never allocates, frees or synchronises inside these calls.
+ *  - Matrices are row-major.  x/activations are [M][K]; weights are [N][K]
+ *    (output-channel major, the Linear convention), so the GEMMs contract
+ *    both operands along their contiguous K axis.
+ *  - bf16 tensors hold IEEE bfloat16 bit patterns (uint16_t storage); e4m3
+ *    tensors hold OCP FP8 E4M3 codes (finite variant, max 448).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls
+ *    launch asynchronously and return; results are ready when the stream is.
+ *  - Return value: CLEF_OK, or an error code from argument checks made on
+ *    the host before anything is launched (nothing is launched on error),
+ *    or CLEF_ERR_CUDA when a launch fails.  Device-side waits that exceed
+ *    their time limit record CLEF_ERR_TIMEOUT in a library-owned status word
+ *    read by clef_poll_status(); the kernels never trap.
+ *  - M = 0 is a valid empty call: it returns CLEF_OK without a launch.
+ *  - Inputs are assumed finite; NaN/Inf inputs give unspecified codes.
+ *  - Alignment: every tensor base and every row pitch must be a multiple of
+ *    16 bytes (TMA and vector-access rule); the checks below state it per
+ *    call as the element counts that satisfy it.
+ *
+ * Sources (web pages; cited by title and section):
+ *  [INT8]  "CLEF Calibrated INT8 ConvRot" model card: Benefits (kernels fuse
+ *          calibrated scales, biases and MLP SwiGLU) and the note under the
+ *          latency table (a CUDA ConvRot activation quantizer feeds integer
+ *          GEMMs).
+ *  [USAGE] "Loading CLEF INT8" usage notes: fuse_mlp (paired gate/up epilogue
+ *          fusion) and gate/up weights packed during loading.
+ *  [FP8]   "clef-flash-FP8" model card, Quantization table and the note below
+ *          the recipe (FP8 weights per channel, FP8 activations per token,
+ *          dynamic; weight scales computed from the weights).
+ *  [LORA]  TensorFold pull request 1364, first bullet of the description:
+ *          y = bf16(y + bf16(x A^T) B^T), fp32 sums, bf16 add; A (rank, k),
+ *          B (n, rank); ranks zero-padded to whole 64-groups; a row's bits
+ *          independent of row count and chunking.
+ */
+#ifndef CLEF_H
+#define CLEF_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum clef_status {
+    CLEF_OK = 0,
+    CLEF_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or stride */
+    CLEF_ERR_UNSUPPORTED = 2,   /* device is not sm_103, or a mode not built */
+    CLEF_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    CLEF_ERR_TIMEOUT = 4        /* a device-side wait exceeded its limit */
+} clef_status;
+
+typedef enum clef_act_mode {
+    CLEF_ACT_INT8_H128 = 0,     /* rotate 128-blocks, s = amax/127, int8 codes */
+    CLEF_ACT_FP8_E4M3 = 1,      /* no rotation, s = amax/448, e4m3 codes */
+    CLEF_ACT_FP8_E4M3_H128 = 2  /* rotate 128-blocks, then the FP8 codes */
+} clef_act_mode;
+
+/*
+ * clef_quant_act -- per-token activation quantizer [INT8: latency-table
+ * note, "ConvRot activation quantizer"; FP8: Quantization table,
+ * "Activations FP8, per-token, dynamic"].  Also the weight quantizer: run on
+ * W's N rows it gives the per-output-channel codes and scales.
+ *
+ * For each row m of x (bf16 [M][K], row pitch ldx elements):
+ *   v = x[m] widened to fp32; for the H128 modes each contiguous 128-block of
+ *   v is rotated by the orthonormal Walsh-Hadamard butterfly (strides 1, 2,
+ *   4, ..., 64, (a+b, a-b) in fp32, then one multiply by fp32(1/sqrt(128)));
+ *   amax = max |v|;
+ *   INT8:  scale[m] = amax/127, q = clamp(rne(v * (127/amax)), -127, 127);
+ *   FP8:   scale[m] = amax/448, q = e4m3_rn_satfinite(v * (448/amax));
+ *   an all-zero row gives scale 0 and codes 0.
+ * q: int8 or e4m3 [M][K], dense (row pitch K); scale: fp32 [M].
+ * Requirements: K > 0, K % 128 == 0 for H128 modes else K % 32 == 0,
+ *   K <= 65536, ldx >= K, ldx % 8 == 0; x and q 16-byte aligned, scale 4-byte.
+ */
+int clef_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, int mode,
+                   void *q, float *scale, void *stream);
+
+/*
+ * clef_w8a8_linear -- W8A8 INT8 linear with the fused scale/bias epilogue
+ * [INT8: Benefits, "fuse calibrated scales, biases"].
+ *   acc[m][n] = sum_k qx[m][k] * qw[n][k]        (exact int32)
+ *   y[m][n]   = bf16(((float)acc * sx[m]) * sw[n] + bias[n])
+ * qx: int8 [M][K] dense; sx: fp32 [M]; qw: int8 [N][K] dense; sw: fp32 [N];
+ * bias: bf16 [N] or NULL; y: bf16 [M][N], row pitch ldy elements.
+ * Requirements: K % 16 == 0, N % 8 == 0, ldy >= N, ldy % 8 == 0.
+ */
+int clef_w8a8_linear(const int8_t *qx, const float *sx, const int8_t *qw, const float *sw,
+                     const void *bias, int64_t M, int64_t N, int64_t K,
+                     void *y, int64_t ldy, void *stream);
+
+/*
+ * clef_w8a8_gateup_swiglu -- INT8 gate/up projection with the paired SwiGLU
+ * epilogue [USAGE: fuse_mlp; gate/up packed during loading; INT8: Benefits,
+ * "MLP SwiGLU"].  qw_gu: int8 [2N][K] with the gate rows 0..N-1 followed by
+ * the up rows N..2N-1; sw_gu, bias_gu: [2N] in the same order (bias may be
+ * NULL).  With g, u the unrounded fp32 epilogue values of rows n and N+n:
+ *   h[m][n] = bf16(g / (1 + expf(-g)) * u)
+ * h: bf16 [M][N], row pitch ldh.  Requirements as clef_w8a8_linear.
+ */
+int clef_w8a8_gateup_swiglu(const int8_t *qx, const float *sx, const int8_t *qw_gu,
+                            const float *sw_gu, const void *bias_gu,
+                            int64_t M, int64_t N, int64_t K,
+                            void *h, int64_t ldh, void *stream);
+
+/*
+ * clef_fp8_linear -- FP8 e4m3 W8A8 dynamic linear [FP8: Quantization table,
+ * "Weights FP8, per-channel; Activations FP8, per-token, dynamic"].
+ *   acc = sum_k qx[m][k] * qw[n][k] in fp32 (tensor-core accumulation order)
+ *   y[m][n] = bf16(((float)acc * sx[m]) * sw[n] + bias[n])
+ * qx: e4m3 [M][K]; qw: e4m3 [N][K]; other arguments as clef_w8a8_linear.
+ */
+int clef_fp8_linear(const void *qx, const float *sx, const void *qw, const float *sw,
+                    const void *bias, int64_t M, int64_t N, int64_t K,
+                    void *y, int64_t ldy, void *stream);
+
+/*
+ * clef_fp8_gateup_swiglu -- the FP8 counterpart of clef_w8a8_gateup_swiglu
+ * (the paired SwiGLU epilogue of [USAGE] over the FP8 scheme of [FP8]).
+ */
+int clef_fp8_gateup_swiglu(const void *qx, const float *sx, const void *qw_gu,
+                           const float *sw_gu, const void *bias_gu,
+                           int64_t M, int64_t N, int64_t K,
+                           void *h, int64_t ldh, void *stream);
+
+/*
+ * clef_lora_add -- runtime LoRA add [LORA: y = bf16(y + bf16(x A^T) B^T),
+ * fp32 sums and a bf16 add, rank zero-padded to a 64-group].
+ *   t[m][j] = bf16(sum_k x[m][k] * A[j][k])  for j < r, 0 for r <= j < r_pad
+ *   y[m][n] = bf16((float)y[m][n] + sum_j t[m][j] * B[n][j])   (in place)
+ * with r_pad = r rounded up to a multiple of 64.
+ * x: bf16 [M][K], row pitch ldx (the unquantized, unrotated input of the
+ * projection); A: bf16 [r][K] dense; B: bf16 [N][r] dense;
+ * t_scratch: bf16 [M][r_pad] dense, caller-owned scratch that receives t;
+ * y: bf16 [M][N], row pitch ldy, read and written.
+ * Requirements: K % 8 == 0, r % 8 == 0, 0 < r <= 1024, N % 8 == 0,
+ *   ldx >= K, ldx % 8 == 0, ldy >= N, ldy % 8 == 0.
+ */
+int clef_lora_add(const void *x, int64_t ldx, const void *A, const void *B,
+                  int64_t M, int64_t K, int64_t N, int64_t r,
+                  void *t_scratch, void *y, int64_t ldy, void *stream);
+
+/*
+ * clef_swiglu_bf16 -- the unfused MLP reading (fuse_mlp off in [USAGE]):
+ * y_gu holds bf16 gate values in columns 0..N-1 and up values in N..2N-1
+ * (row pitch ldg); h[m][n] = bf16(silu(float(g)) * float(u)).
+ * Requirements: N % 8 == 0, ldg >= 2N, ldg % 8 == 0, ldh >= N, ldh % 8 == 0.
+ */
+int clef_swiglu_bf16(const void *y_gu, int64_t M, int64_t N, int64_t ldg,
+                     void *h, int64_t ldh, void *stream);
+
+/*
+ * clef_w8a8_gemm_s32 -- the INT8 GEMM with its raw accumulator as output
+ * (acc[m][n] = sum_k qx[m][k] * qw[n][k], exact int32, row pitch ldc),
+ * through the same kernel and mainloop as clef_w8a8_linear.  It exists so
+ * that the integer accumulators can be compared bit for bit.
+ * Requirements: K % 16 == 0, N % 8 == 0, ldc >= N, ldc % 8 == 0.
+ */
+int clef_w8a8_gemm_s32(const int8_t *qx, const int8_t *qw, int64_t M, int64_t N, int64_t K,
+                       int32_t *acc, int64_t ldc, void *stream);
+
+/*
+ * clef_poll_status -- synchronises the device, then returns and clears the
+ * device-side status word (CLEF_OK if no kernel recorded an error).
+ */
+int clef_poll_status(void);
+
+/*
+ * clef_set_wait_limit_ns -- time limit of every device-side wait in kernels
+ * launched afterwards (default 1e9 ns).  A wait that exceeds it records
+ * CLEF_ERR_TIMEOUT and its kernel winds down and returns.  Test knob.
+ */
+void clef_set_wait_limit_ns(uint64_t ns);
+
+/* Human-readable name of a status code (static string). */
+const char *clef_status_string(int status);
+
+/* Text of the most recent argument or CUDA error seen by this thread's calls
+ * (empty if none); valid until the thread's next failing call. */
+const char *clef_last_error(void);
+
+/* ABI version of this library (major * 100 + minor). */
+int clef_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CLEF_H */

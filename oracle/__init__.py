@@ -64,11 +64,12 @@ def lib():
             L.orc_int8_gateup_swiglu.argtypes = [i8p, f32p, i8p, f32p, u16p, i64, i64, i64, u16p, i64]
             L.orc_swiglu_bf16.argtypes = [u16p, i64, i64, i64, u16p, i64]
             L.orc_fp8_linear.argtypes = [u8p, f32p, u8p, f32p, u16p, i64, i64, i64, u16p, i64]
+            L.orc_fp8_gateup_swiglu.argtypes = [u8p, f32p, u8p, f32p, u16p, i64, i64, i64, u16p, i64]
             L.orc_lora_t.argtypes = [u16p, i64, u16p, i64, i64, i64, i64, u16p]
             L.orc_lora_y.argtypes = [u16p, u16p, i64, i64, i64, i64, u16p, i64]
             for name in ("orc_rotate_rows_f32", "orc_quant_int8_h128", "orc_quant_fp8",
                          "orc_int8_gemm_acc", "orc_int8_linear", "orc_int8_gateup_swiglu",
-                         "orc_swiglu_bf16", "orc_fp8_linear", "orc_lora_t", "orc_lora_y"):
+                         "orc_swiglu_bf16", "orc_fp8_linear", "orc_fp8_gateup_swiglu", "orc_lora_t", "orc_lora_y"):
                 getattr(L, name).restype = C.c_int
             _lib = L
     return _lib
@@ -221,6 +222,19 @@ def fp8_linear(qx, sx, qw, sw, bias=None) -> np.ndarray:
                                 _ptr(sw, C.c_float), _ptr(bias, C.c_uint16), M, N, K,
                                 _ptr(y, C.c_uint16), N), "fp8_linear")
     return y
+
+
+def fp8_gateup_swiglu(qx, sx, qw_gu, sw_gu, bias_gu=None) -> np.ndarray:
+    qx, qw_gu = _c(qx, np.uint8), _c(qw_gu, np.uint8)
+    sx, sw_gu, bias_gu = _c(sx, np.float32), _c(sw_gu, np.float32), _c(bias_gu, np.uint16)
+    M, K = qx.shape
+    N = qw_gu.shape[0] // 2
+    h = np.empty((M, N), np.uint16)
+    _check(lib().orc_fp8_gateup_swiglu(_ptr(qx, C.c_uint8), _ptr(sx, C.c_float),
+                                       _ptr(qw_gu, C.c_uint8), _ptr(sw_gu, C.c_float),
+                                       _ptr(bias_gu, C.c_uint16), M, N, K,
+                                       _ptr(h, C.c_uint16), N), "fp8_gateup_swiglu")
+    return h
 
 
 # ---------------------------------------------------------------- LoRA

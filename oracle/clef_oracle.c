@@ -491,3 +491,30 @@ int orc_lora_y(const uint16_t *t, const uint16_t *B, int64_t M, int64_t N, int64
         }
     return ORC_OK;
 }
+
+/* FP8 gate/up with the paired SwiGLU epilogue (packing as the INT8 call):
+ * g, u = fp32 epilogue values of rows n and N+n of qw_gu [2N][K];
+ * h = bf16(silu(g) * u). */
+int orc_fp8_gateup_swiglu(const uint8_t *qx, const float *sx, const uint8_t *qw_gu,
+                          const float *sw_gu, const uint16_t *bias_gu,
+                          int64_t M, int64_t N, int64_t K, uint16_t *h, int64_t ldh)
+{
+    if (M < 0 || N < 0 || K <= 0 || K > 16384 || ldh < N)
+        return ORC_ERR_ARG;
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = 0; n < N; n++) {
+            float gu[2];
+            for (int half = 0; half < 2; half++) {
+                int64_t row = n + half * N;
+                double a = 0.0;
+                for (int64_t k = 0; k < K; k++)
+                    a += orc_e4m3_decode(qx[m * K + k]) * orc_e4m3_decode(qw_gu[row * K + k]);
+                float v = ((float)a * sx[m]) * sw_gu[row];
+                if (bias_gu)
+                    v = v + bf16_to_f32(bias_gu[row]);
+                gu[half] = v;
+            }
+            h[m * ldh + n] = f32_to_bf16(swiglu_f32(gu[0], gu[1]));
+        }
+    return ORC_OK;
+}

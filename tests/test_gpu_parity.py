@@ -1,0 +1,313 @@
+"""GPU parity: every CUDA entry point against the CPU oracle on the same
+seeded inputs, through the C ABI (via the thin Python binding).
+
+Bars: INT8 and e4m3 codes, scales and int32 accumulators bit-exact; INT8
+path bf16 outputs within 1 bf16 ulp (the scale/bias epilogue is asserted
+bit-exact: it runs the same rounded operations in the same order); FP8
+outputs within 1e-2 x RMS(reference) given identical codes; LoRA within the
+bound derived from fp32 accumulation (see test_lora_add)."""
+import numpy as np
+import pytest
+import torch
+
+import clef_synth as S
+import w8a8_quantized_projections_gb300 as clef
+from gpu_util import (assert_bf16_within, bf16_dev, bf16_host, bf16_ulp, dev, host, par_rows,
+                      ulp_diff)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    clef.library()
+    yield
+    assert clef.poll_status() == 0
+
+
+def special_rows(x: np.ndarray) -> np.ndarray:
+    """Row 0 all zero, row 1 one-hot, row 2 a single huge outlier."""
+    x = x.copy()
+    if x.shape[0] >= 3:
+        x[0] = 0
+        x[1] = 0
+        x[1, 5] = S.f64_to_bf16_bits(np.array([-3.25]))[0]
+        x[2, x.shape[1] // 2] = S.f64_to_bf16_bits(np.array([1.0e4]))[0]
+    return x
+
+
+# ------------------------------------------------------------------ quantizer
+
+@pytest.mark.parametrize("M,K", [(298, 2048), (1, 128), (5, 384), (130, 5120), (1502, 17408),
+                                 (2270, 6144), (3, 40960)])
+def test_quant_int8_h128_bitexact(orc, M, K):
+    x = special_rows(S.activation(0, f"t/q8/{M}x{K}", M, K))
+    q, s = clef.quant_act(bf16_dev(x), "int8_h128")
+    rq, rs = par_rows(lambda a, b: orc.quant_int8_h128(x[a:b]), M)
+    assert np.array_equal(host(s), rs)
+    assert np.array_equal(host(q), rq)
+
+
+def test_quant_strided_rows(orc):
+    M, K, ld = 37, 1024, 1536
+    big = S.activation(0, "t/q8/strided", M, ld)
+    xt = bf16_dev(big)[:, :K]
+    q, s = clef.quant_act(xt, "int8_h128")
+    rq, rs = orc.quant_int8_h128(np.ascontiguousarray(big[:, :K]))
+    assert np.array_equal(host(q), rq) and np.array_equal(host(s), rs)
+
+
+@pytest.mark.parametrize("mode", ["fp8", "fp8_h128"])
+@pytest.mark.parametrize("M,K", [(1502, 4096), (7, 12288), (33, 640), (1, 128)])
+def test_quant_fp8_bitexact(orc, mode, M, K):
+    x = special_rows(S.activation(0, f"t/q8f/{M}x{K}", M, K))
+    q, s = clef.quant_act(bf16_dev(x), mode)
+    rq, rs = par_rows(lambda a, b: orc.quant_fp8(x[a:b], rotate=(mode == "fp8_h128")), M)
+    assert np.array_equal(host(s), rs)
+    got = host(q)
+    if not np.array_equal(got, rq):
+        bad = np.argwhere(got != rq)
+        m, k = bad[0]
+        raise AssertionError(f"{len(bad)} e4m3 codes differ, first at {m},{k}: gpu {got[m, k]:#x} "
+                             f"oracle {rq[m, k]:#x}")
+
+
+def test_quant_empty_rows():
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    q, s = clef.quant_act(x, "int8_h128")
+    assert q.shape == (0, 256) and s.shape == (0,)
+
+
+# ------------------------------------------------------------------ INT8 GEMM
+
+def quantized(orc, name, M, N, K, seed=0):
+    x = S.activation(seed, f"{name}/x", M, K)
+    w = S.weight(seed, f"{name}/w", N, K)
+    b = S.bias(seed, f"{name}/b", N)
+    qx, sx = par_rows(lambda a, c: orc.quant_int8_h128(x[a:c]), M)
+    qw, sw = par_rows(lambda a, c: orc.quant_int8_h128(w[a:c]), N)
+    return x, w, b, qx, sx, qw, sw
+
+
+@pytest.mark.parametrize("M,N,K", [(298, 2048, 2048), (1, 8, 16), (130, 264, 80), (257, 512, 1088),
+                                   (129, 1024, 5120)])
+def test_int8_gemm_s32_bitexact(orc, M, N, K):
+    rng = np.random.default_rng(M * 7 + N + K)
+    qx = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    qw = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    acc = host(clef.w8a8_gemm_s32(dev(qx), dev(qw)))
+    ref = par_rows(lambda a, b: orc.int8_gemm_acc(qx[a:b], qw), M)
+    assert np.array_equal(acc, ref)
+
+
+def test_int8_gemm_s32_adversarial(orc):
+    """Sums far beyond 2^24 (the exact range of fp32) stay exact: all codes
+    +-127 over K = 17408 reach +-280,773,632."""
+    M, N, K = 130, 264, 17408
+    rng = np.random.default_rng(11)
+    qx = np.full((M, K), 127, np.int8)
+    qx[1::2] = -127
+    qx[5, :] = rng.choice(np.array([-127, 127], np.int8), K)
+    qw = np.full((N, K), 127, np.int8)
+    qw[3] = -127
+    qw[7, ::3] = -127
+    qw[9, :] = rng.integers(-127, 128, K).astype(np.int8)
+    acc = host(clef.w8a8_gemm_s32(dev(qx), dev(qw)))
+    assert acc[0, 0] == 280773632 and acc[1, 0] == -280773632
+    ref = par_rows(lambda a, b: orc.int8_gemm_acc(qx[a:b], qw), M)
+    assert np.array_equal(acc, ref)
+
+
+@pytest.mark.parametrize("M,N,K,with_bias", [(298, 2048, 2048, True), (300, 1024, 5120, False),
+                                             (5, 8, 128, True)])
+def test_w8a8_linear_bitexact(orc, M, N, K, with_bias):
+    x, w, b, qx, sx, qw, sw = quantized(orc, f"t/lin/{M}x{N}x{K}", M, N, K)
+    bias = b if with_bias else None
+    # the GPU quantizer feeds the GPU GEMM; its codes equal the oracle's (tested above)
+    gqx, gsx = clef.quant_act(bf16_dev(x), "int8_h128")
+    gqw, gsw = clef.quant_act(bf16_dev(w), "int8_h128")
+    assert np.array_equal(host(gqx), qx) and np.array_equal(host(gqw), qw)
+    y = bf16_host(clef.w8a8_linear(gqx, gsx, gqw, gsw, bf16_dev(bias) if with_bias else None))
+    ref = par_rows(lambda a, c: orc.int8_linear(qx[a:c], sx[a:c], qw, sw, bias), M)
+    assert np.array_equal(y, ref), f"max {ulp_diff(y, ref).max()} ulp"
+
+
+def test_w8a8_linear_zero_row_gives_bias(orc):
+    M, N, K = 4, 64, 256
+    x = S.activation(0, "t/zero/x", M, K)
+    x[2] = 0
+    w = S.weight(0, "t/zero/w", N, K)
+    b = S.bias(0, "t/zero/b", N)
+    qx, sx = clef.quant_act(bf16_dev(x))
+    qw, sw = clef.quant_act(bf16_dev(w))
+    y = bf16_host(clef.w8a8_linear(qx, sx, qw, sw, bf16_dev(b)))
+    assert np.array_equal(y[2], b)
+
+
+@pytest.mark.parametrize("M,N,K", [(298, 1024, 2048), (130, 136, 1024), (1, 8, 128)])
+def test_w8a8_gateup_swiglu(orc, M, N, K):
+    x, w, b, qx, sx, qw, sw = quantized(orc, f"t/gu/{M}x{N}x{K}", M, 2 * N, K)
+    h = bf16_host(clef.w8a8_gateup_swiglu(dev(qx), dev(sx), dev(qw), dev(sw), bf16_dev(b)))
+    ref = par_rows(lambda a, c: orc.int8_gateup_swiglu(qx[a:c], sx[a:c], qw, sw, b), M)
+    assert_bf16_within(h, ref, 1.0, "swiglu")
+
+
+def test_swiglu_bf16(orc):
+    M, N = 300, 1024
+    y = S.normal_bf16(0, "t/sw/y", (M, 2 * N), 3.0)
+    h = bf16_host(clef.swiglu_bf16(bf16_dev(y)))
+    ref = orc.swiglu_bf16(y)
+    assert_bf16_within(h, ref, 1.0, "swiglu_bf16")
+
+
+# ------------------------------------------------------------------ FP8 GEMM
+
+def fp8_quantized(orc, name, M, N, K):
+    x = S.activation(0, f"{name}/x", M, K)
+    w = S.weight(0, f"{name}/w", N, K)
+    b = S.bias(0, f"{name}/b", N)
+    gqx, gsx = clef.quant_act(bf16_dev(x), "fp8")
+    gqw, gsw = clef.quant_act(bf16_dev(w), "fp8")
+    qx, sx = par_rows(lambda a, c: orc.quant_fp8(x[a:c]), M)
+    qw, sw = par_rows(lambda a, c: orc.quant_fp8(w[a:c]), N)
+    assert np.array_equal(host(gqx), qx) and np.array_equal(host(gqw), qw)
+    return b, gqx, gsx, gqw, gsw, qx, sx, qw, sw
+
+
+def assert_rms_close(got_u16, ref_u16, rel=1e-2, what=""):
+    g, r = S.bf16_bits_to_f64(got_u16), S.bf16_bits_to_f64(ref_u16)
+    rms = np.sqrt(np.mean(r ** 2))
+    err = np.abs(g - r).max()
+    assert err <= rel * rms, f"{what}: max |diff| {err:.3g} > {rel} x RMS {rms:.3g}"
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 1024, 4096), (130, 264, 256), (1, 8, 128), (129, 512, 12288)])
+def test_fp8_linear(orc, M, N, K):
+    b, gqx, gsx, gqw, gsw, qx, sx, qw, sw = fp8_quantized(orc, f"t/f8/{M}x{N}x{K}", M, N, K)
+    y = bf16_host(clef.fp8_linear(gqx, gsx, gqw, gsw, bf16_dev(b)))
+    ref = par_rows(lambda a, c: orc.fp8_linear(qx[a:c], sx[a:c], qw, sw, b), M)
+    assert_rms_close(y, ref, 1e-2, "fp8_linear")
+
+
+def test_fp8_gateup_swiglu(orc):
+    M, N, K = 300, 512, 4096
+    b, gqx, gsx, gqw, gsw, qx, sx, qw, sw = fp8_quantized(orc, "t/f8gu", M, 2 * N, K)
+    h = bf16_host(clef.fp8_gateup_swiglu(gqx, gsx, gqw, gsw, bf16_dev(b)))
+    ref = par_rows(lambda a, c: orc.fp8_gateup_swiglu(qx[a:c], sx[a:c], qw, sw, b), M)
+    assert_rms_close(h, ref, 1e-2, "fp8_gateup_swiglu")
+
+
+# ------------------------------------------------------------------ LoRA
+
+def lora_bound(x_u16, A_u16, K):
+    """fp32 accumulation bound: (K/16 + 2) * 2^-23 * sum_k |x_k A_jk|."""
+    xa = np.abs(S.bf16_bits_to_f64(x_u16)) @ np.abs(S.bf16_bits_to_f64(A_u16)).T
+    return (K / 16 + 2) * 2.0 ** -23 * xa
+
+
+@pytest.mark.parametrize("M,K,N,r", [(300, 5120, 1024, 256), (130, 2048, 264, 48), (1, 128, 8, 8),
+                                     (257, 1024, 512, 128)])
+def test_lora_add(orc, M, K, N, r):
+    x = S.activation(0, f"t/lora/{M}/x", M, K)
+    A, B = S.lora_pair(0, f"t/lora/{M}", r, K, N)
+    y0 = S.normal_bf16(0, f"t/lora/{M}/y", (M, N))
+    r_pad = clef.lora_pad(r)
+    t_dev = torch.empty((M, r_pad), dtype=torch.bfloat16, device="cuda")
+    y_dev = bf16_dev(y0)
+    clef.lora_add(bf16_dev(x), bf16_dev(A), bf16_dev(B), y_dev, t_scratch=t_dev)
+    t = bf16_host(t_dev)
+    # stage 1: t within 1 ulp of the oracle plus the fp32 accumulation bound
+    t_ref = par_rows(lambda a, c: orc.lora_t(x[a:c], A), M)
+    assert np.all(t[:, r:] == 0), "padding columns of t must be exact zeros"
+    tol = bf16_ulp(S.bf16_bits_to_f64(t_ref[:, :r])) + 2 * lora_bound(x, A, K)
+    d = np.abs(S.bf16_bits_to_f64(t[:, :r]) - S.bf16_bits_to_f64(t_ref[:, :r]))
+    assert np.all(d <= tol), f"t: worst excess {(d - tol).max():.3g}"
+    # stage 2, fed the GPU's t
+    y = bf16_host(y_dev)
+    y_ref = par_rows(lambda a, c: orc.lora_y(t[a:c], B, y0[a:c]), M)
+    tol2 = bf16_ulp(S.bf16_bits_to_f64(y_ref)) + 2 * lora_bound(t, np.pad(B, ((0, 0), (0, r_pad - r))), r_pad)
+    d2 = np.abs(S.bf16_bits_to_f64(y) - S.bf16_bits_to_f64(y_ref))
+    assert np.all(d2 <= tol2), f"y: worst excess {(d2 - tol2).max():.3g}"
+
+
+def test_lora_rank48_equals_zero_padded_64(orc):
+    """A rank-48 pair and the same pair zero-padded to 64 give identical bytes."""
+    M, K, N = 64, 1024, 256
+    x = bf16_dev(S.activation(0, "t/l48/x", M, K))
+    A, B = S.lora_pair(0, "t/l48", 48, K, N)
+    y0 = S.normal_bf16(0, "t/l48/y", (M, N))
+    y48, y64 = bf16_dev(y0), bf16_dev(y0)
+    clef.lora_add(x, bf16_dev(A), bf16_dev(B), y48)
+    A64 = np.zeros((64, K), np.uint16); A64[:48] = A
+    B64 = np.zeros((N, 64), np.uint16); B64[:, :48] = B
+    clef.lora_add(x, bf16_dev(A64), bf16_dev(B64), y64)
+    assert torch.equal(y48.view(torch.int16), y64.view(torch.int16))
+
+
+# ------------------------------------------------------------------ invariances
+
+PIECES = [1, 2, 3, 5, 8, 13, 21, 34, 55, 89, 144, 255]
+
+
+def pieces(M):
+    out, a, i = [], 0, 0
+    while a < M:
+        n = min(PIECES[i % len(PIECES)], M - a)
+        out.append((a, a + n))
+        a += n
+        i += 1
+    return out
+
+
+def test_row_invariance_int8_fp8_lora():
+    """600 rows at once are byte-equal to pieces of 1..255 rows."""
+    M, N, K = 600, 512, 2048
+    x = bf16_dev(S.activation(0, "t/inv/x", M, K))
+    w = bf16_dev(S.weight(0, "t/inv/w", N, K))
+    b = bf16_dev(S.bias(0, "t/inv/b", N))
+    for mode, lin in (("int8_h128", clef.w8a8_linear), ("fp8", clef.fp8_linear)):
+        qx, sx = clef.quant_act(x, mode)
+        qw, sw = clef.quant_act(w, mode)
+        whole = lin(qx, sx, qw, sw, b)
+        part = torch.empty_like(whole)
+        for a, c in pieces(M):
+            lin(qx[a:c], sx[a:c], qw, sw, b, y=part[a:c])
+        assert torch.equal(whole.view(torch.int16), part.view(torch.int16)), mode
+    A, B = S.lora_pair(0, "t/inv/l", 256, K, N)
+    A, B = bf16_dev(A), bf16_dev(B)
+    y0 = bf16_dev(S.normal_bf16(0, "t/inv/y", (M, N)))
+    whole = y0.clone()
+    clef.lora_add(x, A, B, whole)
+    part = y0.clone()
+    for a, c in pieces(M):
+        clef.lora_add(x[a:c], A, B, part[a:c])
+    assert torch.equal(whole.view(torch.int16), part.view(torch.int16)), "lora"
+
+
+def test_two_streams_and_repeats_are_deterministic():
+    M, N, K = 1024, 2048, 4096
+    x = bf16_dev(S.activation(0, "t/det/x", M, K))
+    w = bf16_dev(S.weight(0, "t/det/w", N, K))
+    qx, sx = clef.quant_act(x)
+    qw, sw = clef.quant_act(w)
+    ref = clef.w8a8_linear(qx, sx, qw, sw)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    outs = []
+    for s in (s1, s2, s1, s2):
+        with torch.cuda.stream(s):
+            outs.append(clef.w8a8_linear(qx, sx, qw, sw))
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o.view(torch.int16), ref.view(torch.int16))
+
+
+def test_empty_calls_are_noops():
+    z8 = torch.empty((0, 256), dtype=torch.int8, device="cuda")
+    w8 = torch.zeros((64, 256), dtype=torch.int8, device="cuda")
+    s0 = torch.empty((0,), dtype=torch.float32, device="cuda")
+    sw = torch.ones((64,), dtype=torch.float32, device="cuda")
+    y = clef.w8a8_linear(z8, s0, w8, sw)
+    assert y.shape == (0, 64)

@@ -452,3 +452,19 @@ def test_lora_against_fp64_and_row_invariance(orc):
     assert np.all(np.abs(S.bf16_bits_to_f64(out) - z) <= bf16_ulp(z) * 0.5001 + 2.0 ** -23 * np.abs(z))
     pieces = np.concatenate([orc.lora_add(x[a:a + 7], A, B, y[a:a + 7]) for a in range(0, M, 7)])
     assert np.array_equal(pieces, orc.lora_add(x, A, B, y))
+
+
+def test_fp8_gateup_swiglu_matches_linear_halves(orc):
+    """The fused FP8 SwiGLU oracle agrees with silu(gate) * up formed from the
+    oracle's FP8 linear halves (which round g and u to bf16 first)."""
+    M, N, K = 3, 16, 256
+    x = S.activation(0, "pin/f8gu_x", M, K)
+    w = S.weight(0, "pin/f8gu_w", 2 * N, K)
+    qx, sx = orc.quant_fp8(x)
+    qw, sw = orc.quant_fp8(w)
+    h = S.bf16_bits_to_f64(orc.fp8_gateup_swiglu(qx, sx, qw, sw))
+    y = orc.fp8_linear(qx, sx, qw, sw)
+    g, u = S.bf16_bits_to_f64(y[:, :N]), S.bf16_bits_to_f64(y[:, N:])
+    ref = g / (1 + np.exp(-g)) * u
+    bound = 1.1 * np.abs(u) * bf16_ulp(g) + np.abs(g) * bf16_ulp(u) + 2 * bf16_ulp(ref)
+    assert np.all(np.abs(h - ref) <= bound)

@@ -1,0 +1,230 @@
+"""Python binding of the GB300 W8A8 quantized projection library (libclef.so).
+
+Argument marshalling only: every function checks tensor placement, dtype and
+layout, allocates outputs with torch when the caller passes none, and calls
+the C ABI of ``include/clef.h`` on the current CUDA stream.  All arithmetic
+runs in the library's CUDA kernels; there is no fallback path, and a missing
+library or GPU raises.
+
+bf16 tensors are ``torch.bfloat16``; INT8 codes ``torch.int8``; e4m3 codes
+``torch.uint8`` (bit patterns; ``torch.float8_e4m3fn`` inputs are accepted).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "ClefError", "library", "library_path", "quant_act", "w8a8_linear", "w8a8_gateup_swiglu",
+    "fp8_linear", "fp8_gateup_swiglu", "lora_add", "swiglu_bf16", "w8a8_gemm_s32",
+    "poll_status", "set_wait_limit_ns", "ACT_MODES",
+]
+
+ACT_MODES = {"int8_h128": 0, "fp8": 1, "fp8_h128": 2}
+_STATUS = {0: "CLEF_OK", 1: "CLEF_ERR_INVALID_ARG", 2: "CLEF_ERR_UNSUPPORTED", 3: "CLEF_ERR_CUDA",
+           4: "CLEF_ERR_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class ClefError(RuntimeError):
+    def __init__(self, call: str, status: int, detail: str = ""):
+        self.status = status
+        super().__init__(f"{call} returned {_STATUS.get(status, status)}" + (f": {detail}" if detail else ""))
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def library():
+    """The loaded libclef.so (built on first use if absent or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(f"CUDA library missing at {path}")
+            L = C.CDLL(path)
+            vp, i64, i32 = C.c_void_p, C.c_int64, C.c_int
+            sigs = {
+                "clef_quant_act": [vp, i64, i64, i64, i32, vp, vp, vp],
+                "clef_w8a8_linear": [vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp],
+                "clef_w8a8_gateup_swiglu": [vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp],
+                "clef_fp8_linear": [vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp],
+                "clef_fp8_gateup_swiglu": [vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp],
+                "clef_lora_add": [vp, i64, vp, vp, i64, i64, i64, i64, vp, vp, i64, vp],
+                "clef_swiglu_bf16": [vp, i64, i64, i64, vp, i64, vp],
+                "clef_w8a8_gemm_s32": [vp, vp, i64, i64, i64, vp, i64, vp],
+                "clef_poll_status": [],
+                "clef_abi_version": [],
+            }
+            for name, args in sigs.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = C.c_int
+            L.clef_set_wait_limit_ns.argtypes = [C.c_uint64]
+            L.clef_set_wait_limit_ns.restype = None
+            L.clef_status_string.argtypes = [C.c_int]
+            L.clef_status_string.restype = C.c_char_p
+            L.clef_last_error.argtypes = []
+            L.clef_last_error.restype = C.c_char_p
+            _lib = L
+    return _lib
+
+
+def _call(name: str, *args) -> None:
+    L = library()
+    rc = getattr(L, name)(*args)
+    if rc != 0:
+        raise ClefError(name, rc, L.clef_last_error().decode(errors="replace"))
+
+
+def _stream(t: torch.Tensor, stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream(t.device)
+    return C.c_void_p(s.cuda_stream)
+
+
+def _cuda(t: torch.Tensor, name: str, dtypes) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    return t
+
+
+def _rows(t: torch.Tensor, name: str) -> int:
+    """Row pitch of a 2-D tensor whose rows are contiguous."""
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be 2-D with contiguous rows")
+    return t.stride(0) if t.size(0) > 1 else t.size(1)
+
+
+def _dense(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _ptr(t):
+    return C.c_void_p(t.data_ptr()) if t is not None else C.c_void_p(None)
+
+
+_FP8 = (torch.uint8, torch.float8_e4m3fn)
+
+
+def quant_act(x: torch.Tensor, mode: str = "int8_h128", q=None, scale=None, stream=None):
+    """Per-token quantizer: returns (codes [M][K], scales fp32 [M])."""
+    _cuda(x, "x", (torch.bfloat16,))
+    ldx = _rows(x, "x")
+    M, K = x.shape
+    m = ACT_MODES[mode]
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.int8 if m == 0 else torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _dense(q, "q")
+    _call("clef_quant_act", _ptr(x), M, K, ldx, m, _ptr(q), _ptr(scale), _stream(x, stream))
+    return q, scale
+
+
+def _w8a8(name, codes, qx, sx, qw, sw, bias, out, n_out, stream):
+    _cuda(qx, "qx", codes)
+    _cuda(qw, "qw", codes)
+    _dense(qx, "qx"); _dense(qw, "qw")
+    _cuda(sx, "sx", (torch.float32,)); _cuda(sw, "sw", (torch.float32,))
+    if bias is not None:
+        _cuda(bias, "bias", (torch.bfloat16,))
+    M, K = qx.shape
+    if qw.shape[1] != K:
+        raise ValueError("qx and qw disagree on K")
+    if out is None:
+        out = torch.empty((M, n_out), dtype=torch.bfloat16, device=qx.device)
+    _cuda(out, "out", (torch.bfloat16,))
+    ldo = _rows(out, "out")
+    _call(name, _ptr(qx), _ptr(sx), _ptr(qw), _ptr(sw), _ptr(bias), M, n_out, K, _ptr(out), ldo,
+          _stream(qx, stream))
+    return out
+
+
+def w8a8_linear(qx, sx, qw, sw, bias=None, y=None, stream=None):
+    """y = bf16(((acc * sx) * sw) + bias) with acc the exact INT8 GEMM of qx and qw^T."""
+    return _w8a8("clef_w8a8_linear", (torch.int8,), qx, sx, qw, sw, bias, y, qw.shape[0], stream)
+
+
+def w8a8_gateup_swiglu(qx, sx, qw_gu, sw_gu, bias_gu=None, h=None, stream=None):
+    """h = bf16(silu(g) * u) for packed gate/up INT8 weights [2N][K]."""
+    return _w8a8("clef_w8a8_gateup_swiglu", (torch.int8,), qx, sx, qw_gu, sw_gu, bias_gu, h,
+                 qw_gu.shape[0] // 2, stream)
+
+
+def fp8_linear(qx, sx, qw, sw, bias=None, y=None, stream=None):
+    return _w8a8("clef_fp8_linear", _FP8, qx, sx, qw, sw, bias, y, qw.shape[0], stream)
+
+
+def fp8_gateup_swiglu(qx, sx, qw_gu, sw_gu, bias_gu=None, h=None, stream=None):
+    return _w8a8("clef_fp8_gateup_swiglu", _FP8, qx, sx, qw_gu, sw_gu, bias_gu, h,
+                 qw_gu.shape[0] // 2, stream)
+
+
+def w8a8_gemm_s32(qx, qw, acc=None, stream=None):
+    """Exact int32 accumulators of the INT8 GEMM (same kernel as w8a8_linear)."""
+    _cuda(qx, "qx", (torch.int8,)); _cuda(qw, "qw", (torch.int8,))
+    _dense(qx, "qx"); _dense(qw, "qw")
+    M, K = qx.shape
+    N = qw.shape[0]
+    if acc is None:
+        acc = torch.empty((M, N), dtype=torch.int32, device=qx.device)
+    _cuda(acc, "acc", (torch.int32,))
+    _call("clef_w8a8_gemm_s32", _ptr(qx), _ptr(qw), M, N, K, _ptr(acc), _rows(acc, "acc"),
+          _stream(qx, stream))
+    return acc
+
+
+def lora_pad(r: int) -> int:
+    return (r + 63) // 64 * 64
+
+
+def lora_add(x, A, B, y, t_scratch=None, stream=None):
+    """In place: y = bf16(y + bf16(x A^T) B^T).  Returns y."""
+    for t, n in ((x, "x"), (A, "A"), (B, "B"), (y, "y")):
+        _cuda(t, n, (torch.bfloat16,))
+    _dense(A, "A"); _dense(B, "B")
+    M, K = x.shape
+    r = A.shape[0]
+    N = B.shape[0]
+    if A.shape[1] != K or B.shape[1] != r or y.shape != (M, N):
+        raise ValueError("LoRA shapes disagree")
+    if t_scratch is None:
+        t_scratch = torch.empty((M, lora_pad(r)), dtype=torch.bfloat16, device=x.device)
+    _dense(t_scratch, "t_scratch")
+    _call("clef_lora_add", _ptr(x), _rows(x, "x"), _ptr(A), _ptr(B), M, K, N, r, _ptr(t_scratch),
+          _ptr(y), _rows(y, "y"), _stream(x, stream))
+    return y
+
+
+def swiglu_bf16(y_gu, h=None, stream=None):
+    """Unfused MLP product: h = bf16(silu(g) * u) of bf16 [M][2N] gate|up rows."""
+    _cuda(y_gu, "y_gu", (torch.bfloat16,))
+    M, N2 = y_gu.shape
+    N = N2 // 2
+    if h is None:
+        h = torch.empty((M, N), dtype=torch.bfloat16, device=y_gu.device)
+    _call("clef_swiglu_bf16", _ptr(y_gu), M, N, _rows(y_gu, "y_gu"), _ptr(h), _rows(h, "h"),
+          _stream(y_gu, stream))
+    return h
+
+
+def poll_status() -> int:
+    """Synchronise and return (then clear) the device-side status word."""
+    return int(library().clef_poll_status())
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    library().clef_set_wait_limit_ns(int(ns))

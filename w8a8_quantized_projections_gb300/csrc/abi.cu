@@ -1,0 +1,315 @@
+// abi.cu -- the extern "C" boundary declared in include/clef.h: host-side
+// argument checks (nothing is launched on a bad argument), TMA tensor maps
+// for each operand, dispatch to the kernels on the caller's stream, and the
+// library-owned device status word that time-limited device waits report to.
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/clef.h"
+#include "clef_kernels.h"
+
+namespace clef {
+
+__device__ unsigned int g_status = 0u;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    bool supported = false;
+    int num_sms = 0;
+    unsigned int *status = nullptr;  // device address of g_status on this device
+};
+
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
+thread_local char g_last_err[256] = "";
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int cuda_fail(cudaError_t e, const char *what) {
+    snprintf(g_last_err, sizeof g_last_err, "%s: %s", what, cudaGetErrorString(e));
+    return CLEF_ERR_CUDA;
+}
+
+int arg_fail(const char *what) {
+    snprintf(g_last_err, sizeof g_last_err, "invalid argument: %s", what);
+    return CLEF_ERR_INVALID_ARG;
+}
+
+// Device checks and per-device set-up (status-word address, SM count).
+int device_state(DeviceState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return arg_fail("device index");
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+            return cuda_fail(e, "compute capability");
+        if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return cuda_fail(e, "compute capability");
+        d.supported = (major == 10 && minor == 3);
+        if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "SM count");
+        if (d.supported) {
+            void *p = nullptr;
+            if ((e = cudaGetSymbolAddress(&p, g_status)) != cudaSuccess)
+                return cuda_fail(e, "status word address");
+            d.status = static_cast<unsigned int *>(p);
+        }
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                return cuda_fail(e == cudaSuccess ? cudaErrorNotSupported : e, "cuTensorMapEncodeTiled");
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        d.ready = true;
+    }
+    if (!d.supported) {
+        snprintf(g_last_err, sizeof g_last_err, "device %d is not sm_103 (GB300)", dev);
+        return CLEF_ERR_UNSUPPORTED;
+    }
+    *out = &d;
+    return CLEF_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D tensor map over a row-major [rows][inner] tensor with the given row
+// pitch; zero fill outside the tensor.
+int make_tmap(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
+              uint64_t rows, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows,
+              CUtensorMapSwizzle sw) {
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {pitch_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_err, sizeof g_last_err, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+        return CLEF_ERR_INVALID_ARG;
+    }
+    return CLEF_OK;
+}
+
+GemmArgs base_args(const DeviceState *d, int64_t M, int64_t N, int64_t K) {
+    GemmArgs a;
+    memset(&a, 0, sizeof a);
+    a.M = (int)M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.status = d->status;
+    a.wait_limit_ns = g_wait_limit_ns.load();
+    return a;
+}
+
+constexpr int64_t kMaxDim = (int64_t)1 << 30;
+
+// Shared checks of the W8A8 GEMM entry points.  b_rows is the row count of
+// the weight operand; out_elem the output element size.
+int check_gemm(const void *qx, const float *sx, const void *qw, const float *sw, const void *bias,
+               int64_t M, int64_t N, int64_t K, const void *out, int64_t ldo, bool scaled) {
+    if (!qx || !qw || !out) return arg_fail("null operand or output pointer");
+    if (scaled && (!sx || !sw)) return arg_fail("null scale pointer");
+    if (M < 0 || M > kMaxDim) return arg_fail("M out of range");
+    if (N <= 0 || N > kMaxDim || N % 8 != 0) return arg_fail("N must be positive and a multiple of 8");
+    if (K <= 0 || K > kMaxDim || K % 16 != 0) return arg_fail("K must be positive and a multiple of 16");
+    if (ldo < N || ldo % 8 != 0) return arg_fail("output row pitch must be >= N and a multiple of 8");
+    if (!aligned16(qx) || !aligned16(qw) || !aligned16(out)) return arg_fail("operand/output not 16-byte aligned");
+    if (scaled && (!aligned16(sw) || (reinterpret_cast<uintptr_t>(sx) & 3u)))
+        return arg_fail("weight scales must be 16-byte aligned, row scales 4-byte aligned");
+    if (bias && (reinterpret_cast<uintptr_t>(bias) & 1u)) return arg_fail("bias not 2-byte aligned");
+    return CLEF_OK;
+}
+
+int run_w8a8(int op, int epi, const void *qx, const float *sx, const void *qw, const float *sw,
+             const void *bias, int64_t M, int64_t N, int64_t K, void *out, int64_t ldo,
+             void *stream) {
+    const bool swiglu = (epi == kEpiSwiGLU);
+    int rc = check_gemm(qx, sx, qw, sw, bias, M, N, K, out, ldo, epi != kEpiStoreS32);
+    if (rc) return rc;
+    if (swiglu && 2 * N > kMaxDim) return arg_fail("2N out of range");
+    DeviceState *d = nullptr;
+    if ((rc = device_state(&d))) return rc;
+    if (M == 0) return CLEF_OK;
+    const bool i8 = (op == kOpI8);
+    const uint32_t box_k = i8 ? 64 : 128;  // int8 raw 64 B rows; e4m3 128 B swizzled rows
+    const CUtensorMapSwizzle swz = i8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+    const uint64_t b_rows = swiglu ? 2 * (uint64_t)N : (uint64_t)N;
+    CUtensorMap ta, tb;
+    if ((rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, qx, K, M, K, box_k, 128, swz))) return rc;
+    if ((rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, K, b_rows, K, box_k, swiglu ? 128 : 256, swz)))
+        return rc;
+    GemmArgs a = base_args(d, M, N, K);
+    a.n_half = swiglu ? (int)N : 0;
+    a.sa = sx;
+    a.sb = sw;
+    a.bias = static_cast<const uint16_t *>(bias);
+    a.out = out;
+    a.ldo = ldo;
+    cudaError_t e = launch_gemm(op, epi, 256, ta, tb, a, d->num_sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CLEF_OK : cuda_fail(e, "gemm launch");
+}
+
+}  // namespace
+}  // namespace clef
+
+using namespace clef;
+
+extern "C" {
+
+int clef_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, int mode, void *q,
+                   float *scale, void *stream) {
+    if (!x || !q || !scale) return arg_fail("null pointer");
+    if (mode != CLEF_ACT_INT8_H128 && mode != CLEF_ACT_FP8_E4M3 && mode != CLEF_ACT_FP8_E4M3_H128)
+        return arg_fail("unknown quantizer mode");
+    if (M < 0 || M > 0x7FFFFFFF) return arg_fail("M out of range");
+    const bool rot = (mode != CLEF_ACT_FP8_E4M3);
+    if (K <= 0 || K > 65536 || K % (rot ? 128 : 32) != 0)
+        return arg_fail("K must be in (0, 65536] and a multiple of 128 (rotated) or 32");
+    if (ldx < K || ldx % 8 != 0) return arg_fail("ldx must be >= K and a multiple of 8");
+    if (!aligned16(x) || !aligned16(q)) return arg_fail("x and q must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(scale) & 3u) return arg_fail("scale not 4-byte aligned");
+    DeviceState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc) return rc;
+    if (M == 0) return CLEF_OK;
+    cudaError_t e = launch_quant_act(mode, static_cast<const uint16_t *>(x), M, K, ldx,
+                                     static_cast<uint8_t *>(q), scale, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CLEF_OK : cuda_fail(e, "quantizer launch");
+}
+
+int clef_w8a8_linear(const int8_t *qx, const float *sx, const int8_t *qw, const float *sw,
+                     const void *bias, int64_t M, int64_t N, int64_t K, void *y, int64_t ldy,
+                     void *stream) {
+    return run_w8a8(kOpI8, kEpiScaleBias, qx, sx, qw, sw, bias, M, N, K, y, ldy, stream);
+}
+
+int clef_w8a8_gateup_swiglu(const int8_t *qx, const float *sx, const int8_t *qw_gu,
+                            const float *sw_gu, const void *bias_gu, int64_t M, int64_t N,
+                            int64_t K, void *h, int64_t ldh, void *stream) {
+    return run_w8a8(kOpI8, kEpiSwiGLU, qx, sx, qw_gu, sw_gu, bias_gu, M, N, K, h, ldh, stream);
+}
+
+int clef_fp8_linear(const void *qx, const float *sx, const void *qw, const float *sw,
+                    const void *bias, int64_t M, int64_t N, int64_t K, void *y, int64_t ldy,
+                    void *stream) {
+    return run_w8a8(kOpF8, kEpiScaleBias, qx, sx, qw, sw, bias, M, N, K, y, ldy, stream);
+}
+
+int clef_fp8_gateup_swiglu(const void *qx, const float *sx, const void *qw_gu, const float *sw_gu,
+                           const void *bias_gu, int64_t M, int64_t N, int64_t K, void *h,
+                           int64_t ldh, void *stream) {
+    return run_w8a8(kOpF8, kEpiSwiGLU, qx, sx, qw_gu, sw_gu, bias_gu, M, N, K, h, ldh, stream);
+}
+
+int clef_w8a8_gemm_s32(const int8_t *qx, const int8_t *qw, int64_t M, int64_t N, int64_t K,
+                       int32_t *acc, int64_t ldc, void *stream) {
+    return run_w8a8(kOpI8, kEpiStoreS32, qx, nullptr, qw, nullptr, nullptr, M, N, K, acc, ldc, stream);
+}
+
+int clef_lora_add(const void *x, int64_t ldx, const void *A, const void *B, int64_t M, int64_t K,
+                  int64_t N, int64_t r, void *t_scratch, void *y, int64_t ldy, void *stream) {
+    if (!x || !A || !B || !t_scratch || !y) return arg_fail("null pointer");
+    if (M < 0 || M > kMaxDim) return arg_fail("M out of range");
+    if (K <= 0 || K > kMaxDim || K % 8 != 0) return arg_fail("K must be positive and a multiple of 8");
+    if (N <= 0 || N > kMaxDim || N % 8 != 0) return arg_fail("N must be positive and a multiple of 8");
+    if (r <= 0 || r > 1024 || r % 8 != 0) return arg_fail("rank must be in (0, 1024] and a multiple of 8");
+    if (ldx < K || ldx % 8 != 0) return arg_fail("ldx must be >= K and a multiple of 8");
+    if (ldy < N || ldy % 8 != 0) return arg_fail("ldy must be >= N and a multiple of 8");
+    if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(t_scratch) || !aligned16(y))
+        return arg_fail("pointers must be 16-byte aligned");
+    DeviceState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc) return rc;
+    if (M == 0) return CLEF_OK;
+    const int64_t r_pad = (r + 63) / 64 * 64;
+    const int bn = r_pad == 64 ? 64 : (r_pad == 128 ? 128 : 256);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CUtensorMap tx, ta, tt, tbm;
+    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    // stage 1: t = bf16(x A^T), [M][r_pad]; rows of A past r read as zeros
+    if ((rc = make_tmap(&tx, bf, x, K, M, ldx * 2, 64, 128, sw))) return rc;
+    if ((rc = make_tmap(&ta, bf, A, K, r, K * 2, 64, bn, sw))) return rc;
+    GemmArgs a1 = base_args(d, M, r_pad, K);
+    a1.out = t_scratch;
+    a1.ldo = r_pad;
+    cudaError_t e = launch_gemm(kOpBF16, kEpiStoreBF16, bn, tx, ta, a1, d->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "lora stage 1 launch");
+    // stage 2: y = bf16(y + t B^T); columns of B past r read as zeros
+    if ((rc = make_tmap(&tt, bf, t_scratch, r_pad, M, r_pad * 2, 64, 128, sw))) return rc;
+    if ((rc = make_tmap(&tbm, bf, B, r, N, r * 2, 64, 256, sw))) return rc;
+    GemmArgs a2 = base_args(d, M, N, r_pad);
+    a2.out = y;
+    a2.ldo = ldy;
+    e = launch_gemm(kOpBF16, kEpiAddBF16, 256, tt, tbm, a2, d->num_sms, st);
+    return e == cudaSuccess ? CLEF_OK : cuda_fail(e, "lora stage 2 launch");
+}
+
+int clef_swiglu_bf16(const void *y_gu, int64_t M, int64_t N, int64_t ldg, void *h, int64_t ldh,
+                     void *stream) {
+    if (!y_gu || !h) return arg_fail("null pointer");
+    if (M < 0 || M > kMaxDim) return arg_fail("M out of range");
+    if (N <= 0 || N > kMaxDim || N % 8 != 0) return arg_fail("N must be positive and a multiple of 8");
+    if (ldg < 2 * N || ldg % 8 != 0) return arg_fail("ldg must be >= 2N and a multiple of 8");
+    if (ldh < N || ldh % 8 != 0) return arg_fail("ldh must be >= N and a multiple of 8");
+    if (!aligned16(y_gu) || !aligned16(h)) return arg_fail("pointers must be 16-byte aligned");
+    DeviceState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc) return rc;
+    if (M == 0) return CLEF_OK;
+    cudaError_t e = launch_swiglu_bf16(static_cast<const uint16_t *>(y_gu), M, N, ldg,
+                                       static_cast<uint16_t *>(h), ldh, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CLEF_OK : cuda_fail(e, "swiglu launch");
+}
+
+int clef_poll_status(void) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    unsigned int w = 0, zero = 0;
+    if ((e = cudaMemcpyFromSymbol(&w, g_status, sizeof w)) != cudaSuccess) return cuda_fail(e, "read status");
+    if ((e = cudaMemcpyToSymbol(g_status, &zero, sizeof zero)) != cudaSuccess) return cuda_fail(e, "clear status");
+    if (w) snprintf(g_last_err, sizeof g_last_err, "device status word 0x%08x (site %u)", w, (w >> 8) & 0xFFu);
+    return (int)(w & 0xFFu);
+}
+
+void clef_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
+
+const char *clef_status_string(int status) {
+    switch (status) {
+        case CLEF_OK: return "CLEF_OK";
+        case CLEF_ERR_INVALID_ARG: return "CLEF_ERR_INVALID_ARG";
+        case CLEF_ERR_UNSUPPORTED: return "CLEF_ERR_UNSUPPORTED";
+        case CLEF_ERR_CUDA: return "CLEF_ERR_CUDA";
+        case CLEF_ERR_TIMEOUT: return "CLEF_ERR_TIMEOUT";
+        default: return "CLEF_ERR_UNKNOWN";
+    }
+}
+
+const char *clef_last_error(void) { return g_last_err; }
+
+int clef_abi_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// clef_kernels.h -- internal launchers shared by the C-ABI layer (abi.cu)
+// and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace clef {
+
+enum ActMode : int { kActInt8H128 = 0, kActFp8 = 1, kActFp8H128 = 2 };
+
+cudaError_t launch_quant_act(int mode, const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                             uint8_t *q, float *scale, cudaStream_t st);
+
+// Operand kinds of the tensor-core GEMM.
+enum GemmOp : int {
+    kOpI8 = 0,    // int8 codes in HBM, widened to fp16 on chip, exact chunked accumulation
+    kOpF8 = 1,    // e4m3 codes, kind::f8f6f4
+    kOpBF16 = 2,  // bf16 operands, kind::f16
+};
+
+// Epilogues.
+enum GemmEpi : int {
+    kEpiScaleBias = 0,  // y = bf16((acc * sa[m]) * sb[n] + bias[n])
+    kEpiSwiGLU = 1,     // h = bf16(silu(g) * u), g/u from the two halves of the tile
+    kEpiStoreBF16 = 2,  // t = bf16(acc)
+    kEpiAddBF16 = 3,    // y = bf16(float(y) + acc), y read and written
+    kEpiStoreS32 = 4,   // acc as int32 (INT8 operands only)
+};
+
+struct GemmArgs {
+    int M, N, K;             // output rows, output columns (h columns for SwiGLU), depth
+    int n_half;              // SwiGLU: row offset of the up half inside the packed B operand
+    const float *sa;         // per-row scale [M]
+    const float *sb;         // per-column scale (packed order for SwiGLU)
+    const uint16_t *bias;    // bf16, may be null
+    void *out;               // bf16 or int32 output
+    int64_t ldo;             // output row pitch (elements)
+    unsigned int *status;    // device status word
+    uint64_t wait_limit_ns;
+};
+
+// A: [M][K] operand rows, B: [rows][K]; tensor maps are built by the caller
+// for the operand kind (see abi.cu).  bn selects the tile width.
+cudaError_t launch_gemm(int op, int epi, int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                        const GemmArgs &args, int num_sms, cudaStream_t st);
+
+// Smem bytes a (op, bn) instantiation needs (host side, for the attribute).
+int gemm_smem_bytes(int op, int bn);
+
+cudaError_t launch_swiglu_bf16(const uint16_t *y_gu, int64_t M, int64_t N, int64_t ldg,
+                               uint16_t *h, int64_t ldh, cudaStream_t st);
+
+}  // namespace clef
