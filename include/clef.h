@@ -24,7 +24,8 @@
  *    or CLEF_ERR_CUDA when a launch fails.  Device-side waits that exceed
  *    their time limit record CLEF_ERR_TIMEOUT in a library-owned status word
  *    read by clef_poll_status(); the kernels never trap.
- *  - M = 0 is a valid empty call: it returns CLEF_OK without a launch.
+ *  - M = 0 is a valid empty call: it returns CLEF_OK without a launch (its
+ *    row-indexed pointers may then be null, as those of empty tensors are).
  *  - Inputs are assumed finite; NaN/Inf inputs give unspecified codes.
  *  - Alignment: every tensor base and every row pitch must be a multiple of
  *    16 bytes (TMA and vector-access rule); the checks below state it per

@@ -177,10 +177,18 @@ def fp8_quantized(orc, name, M, N, K):
 
 
 def assert_rms_close(got_u16, ref_u16, rel=1e-2, what=""):
+    """FP8 bar: |gpu - oracle| <= rel * RMS(oracle) + 1 bf16 ulp(oracle).  The
+    RMS term bounds the accumulation-order difference; the ulp term is the
+    final bf16 rounding, which may fall either way once the fp32 values differ
+    (at |y| >= 4 one ulp, 2^-5, already exceeds 1e-2 * RMS for RMS < 3.1)."""
     g, r = S.bf16_bits_to_f64(got_u16), S.bf16_bits_to_f64(ref_u16)
     rms = np.sqrt(np.mean(r ** 2))
-    err = np.abs(g - r).max()
-    assert err <= rel * rms, f"{what}: max |diff| {err:.3g} > {rel} x RMS {rms:.3g}"
+    d = np.abs(g - r)
+    excess = d - (rel * rms + bf16_ulp(r))
+    assert np.all(excess <= 0), (f"{what}: {int((excess > 0).sum())} outside, max |diff| {d.max():.3g}, "
+                                 f"RMS {rms:.3g}")
+    # and the accumulation difference itself is small: nearly all within one ulp
+    assert np.mean(d > bf16_ulp(r)) < 1e-3, f"{what}: {np.mean(d > bf16_ulp(r)):.2e} beyond 1 ulp"
 
 
 @pytest.mark.parametrize("M,N,K", [(300, 1024, 4096), (130, 264, 256), (1, 8, 128), (129, 512, 12288)])

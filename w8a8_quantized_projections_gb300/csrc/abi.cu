@@ -128,14 +128,19 @@ constexpr int64_t kMaxDim = (int64_t)1 << 30;
 
 // Shared checks of the W8A8 GEMM entry points.  b_rows is the row count of
 // the weight operand; out_elem the output element size.
+// Returns CLEF_OK with *empty = true for a valid M = 0 call (whose row-indexed
+// pointers may be null, as empty tensors' are).
 int check_gemm(const void *qx, const float *sx, const void *qw, const float *sw, const void *bias,
-               int64_t M, int64_t N, int64_t K, const void *out, int64_t ldo, bool scaled) {
-    if (!qx || !qw || !out) return arg_fail("null operand or output pointer");
-    if (scaled && (!sx || !sw)) return arg_fail("null scale pointer");
+               int64_t M, int64_t N, int64_t K, const void *out, int64_t ldo, bool scaled,
+               bool *empty) {
     if (M < 0 || M > kMaxDim) return arg_fail("M out of range");
     if (N <= 0 || N > kMaxDim || N % 8 != 0) return arg_fail("N must be positive and a multiple of 8");
     if (K <= 0 || K > kMaxDim || K % 16 != 0) return arg_fail("K must be positive and a multiple of 16");
     if (ldo < N || ldo % 8 != 0) return arg_fail("output row pitch must be >= N and a multiple of 8");
+    *empty = (M == 0);
+    if (*empty) return CLEF_OK;
+    if (!qx || !qw || !out) return arg_fail("null operand or output pointer");
+    if (scaled && (!sx || !sw)) return arg_fail("null scale pointer");
     if (!aligned16(qx) || !aligned16(qw) || !aligned16(out)) return arg_fail("operand/output not 16-byte aligned");
     if (scaled && (!aligned16(sw) || (reinterpret_cast<uintptr_t>(sx) & 3u)))
         return arg_fail("weight scales must be 16-byte aligned, row scales 4-byte aligned");
@@ -147,12 +152,12 @@ int run_w8a8(int op, int epi, const void *qx, const float *sx, const void *qw, c
              const void *bias, int64_t M, int64_t N, int64_t K, void *out, int64_t ldo,
              void *stream) {
     const bool swiglu = (epi == kEpiSwiGLU);
-    int rc = check_gemm(qx, sx, qw, sw, bias, M, N, K, out, ldo, epi != kEpiStoreS32);
-    if (rc) return rc;
+    bool empty = false;
+    int rc = check_gemm(qx, sx, qw, sw, bias, M, N, K, out, ldo, epi != kEpiStoreS32, &empty);
+    if (rc || empty) return rc;
     if (swiglu && 2 * N > kMaxDim) return arg_fail("2N out of range");
     DeviceState *d = nullptr;
     if ((rc = device_state(&d))) return rc;
-    if (M == 0) return CLEF_OK;
     const bool i8 = (op == kOpI8);
     const uint32_t box_k = i8 ? 64 : 128;  // int8 raw 64 B rows; e4m3 128 B swizzled rows
     const CUtensorMapSwizzle swz = i8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
@@ -181,7 +186,6 @@ extern "C" {
 
 int clef_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, int mode, void *q,
                    float *scale, void *stream) {
-    if (!x || !q || !scale) return arg_fail("null pointer");
     if (mode != CLEF_ACT_INT8_H128 && mode != CLEF_ACT_FP8_E4M3 && mode != CLEF_ACT_FP8_E4M3_H128)
         return arg_fail("unknown quantizer mode");
     if (M < 0 || M > 0x7FFFFFFF) return arg_fail("M out of range");
@@ -189,12 +193,13 @@ int clef_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, int mode, v
     if (K <= 0 || K > 65536 || K % (rot ? 128 : 32) != 0)
         return arg_fail("K must be in (0, 65536] and a multiple of 128 (rotated) or 32");
     if (ldx < K || ldx % 8 != 0) return arg_fail("ldx must be >= K and a multiple of 8");
+    if (M == 0) return CLEF_OK;
+    if (!x || !q || !scale) return arg_fail("null pointer");
     if (!aligned16(x) || !aligned16(q)) return arg_fail("x and q must be 16-byte aligned");
     if (reinterpret_cast<uintptr_t>(scale) & 3u) return arg_fail("scale not 4-byte aligned");
     DeviceState *d = nullptr;
     int rc = device_state(&d);
     if (rc) return rc;
-    if (M == 0) return CLEF_OK;
     cudaError_t e = launch_quant_act(mode, static_cast<const uint16_t *>(x), M, K, ldx,
                                      static_cast<uint8_t *>(q), scale, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CLEF_OK : cuda_fail(e, "quantizer launch");
@@ -231,19 +236,19 @@ int clef_w8a8_gemm_s32(const int8_t *qx, const int8_t *qw, int64_t M, int64_t N,
 
 int clef_lora_add(const void *x, int64_t ldx, const void *A, const void *B, int64_t M, int64_t K,
                   int64_t N, int64_t r, void *t_scratch, void *y, int64_t ldy, void *stream) {
-    if (!x || !A || !B || !t_scratch || !y) return arg_fail("null pointer");
     if (M < 0 || M > kMaxDim) return arg_fail("M out of range");
     if (K <= 0 || K > kMaxDim || K % 8 != 0) return arg_fail("K must be positive and a multiple of 8");
     if (N <= 0 || N > kMaxDim || N % 8 != 0) return arg_fail("N must be positive and a multiple of 8");
     if (r <= 0 || r > 1024 || r % 8 != 0) return arg_fail("rank must be in (0, 1024] and a multiple of 8");
     if (ldx < K || ldx % 8 != 0) return arg_fail("ldx must be >= K and a multiple of 8");
     if (ldy < N || ldy % 8 != 0) return arg_fail("ldy must be >= N and a multiple of 8");
+    if (M == 0) return CLEF_OK;
+    if (!x || !A || !B || !t_scratch || !y) return arg_fail("null pointer");
     if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(t_scratch) || !aligned16(y))
         return arg_fail("pointers must be 16-byte aligned");
     DeviceState *d = nullptr;
     int rc = device_state(&d);
     if (rc) return rc;
-    if (M == 0) return CLEF_OK;
     const int64_t r_pad = (r + 63) / 64 * 64;
     const int bn = r_pad == 64 ? 64 : (r_pad == 128 ? 128 : 256);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -270,16 +275,16 @@ int clef_lora_add(const void *x, int64_t ldx, const void *A, const void *B, int6
 
 int clef_swiglu_bf16(const void *y_gu, int64_t M, int64_t N, int64_t ldg, void *h, int64_t ldh,
                      void *stream) {
-    if (!y_gu || !h) return arg_fail("null pointer");
     if (M < 0 || M > kMaxDim) return arg_fail("M out of range");
     if (N <= 0 || N > kMaxDim || N % 8 != 0) return arg_fail("N must be positive and a multiple of 8");
     if (ldg < 2 * N || ldg % 8 != 0) return arg_fail("ldg must be >= 2N and a multiple of 8");
     if (ldh < N || ldh % 8 != 0) return arg_fail("ldh must be >= N and a multiple of 8");
+    if (M == 0) return CLEF_OK;
+    if (!y_gu || !h) return arg_fail("null pointer");
     if (!aligned16(y_gu) || !aligned16(h)) return arg_fail("pointers must be 16-byte aligned");
     DeviceState *d = nullptr;
     int rc = device_state(&d);
     if (rc) return rc;
-    if (M == 0) return CLEF_OK;
     cudaError_t e = launch_swiglu_bf16(static_cast<const uint16_t *>(y_gu), M, N, ldg,
                                        static_cast<uint16_t *>(h), ldh, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CLEF_OK : cuda_fail(e, "swiglu launch");
