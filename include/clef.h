@@ -174,6 +174,28 @@ int clef_w8a8_gemm_s32(const int8_t *qx, const int8_t *qw, int64_t M, int64_t N,
                        int32_t *acc, int64_t ldc, void *stream);
 
 /*
+ * clef_lora_add_noalloc -- the same LoRA add as clef_lora_add, without the
+ * t_scratch argument, for callers that cannot allocate device memory: a host
+ * whose runtime owns a fixed device-memory budget and forbids allocations
+ * outside it, a plugin living inside another framework's allocator, or code
+ * that must not pay the device-wide synchronisation cudaMalloc/cudaFree can
+ * imply.  The pages have no counterpart of this call; it is a library
+ * convenience.
+ * t lives in a library-owned static device array of 4,194,304 bf16 elements
+ * (8 MiB, held by every GPU that loads the library until exit):
+ * M * round_up(r, 64) beyond that returns CLEF_ERR_INVALID_ARG.  The call
+ * allocates nothing.  Its first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls share the array and it keeps the
+ * previous call's contents (nothing needs clearing: each call rewrites every
+ * element it reads), so calls whose kernels may overlap on the GPU race and
+ * must be serialised.  Other arguments and requirements as clef_lora_add.
+ */
+int clef_lora_add_noalloc(const void *x, int64_t ldx, const void *A, const void *B,
+                          int64_t M, int64_t K, int64_t N, int64_t r,
+                          void *y, int64_t ldy, void *stream);
+
+/*
  * clef_poll_status -- synchronises the device, then returns and clears the
  * device-side status word (CLEF_OK if no kernel recorded an error).
  */

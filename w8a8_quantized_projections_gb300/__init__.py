@@ -21,7 +21,7 @@ from . import build as _build
 
 __all__ = [
     "ClefError", "library", "library_path", "quant_act", "w8a8_linear", "w8a8_gateup_swiglu",
-    "fp8_linear", "fp8_gateup_swiglu", "lora_add", "swiglu_bf16", "w8a8_gemm_s32",
+    "fp8_linear", "fp8_gateup_swiglu", "lora_add", "lora_add_noalloc", "swiglu_bf16", "w8a8_gemm_s32",
     "poll_status", "set_wait_limit_ns", "ACT_MODES",
 ]
 
@@ -60,6 +60,7 @@ def library():
                 "clef_fp8_linear": [vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp],
                 "clef_fp8_gateup_swiglu": [vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp],
                 "clef_lora_add": [vp, i64, vp, vp, i64, i64, i64, i64, vp, vp, i64, vp],
+                "clef_lora_add_noalloc": [vp, i64, vp, vp, i64, i64, i64, i64, vp, i64, vp],
                 "clef_swiglu_bf16": [vp, i64, i64, i64, vp, i64, vp],
                 "clef_w8a8_gemm_s32": [vp, vp, i64, i64, i64, vp, i64, vp],
                 "clef_poll_status": [],
@@ -205,6 +206,22 @@ def lora_add(x, A, B, y, t_scratch=None, stream=None):
         t_scratch = torch.empty((M, lora_pad(r)), dtype=torch.bfloat16, device=x.device)
     _dense(t_scratch, "t_scratch")
     _call("clef_lora_add", _ptr(x), _rows(x, "x"), _ptr(A), _ptr(B), M, K, N, r, _ptr(t_scratch),
+          _ptr(y), _rows(y, "y"), _stream(x, stream))
+    return y
+
+
+def lora_add_noalloc(x, A, B, y, stream=None):
+    """In place: y = bf16(y + bf16(x A^T) B^T), with t kept in the library's
+    built-in device scratch (for callers that cannot allocate).  Returns y."""
+    for t, n in ((x, "x"), (A, "A"), (B, "B"), (y, "y")):
+        _cuda(t, n, (torch.bfloat16,))
+    _dense(A, "A"); _dense(B, "B")
+    M, K = x.shape
+    r = A.shape[0]
+    N = B.shape[0]
+    if A.shape[1] != K or B.shape[1] != r or y.shape != (M, N):
+        raise ValueError("LoRA shapes disagree")
+    _call("clef_lora_add_noalloc", _ptr(x), _rows(x, "x"), _ptr(A), _ptr(B), M, K, N, r,
           _ptr(y), _rows(y, "y"), _stream(x, stream))
     return y
 

@@ -178,6 +178,25 @@ int run_w8a8(int op, int epi, const void *qx, const float *sx, const void *qw, c
 }
 
 }  // namespace
+
+// Internal services for other translation units of this library.
+int internal_device(int *num_sms, unsigned int **status) {
+    DeviceState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc) return rc;
+    *num_sms = d->num_sms;
+    *status = d->status;
+    return CLEF_OK;
+}
+
+int internal_make_tmap_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
+                            uint64_t pitch_bytes, uint32_t box_rows) {
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, rows, pitch_bytes, 64,
+                     box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+void internal_set_error(const char *msg) { snprintf(g_last_err, sizeof g_last_err, "%s", msg); }
+
 }  // namespace clef
 
 using namespace clef;

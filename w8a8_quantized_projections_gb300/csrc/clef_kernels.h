@@ -52,4 +52,12 @@ int gemm_smem_bytes(int op, int bn);
 cudaError_t launch_swiglu_bf16(const uint16_t *y_gu, int64_t M, int64_t N, int64_t ldg,
                                uint16_t *h, int64_t ldh, cudaStream_t st);
 
+// Services of abi.cu for other translation units: per-device checks and
+// set-up (SM count, status-word address), 128B-swizzled bf16 tensor maps with
+// 64-element boxes, and the calling thread's last-error text.
+int internal_device(int *num_sms, unsigned int **status);
+int internal_make_tmap_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
+                            uint64_t pitch_bytes, uint32_t box_rows);
+void internal_set_error(const char *msg);
+
 }  // namespace clef
