@@ -58,9 +58,11 @@ struct Cfg {
     // Raw int8 k-block (INT8 only): 64 codes = 64 bytes per row, no swizzle.
     static constexpr int kRawA = BM * 64, kRawB = BN * 64, kRawStage = kRawA + kRawB;
     static constexpr int kSmemBudget = 232448 - 1024 - 512;  // opt-in max - align slack - barriers
-    static constexpr int NRAW = kI8 ? 3 : 0;
+    // INT8: two fp16 operand stages (converter -> MMA hand-off) and five raw
+    // int8 stages (enough TMA lookahead to cover L2/HBM latency).
+    static constexpr int NRAW = kI8 ? 5 : 0;
     static constexpr int NSTAGE_RAWFREE = (kSmemBudget - NRAW * kRawStage) / kStage;
-    static constexpr int NSTAGE = kI8 ? 3 : (NSTAGE_RAWFREE > 8 ? 8 : NSTAGE_RAWFREE);
+    static constexpr int NSTAGE = kI8 ? 2 : (NSTAGE_RAWFREE > 8 ? 8 : NSTAGE_RAWFREE);
     static constexpr int kChunkKBlocks = kI8 ? 16 : (1 << 30);  // 1024 K per exact chunk
     static constexpr int kConvWarps = kI8 ? 6 : 0;
     static constexpr int kEpiWarp0 = kI8 ? 8 : 4;
@@ -80,7 +82,7 @@ struct Cfg {
 
 struct Barriers {
     uint64_t full[8], empty[8];
-    uint64_t raw_full[4], raw_empty[4];
+    uint64_t raw_full[6], raw_empty[6];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t drain;
     uint32_t tmem_slot;
@@ -122,6 +124,18 @@ __device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t
     const uint32_t u = w ^ 0x80808080u;
     lo = sub_f16x2(prmt(u, 0x64646464u, 0x4140u), 0x64806480u);
     hi = sub_f16x2(prmt(u, 0x64646464u, 0x4342u), 0x64806480u);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -170,6 +184,7 @@ struct Gemm {
     // ---------------------------------------------------------------- producer
     static __device__ void producer(const Ctx &c, const CUtensorMap *tmA, const CUtensorMap *tmB,
                                     const GemmArgs &a, uint32_t (&fills)[8]) {
+        static_assert(C::NRAW <= 8 && C::NSTAGE <= 8, "fill bookkeeping");
         uint32_t s = 0, ph = 0;
         const int nstage = C::kI8 ? C::NRAW : C::NSTAGE;
         for (int t = blockIdx.x; t < c.num_tiles; t += gridDim.x) {
@@ -223,34 +238,47 @@ struct Gemm {
     }
 
     // ---------------------------------------------------------------- converters
+    // Each converter thread owns the same 16-byte raw pieces in every k-block:
+    // piece = ctid & 3 of rows (ctid >> 2) + 48 j, j = 0..7 (A rows 0..127,
+    // then B rows).  Because 48 is a multiple of 8, the 128-byte swizzle phase
+    // (row & 7) of a thread's rows is constant, so all shared addresses are a
+    // per-thread base plus compile-time offsets.
     static __device__ void converter(const Ctx &c, int ctid) {
-        uint32_t rs = 0, rph = 0, cs = 0, cph = 0;
+        constexpr int kThr = (C::kI8 ? C::kConvWarps : 6) * 32;  // native ops never call this
         constexpr int kRows = C::BM + BN;
-        constexpr int kTasks = kRows * 4;  // 16-byte raw pieces per k-block
+        constexpr int kPer = kRows * 4 / kThr;
+        static_assert(!C::kI8 || kRows * 4 % kThr == 0, "converter tasks");
+        static_assert(!C::kI8 || (kThr / 4) % 8 == 0, "constant swizzle phase");
+        constexpr uint32_t kSrcStep = (kThr / 4) * 64, kDstStep = (kThr / 4) * 128;
+        const int row0 = ctid >> 2, piece = ctid & 3, phase = row0 & 7;
+        const uint32_t src0 = (uint32_t)(row0 * 64 + piece * 16);
+        const uint32_t dst0 = (uint32_t)(row0 * 128 + (((2 * piece) ^ phase) << 4));
+        const uint32_t dst1 = (uint32_t)(row0 * 128 + (((2 * piece + 1) ^ phase) << 4));
+        const uint32_t raw_base = smem_u32(c.raw), stage_base = smem_u32(c.stage);
         const int lane = threadIdx.x & 31;
+        uint32_t rs = 0, rph = 0, cs = 0, cph = 0;
         for (int t = blockIdx.x; t < c.num_tiles; t += gridDim.x) {
             for (int kb = 0; kb < c.nkb; ++kb) {
                 if (!mbar_wait(&c.bar->raw_full[rs], rph, c.w, kSiteConvRaw)) return;
                 if (!mbar_wait(&c.bar->empty[cs], cph ^ 1u, c.w, kSiteConvEmpty)) return;
-                const uint8_t *ra = c.raw + rs * C::kRawStage;
-                uint8_t *sa = c.stage + cs * C::kStage;
-#pragma unroll 4
-                for (int i = ctid; i < kTasks; i += C::kConvWarps * 32) {
-                    const int row = i >> 2, piece = i & 3;
-                    // raw A rows then raw B rows are contiguous (64 B each)
-                    const uint4 w = *reinterpret_cast<const uint4 *>(ra + row * 64 + piece * 16);
-                    uint32_t f[8];
-                    s8x4_to_f16x4(w.x, f[0], f[1]);
-                    s8x4_to_f16x4(w.y, f[2], f[3]);
-                    s8x4_to_f16x4(w.z, f[4], f[5]);
-                    s8x4_to_f16x4(w.w, f[6], f[7]);
-                    // destination: A rows then B rows are contiguous (128 B each)
-                    uint8_t *drow = sa + row * 128;
-                    const int sw = row & 7;
-                    *reinterpret_cast<uint4 *>(drow + (((2 * piece) ^ sw) << 4)) =
-                        make_uint4(f[0], f[1], f[2], f[3]);
-                    *reinterpret_cast<uint4 *>(drow + (((2 * piece + 1) ^ sw) << 4)) =
-                        make_uint4(f[4], f[5], f[6], f[7]);
+                const uint32_t src = raw_base + rs * C::kRawStage + src0;
+                const uint32_t dst = stage_base + cs * C::kStage;
+                constexpr int kBatch = kPer >= 4 ? 4 : kPer;  // loads in flight per thread
+#pragma unroll
+                for (int j0 = 0; j0 < kPer; j0 += kBatch) {
+                    uint4 w[kBatch];
+#pragma unroll
+                    for (int j = 0; j < kBatch; ++j) w[j] = lds128(src + (j0 + j) * kSrcStep);
+#pragma unroll
+                    for (int j = 0; j < kBatch; ++j) {
+                        uint32_t f[8];
+                        s8x4_to_f16x4(w[j].x, f[0], f[1]);
+                        s8x4_to_f16x4(w[j].y, f[2], f[3]);
+                        s8x4_to_f16x4(w[j].z, f[4], f[5]);
+                        s8x4_to_f16x4(w[j].w, f[6], f[7]);
+                        sts128(dst + dst0 + (j0 + j) * kDstStep, f[0], f[1], f[2], f[3]);
+                        sts128(dst + dst1 + (j0 + j) * kDstStep, f[4], f[5], f[6], f[7]);
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
