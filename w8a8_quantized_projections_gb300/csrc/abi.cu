@@ -103,6 +103,10 @@ int make_tmap(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t
     const cuuint64_t strides[1] = {pitch_bytes};
     const cuuint32_t box[2] = {box_inner, box_rows};
     const cuuint32_t estr[2] = {1, 1};
+    if (!g_encode) {
+        snprintf(g_last_err, sizeof g_last_err, "tensor-map encoder not initialised (no device set-up)");
+        return CLEF_ERR_CUDA;
+    }
     CUresult r = g_encode(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -158,14 +162,9 @@ int run_w8a8(int op, int epi, const void *qx, const float *sx, const void *qw, c
     if (swiglu && 2 * N > kMaxDim) return arg_fail("2N out of range");
     DeviceState *d = nullptr;
     if ((rc = device_state(&d))) return rc;
-    const bool i8 = (op == kOpI8);
-    const uint32_t box_k = i8 ? 64 : 128;  // int8 raw 64 B rows; e4m3 128 B swizzled rows
-    const CUtensorMapSwizzle swz = i8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
     const uint64_t b_rows = swiglu ? 2 * (uint64_t)N : (uint64_t)N;
-    CUtensorMap ta, tb;
-    if ((rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, qx, K, M, K, box_k, 128, swz))) return rc;
-    if ((rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, K, b_rows, K, box_k, swiglu ? 128 : 256, swz)))
-        return rc;
+    const Operand A = {qx, (uint64_t)K, (uint64_t)M, (uint64_t)K};
+    const Operand B = {qw, (uint64_t)K, b_rows, (uint64_t)K};
     GemmArgs a = base_args(d, M, N, K);
     a.n_half = swiglu ? (int)N : 0;
     a.sa = sx;
@@ -173,8 +172,7 @@ int run_w8a8(int op, int epi, const void *qx, const float *sx, const void *qw, c
     a.bias = static_cast<const uint16_t *>(bias);
     a.out = out;
     a.ldo = ldo;
-    cudaError_t e = launch_gemm(op, epi, 256, ta, tb, a, d->num_sms, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? CLEF_OK : cuda_fail(e, "gemm launch");
+    return launch_gemm(op, epi, 256, A, B, a, d->num_sms, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -189,11 +187,13 @@ int internal_device(int *num_sms, unsigned int **status) {
     return CLEF_OK;
 }
 
-int internal_make_tmap_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
-                            uint64_t pitch_bytes, uint32_t box_rows) {
-    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, rows, pitch_bytes, 64,
-                     box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+int internal_make_tmap(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
+                       uint64_t rows, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows,
+                       CUtensorMapSwizzle sw) {
+    return make_tmap(m, dt, base, inner, rows, pitch_bytes, box_inner, box_rows, sw);
 }
+
+int internal_cuda_error(cudaError_t e, const char *what) { return cuda_fail(e, what); }
 
 void internal_set_error(const char *msg) { snprintf(g_last_err, sizeof g_last_err, "%s", msg); }
 
@@ -271,25 +271,20 @@ int clef_lora_add(const void *x, int64_t ldx, const void *A, const void *B, int6
     const int64_t r_pad = (r + 63) / 64 * 64;
     const int bn = r_pad == 64 ? 64 : (r_pad == 128 ? 128 : 256);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    CUtensorMap tx, ta, tt, tbm;
-    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
     // stage 1: t = bf16(x A^T), [M][r_pad]; rows of A past r read as zeros
-    if ((rc = make_tmap(&tx, bf, x, K, M, ldx * 2, 64, 128, sw))) return rc;
-    if ((rc = make_tmap(&ta, bf, A, K, r, K * 2, 64, bn, sw))) return rc;
     GemmArgs a1 = base_args(d, M, r_pad, K);
     a1.out = t_scratch;
     a1.ldo = r_pad;
-    cudaError_t e = launch_gemm(kOpBF16, kEpiStoreBF16, bn, tx, ta, a1, d->num_sms, st);
-    if (e != cudaSuccess) return cuda_fail(e, "lora stage 1 launch");
+    rc = launch_gemm(kOpBF16, kEpiStoreBF16, bn, Operand{x, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2},
+                     Operand{A, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2}, a1, d->num_sms, st);
+    if (rc) return rc;
     // stage 2: y = bf16(y + t B^T); columns of B past r read as zeros
-    if ((rc = make_tmap(&tt, bf, t_scratch, r_pad, M, r_pad * 2, 64, 128, sw))) return rc;
-    if ((rc = make_tmap(&tbm, bf, B, r, N, r * 2, 64, 256, sw))) return rc;
     GemmArgs a2 = base_args(d, M, N, r_pad);
     a2.out = y;
     a2.ldo = ldy;
-    e = launch_gemm(kOpBF16, kEpiAddBF16, 256, tt, tbm, a2, d->num_sms, st);
-    return e == cudaSuccess ? CLEF_OK : cuda_fail(e, "lora stage 2 launch");
+    return launch_gemm(kOpBF16, kEpiAddBF16, 256,
+                       Operand{t_scratch, (uint64_t)r_pad, (uint64_t)M, (uint64_t)r_pad * 2},
+                       Operand{B, (uint64_t)r, (uint64_t)N, (uint64_t)r * 2}, a2, d->num_sms, st);
 }
 
 int clef_swiglu_bf16(const void *y_gu, int64_t M, int64_t N, int64_t ldg, void *h, int64_t ldh,

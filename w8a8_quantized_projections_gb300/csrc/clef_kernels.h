@@ -39,25 +39,35 @@ struct GemmArgs {
     int64_t ldo;             // output row pitch (elements)
     unsigned int *status;    // device status word
     uint64_t wait_limit_ns;
+    int *dbg;                // optional: per CTA, its own TMEM base and the one it uses
 };
 
-// A: [M][K] operand rows, B: [rows][K]; tensor maps are built by the caller
-// for the operand kind (see abi.cu).  bn selects the tile width.
-cudaError_t launch_gemm(int op, int epi, int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                        const GemmArgs &args, int num_sms, cudaStream_t st);
+// A row-major 2-D operand: rows of `inner` elements, `pitch` bytes apart.
+struct Operand {
+    const void *base;
+    uint64_t inner, rows, pitch;
+};
 
-// Smem bytes a (op, bn) instantiation needs (host side, for the attribute).
-int gemm_smem_bytes(int op, int bn);
+// A: [M][K] activation rows, B: [rows][K] weight rows.  Builds the TMA maps for
+// the chosen tile mode and launches on st.  bn selects the tile width (256 for
+// the W8A8 GEMMs; 64/128/256 for the LoRA rank).  Returns a clef_status code.
+int launch_gemm(int op, int epi, int bn, const Operand &A, const Operand &B, const GemmArgs &args,
+                int num_sms, cudaStream_t st);
+
+// Whether a launch with this width and row count uses CTA pairs.
+bool gemm_uses_pair(int bn, int M, int num_sms);
 
 cudaError_t launch_swiglu_bf16(const uint16_t *y_gu, int64_t M, int64_t N, int64_t ldg,
                                uint16_t *h, int64_t ldh, cudaStream_t st);
 
 // Services of abi.cu for other translation units: per-device checks and
-// set-up (SM count, status-word address), 128B-swizzled bf16 tensor maps with
-// 64-element boxes, and the calling thread's last-error text.
+// set-up (SM count, status-word address), TMA tensor maps, and the calling
+// thread's last-error text.
 int internal_device(int *num_sms, unsigned int **status);
-int internal_make_tmap_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
-                            uint64_t pitch_bytes, uint32_t box_rows);
+int internal_make_tmap(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
+                       uint64_t rows, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows,
+                       CUtensorMapSwizzle sw);
 void internal_set_error(const char *msg);
+int internal_cuda_error(cudaError_t e, const char *what);  // records the text, returns CLEF_ERR_CUDA
 
 }  // namespace clef

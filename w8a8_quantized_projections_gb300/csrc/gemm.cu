@@ -1,17 +1,26 @@
 // gemm.cu -- persistent, warp-specialised tcgen05 GEMM for sm_103a with the
 // fused epilogues of the W8A8 projection path.
 //
-// Tile: 128 output rows x BN columns, accumulated in TMEM (fp32), two
-// accumulator buffers so that the epilogue of one tile (or K-chunk) overlaps
-// the mainloop of the next.  Operands are K-major ("row . row^T"): A is the
-// activation [M][K], B the weight [N][K].
+// Tiles are 128 output rows per CTA by BN columns, accumulated in TMEM (fp32).
+// Operands are K-major ("row . row^T"): A is the activation [M][K], B the
+// weight [N][K].  Two tile modes:
+//   single  one CTA per 128 x BN tile, two TMEM accumulator buffers so the
+//           epilogue of one tile overlaps the mainloop of the next;
+//   pair    (BN = 256, M > 128) a cluster of two CTAs shares a 256 x 256 tile
+//           through tcgen05 cta_group::2: each CTA stages its own 128 A rows and
+//           half of the B rows, the leader CTA issues the MMAs for both, and the
+//           tensor cores of the two SMs read each B half once.  This halves the
+//           B operand's shared-memory traffic per SM, which is what bounds the
+//           single mode (about 128 B per clock per SM covers TMA writes, thread
+//           accesses and tensor-core operand reads together).
 //
-// Warp roles (one CTA per SM, persistent over tiles in M-fastest order so
-// that concurrently running CTAs share weight tiles in L2):
+// Warp roles (one CTA per SM, persistent over tiles in M-fastest order so that
+// concurrently running CTAs share weight tiles in L2):
 //   warp 0     TMA producer (one elected lane)
-//   warp 1     TMEM allocator and MMA issuer (one elected lane)
-//   warps 2-7  INT8 only: converters, widening int8 codes to fp16 in the
-//              128-byte-swizzled K-major layout the tensor core reads
+//   warp 1     TMEM allocator and MMA issuer (one elected lane; in pair mode the
+//              leader's only)
+//   INT8 only  converter warps widening int8 codes to fp16 in the 128-byte
+//              swizzled K-major layout the tensor core reads
 //   8 warps    epilogue (TMEM -> registers -> scales / bias / SwiGLU -> HBM);
 //              warp w reads TMEM lanes 32*(w%4)..+31, two warps per lane
 //              quadrant split the tile's columns
@@ -43,38 +52,49 @@ namespace clef {
 
 namespace {
 
-template <int OP, int EPI, int BN_>
+template <int OP, int EPI, int BN_, bool PAIR>
 struct Cfg {
-    static constexpr int BM = 128;
-    static constexpr int BN = BN_;
+    static constexpr int BM = 128;                         // A rows per CTA
+    static constexpr int BN = BN_;                         // accumulator columns
+    static constexpr bool kPair = PAIR;
+    static constexpr int kTileRows = PAIR ? 2 * BM : BM;   // output rows per tile
     static constexpr bool kI8 = (OP == kOpI8);
     // Every MMA operand k-block is 128 bytes of K: 64 fp16/bf16 or 128 e4m3.
     static constexpr int kOperandBytes = (OP == kOpF8) ? 1 : 2;
     static constexpr int BK = 128 / kOperandBytes;         // K elements per k-block
     static constexpr int kMmaPerKBlock = 4;                // each MMA consumes 32 bytes of K
+    static constexpr int kBRows = PAIR ? BN / 2 : BN;      // B rows staged per CTA
     static constexpr int kAStage = BM * 128;               // 16 KB
-    static constexpr int kBStage = BN * 128;
+    static constexpr int kBStage = kBRows * 128;
     static constexpr int kStage = kAStage + kBStage;
     // Raw int8 k-block (INT8 only): 64 codes = 64 bytes per row, no swizzle.
-    static constexpr int kRawA = BM * 64, kRawB = BN * 64, kRawStage = kRawA + kRawB;
+    static constexpr int kRawA = BM * 64, kRawB = kBRows * 64, kRawStage = kRawA + kRawB;
     static constexpr int kSmemBudget = 232448 - 1024 - 512;  // opt-in max - align slack - barriers
-    // INT8: two fp16 operand stages (converter -> MMA hand-off) and five raw
-    // int8 stages (enough TMA lookahead to cover L2/HBM latency).
-    static constexpr int NRAW = kI8 ? 5 : 0;
+    // INT8: a few fp16 operand stages (converter -> MMA hand-off) and more raw
+    // int8 stages (TMA lookahead to cover L2/HBM latency).
+    // Pair mode: raw stages are half as large, so eight of them give the TMA
+    // a deep lookahead while three fp16 stages cover the converter -> MMA hand-off.
+    static constexpr int NRAW = kI8 ? (PAIR ? 8 : 5) : 0;
     static constexpr int NSTAGE_RAWFREE = (kSmemBudget - NRAW * kRawStage) / kStage;
-    static constexpr int NSTAGE = kI8 ? 2 : (NSTAGE_RAWFREE > 8 ? 8 : NSTAGE_RAWFREE);
+    static constexpr int NSTAGE = kI8 ? (PAIR ? 3 : 2) : (NSTAGE_RAWFREE > 8 ? 8 : NSTAGE_RAWFREE);
     static constexpr int kChunkKBlocks = kI8 ? 16 : (1 << 30);  // 1024 K per exact chunk
     static constexpr int kConvWarps = kI8 ? 6 : 0;
     static constexpr int kEpiWarp0 = kI8 ? 8 : 4;
     static constexpr int kNumWarps = kEpiWarp0 + 8;
     static constexpr int kThreads = kNumWarps * 32;
-    static constexpr int kTmemCols = 2 * BN;               // two accumulator buffers
+    static constexpr int kAccBufs = 2;                     // double-buffered accumulator
+    static constexpr int kTmemCols = kAccBufs * BN;
     static constexpr int kColsPerThread = BN / 2;          // columns one epilogue thread owns
     static constexpr int kChunks32 = kColsPerThread / 32;
     static constexpr bool kSwiGLU = (EPI == kEpiSwiGLU);
     static constexpr int kOutColsPerTile = kSwiGLU ? BN / 2 : BN;
+    // full[s]: TMA (native) or the local converter warps (INT8); in pair mode
+    // the leader's barrier also counts the peer's forwarded readiness.
+    static constexpr int kFullArrivals = kI8 ? kConvWarps : 1;
+    static constexpr int kAccEmptyArrivals = 8 * (PAIR ? 2 : 1);
     static constexpr int kSmemBytes = NSTAGE * kStage + NRAW * kRawStage + 1024 + 512;
     static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
+    static_assert(!PAIR || BN == 256, "pair mode uses 256-wide tiles");
     static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
     static_assert(kSmemBytes <= 232448, "shared memory");
     static_assert(NSTAGE >= 2, "pipeline depth");
@@ -82,7 +102,7 @@ struct Cfg {
 
 struct Barriers {
     uint64_t full[8], empty[8];
-    uint64_t raw_full[6], raw_empty[6];
+    uint64_t raw_full[8], raw_empty[8];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t drain;
     uint32_t tmem_slot;
@@ -159,19 +179,129 @@ __device__ __forceinline__ float scale_bias(float acc, float sa, float sb, const
     return y;
 }
 
+// ---------------------------------------------------------------- CTA pairs
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Shared::cluster address of the same shared variable in the pair's leader (rank 0).
+__device__ __forceinline__ uint32_t leader_addr(const void *local) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(smem_u32(local)));
+    return r;
+}
+
+__device__ __forceinline__ void arrive_cluster(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
+}
+
+// Relaxed cluster-scope arrive: no release fence.  Used only to forward a
+// readiness signal whose data ordering was already established locally (see
+// Gemm::forwarder); a release at cluster scope costs about a microsecond.
+__device__ __forceinline__ void arrive_cluster_relaxed(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Time-limited wait with cluster-scope acquire (barriers that receive arrivals
+// from the peer CTA or multicast commits); otherwise as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t *bar, uint32_t parity, const WaitCtx &w,
+                                             unsigned int site) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(a, parity)) return true;
+        if ((it & 63u) == 0u) {
+            if (*w.abort) return false;
+            if (globaltimer_ns() - t0 > w.limit_ns) {
+                record_status(w.status, kStatusTimeout | (site << 8));
+                *w.abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void mma2_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma2_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the barrier at this shared offset in both CTAs of the pair once
+// the pair's MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void mma2_commit_both(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)), "h"((uint16_t)3) : "memory");
+}
+
+__device__ __forceinline__ void mma2_commit_local(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+
+// TMA tile load into this CTA's shared memory whose completion is counted on
+// a barrier that may live in the peer CTA (shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorMap *m, int32_t c0,
+                                                 int32_t c1, uint32_t cluster_bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1),
+          "r"(cluster_bar)
+        : "memory");
+}
+
 }  // namespace
 
 namespace {
 
-template <int OP, int EPI, int BN>
+template <int OP, int EPI, int BN, bool PAIR>
 struct Gemm {
-    using C = Cfg<OP, EPI, BN>;
+    using C = Cfg<OP, EPI, BN, PAIR>;
 
     struct Ctx {
         uint8_t *stage;      // NSTAGE x (A tile, B tile), 1024-aligned
         uint8_t *raw;        // NRAW x (raw A, raw B) for INT8
         Barriers *bar;
-        uint32_t tmem;
+        uint32_t tmem;       // accumulator base (the leader's allocation in pair mode)
+        uint32_t rank;       // rank in the CTA pair (0 in single mode)
+        int slot, nslots;    // tile-loop start and stride
         int num_m, num_n, num_tiles, nkb;
         WaitCtx w;
     };
@@ -181,43 +311,65 @@ struct Gemm {
         nb = t / c.num_m;
     }
 
+    // Waits on barriers that receive arrivals from the peer CTA or from the
+    // pair's multicast commits use cluster-scope acquire.
+    static __device__ __forceinline__ bool wait_pair(uint64_t *bar, uint32_t parity, const Ctx &c,
+                                                     unsigned int site) {
+        return PAIR ? mbar_wait_cl(bar, parity, c.w, site) : mbar_wait(bar, parity, c.w, site);
+    }
+
+    // Row of the weight operand that this CTA's B stage starts with.
+    static __device__ __forceinline__ int b_row(const Ctx &c, const GemmArgs &a, int nb, int half) {
+        if (C::kSwiGLU) return (half ? a.n_half : 0) + nb * (BN / 2);
+        return nb * BN + (int)c.rank * C::kBRows;
+    }
+
     // ---------------------------------------------------------------- producer
     static __device__ void producer(const Ctx &c, const CUtensorMap *tmA, const CUtensorMap *tmB,
                                     const GemmArgs &a, uint32_t (&fills)[8]) {
         static_assert(C::NRAW <= 8 && C::NSTAGE <= 8, "fill bookkeeping");
         uint32_t s = 0, ph = 0;
         const int nstage = C::kI8 ? C::NRAW : C::NSTAGE;
-        for (int t = blockIdx.x; t < c.num_tiles; t += gridDim.x) {
+        for (int t = c.slot; t < c.num_tiles; t += c.nslots) {
             int mb, nb;
             tile_coords(c, t, mb, nb);
-            const int row_a = mb * C::BM;
+            const int row_a = mb * C::kTileRows + (int)c.rank * C::BM;
             for (int kb = 0; kb < c.nkb; ++kb) {
-                uint64_t *empty = C::kI8 ? &c.bar->raw_empty[s] : &c.bar->empty[s];
-                uint64_t *full = C::kI8 ? &c.bar->raw_full[s] : &c.bar->full[s];
-                if (!mbar_wait(empty, ph ^ 1u, c.w, kSiteTmaEmpty)) return;
                 if (C::kI8) {
+                    if (!mbar_wait(&c.bar->raw_empty[s], ph ^ 1u, c.w, kSiteTmaEmpty)) return;
+                    uint64_t *full = &c.bar->raw_full[s];
                     uint8_t *ra = c.raw + s * C::kRawStage;
                     uint8_t *rb = ra + C::kRawA;
                     const int k0 = kb * 64;
                     mbar_arrive_expect_tx(full, C::kRawStage);
                     tma_load_2d(ra, tmA, k0, row_a, full);
-                    if (C::kSwiGLU) {
-                        tma_load_2d(rb, tmB, k0, nb * (BN / 2), full);
-                        tma_load_2d(rb + (BN / 2) * 64, tmB, k0, a.n_half + nb * (BN / 2), full);
+                    if (C::kSwiGLU && !PAIR) {
+                        tma_load_2d(rb, tmB, k0, b_row(c, a, nb, 0), full);
+                        tma_load_2d(rb + (BN / 2) * 64, tmB, k0, b_row(c, a, nb, 1), full);
                     } else {
-                        tma_load_2d(rb, tmB, k0, nb * BN, full);
+                        tma_load_2d(rb, tmB, k0, b_row(c, a, nb, (int)c.rank), full);
                     }
                 } else {
+                    if (!wait_pair(&c.bar->empty[s], ph ^ 1u, c, kSiteTmaEmpty)) return;
                     uint8_t *sa = c.stage + s * C::kStage;
                     uint8_t *sb = sa + C::kAStage;
                     const int k0 = kb * C::BK;
-                    mbar_arrive_expect_tx(full, C::kStage);
-                    tma_load_2d(sa, tmA, k0, row_a, full);
-                    if (C::kSwiGLU) {
-                        tma_load_2d(sb, tmB, k0, nb * (BN / 2), full);
-                        tma_load_2d(sb + (BN / 2) * 128, tmB, k0, a.n_half + nb * (BN / 2), full);
+                    if (PAIR) {
+                        // both CTAs' copies complete on the leader's barrier
+                        const uint32_t lfull = leader_addr(&c.bar->full[s]);
+                        if (c.rank == 0) mbar_arrive_expect_tx(&c.bar->full[s], 2 * C::kStage);
+                        tma_load_2d_pair(sa, tmA, k0, row_a, lfull);
+                        tma_load_2d_pair(sb, tmB, k0, b_row(c, a, nb, (int)c.rank), lfull);
                     } else {
-                        tma_load_2d(sb, tmB, k0, nb * BN, full);
+                        uint64_t *full = &c.bar->full[s];
+                        mbar_arrive_expect_tx(full, C::kStage);
+                        tma_load_2d(sa, tmA, k0, row_a, full);
+                        if (C::kSwiGLU) {
+                            tma_load_2d(sb, tmB, k0, b_row(c, a, nb, 0), full);
+                            tma_load_2d(sb + (BN / 2) * 128, tmB, k0, b_row(c, a, nb, 1), full);
+                        } else {
+                            tma_load_2d(sb, tmB, k0, b_row(c, a, nb, 0), full);
+                        }
                     }
                 }
                 fills[s] = ph | 2u;  // bit 1: stage filled at least once; bit 0: parity
@@ -227,8 +379,11 @@ struct Gemm {
     }
 
     // Before the CTA exits: wait (time-limited) until every copy issued into
-    // each stage has landed, so no TMA write targets a finished CTA.
+    // each stage has landed, so no TMA write targets a finished CTA.  In pair
+    // mode the native copies of both CTAs complete on the leader's barriers,
+    // so the leader waits for them (the pair then meets at a cluster barrier).
     static __device__ void drain_copies(const Ctx &c, const uint32_t (&fills)[8], unsigned int *st) {
+        if (PAIR && !C::kI8 && c.rank != 0) return;
         const int nstage = C::kI8 ? C::NRAW : C::NSTAGE;
         for (int s = 0; s < nstage; ++s) {
             if (!(fills[s] & 2u)) continue;
@@ -239,15 +394,14 @@ struct Gemm {
 
     // ---------------------------------------------------------------- converters
     // Each converter thread owns the same 16-byte raw pieces in every k-block:
-    // piece = ctid & 3 of rows (ctid >> 2) + 48 j, j = 0..7 (A rows 0..127,
-    // then B rows).  Because 48 is a multiple of 8, the 128-byte swizzle phase
-    // (row & 7) of a thread's rows is constant, so all shared addresses are a
+    // piece = ctid & 3 of rows (ctid >> 2) + S j (A rows 0..127, then B rows),
+    // where S = threads / 4 is a multiple of 8, so the 128-byte swizzle phase
+    // (row & 7) of a thread's rows is constant and all shared addresses are a
     // per-thread base plus compile-time offsets.
     static __device__ void converter(const Ctx &c, int ctid) {
         constexpr int kThr = (C::kI8 ? C::kConvWarps : 6) * 32;  // native ops never call this
-        constexpr int kRows = C::BM + BN;
-        constexpr int kPer = kRows * 4 / kThr;
-        static_assert(!C::kI8 || kRows * 4 % kThr == 0, "converter tasks");
+        constexpr int kRows = C::BM + C::kBRows;
+        constexpr int kPer = (kRows * 4 + kThr - 1) / kThr;     // the last task may be partial
         static_assert(!C::kI8 || (kThr / 4) % 8 == 0, "constant swizzle phase");
         constexpr uint32_t kSrcStep = (kThr / 4) * 64, kDstStep = (kThr / 4) * 128;
         const int row0 = ctid >> 2, piece = ctid & 3, phase = row0 & 7;
@@ -257,10 +411,10 @@ struct Gemm {
         const uint32_t raw_base = smem_u32(c.raw), stage_base = smem_u32(c.stage);
         const int lane = threadIdx.x & 31;
         uint32_t rs = 0, rph = 0, cs = 0, cph = 0;
-        for (int t = blockIdx.x; t < c.num_tiles; t += gridDim.x) {
+        for (int t = c.slot; t < c.num_tiles; t += c.nslots) {
             for (int kb = 0; kb < c.nkb; ++kb) {
                 if (!mbar_wait(&c.bar->raw_full[rs], rph, c.w, kSiteConvRaw)) return;
-                if (!mbar_wait(&c.bar->empty[cs], cph ^ 1u, c.w, kSiteConvEmpty)) return;
+                if (!wait_pair(&c.bar->empty[cs], cph ^ 1u, c, kSiteConvEmpty)) return;
                 const uint32_t src = raw_base + rs * C::kRawStage + src0;
                 const uint32_t dst = stage_base + cs * C::kStage;
                 constexpr int kBatch = kPer >= 4 ? 4 : kPer;  // loads in flight per thread
@@ -268,9 +422,12 @@ struct Gemm {
                 for (int j0 = 0; j0 < kPer; j0 += kBatch) {
                     uint4 w[kBatch];
 #pragma unroll
-                    for (int j = 0; j < kBatch; ++j) w[j] = lds128(src + (j0 + j) * kSrcStep);
+                    for (int j = 0; j < kBatch; ++j)
+                        if (j0 + j < kPer && row0 + (kThr / 4) * (j0 + j) < kRows)
+                            w[j] = lds128(src + (j0 + j) * kSrcStep);
 #pragma unroll
                     for (int j = 0; j < kBatch; ++j) {
+                        if (j0 + j >= kPer || row0 + (kThr / 4) * (j0 + j) >= kRows) continue;
                         uint32_t f[8];
                         s8x4_to_f16x4(w[j].x, f[0], f[1]);
                         s8x4_to_f16x4(w[j].y, f[2], f[3]);
@@ -292,19 +449,37 @@ struct Gemm {
         }
     }
 
+    // Pair mode, INT8, peer CTA: once this CTA's converters have filled an
+    // operand stage, tell the leader with one cluster-scope arrive (the
+    // converters themselves only arrive on the local barrier).  The stage's
+    // data is this CTA's own shared memory, already written and fenced to the
+    // async proxy by the converters before their local arrive, which this
+    // thread has observed; the leader's tensor-core reads of it are issued only
+    // after this arrive lands, so a relaxed arrive suffices.
+    static __device__ void forwarder(const Ctx &c) {
+        uint32_t s = 0, ph = 0;
+        for (int t = c.slot; t < c.num_tiles; t += c.nslots) {
+            for (int kb = 0; kb < c.nkb; ++kb) {
+                if (!mbar_wait(&c.bar->full[s], ph, c.w, kSiteMmaFull)) return;
+                arrive_cluster_relaxed(leader_addr(&c.bar->full[s]));
+                if (++s == (uint32_t)C::NSTAGE) { s = 0; ph ^= 1u; }
+            }
+        }
+    }
+
     // ---------------------------------------------------------------- MMA issuer
     static __device__ void mma_issuer(const Ctx &c) {
         constexpr uint32_t afmt = (OP == kOpBF16) ? 1u : 0u;  // F16 / BF16 / E4M3
-        constexpr uint32_t idesc = idesc_f32acc(afmt, afmt, C::BM, BN);
+        constexpr uint32_t idesc = idesc_f32acc(afmt, afmt, C::kTileRows, BN);
         uint32_t s = 0, ph = 0, acc = 0, aph = 0;
-        for (int t = blockIdx.x; t < c.num_tiles; t += gridDim.x) {
+        for (int t = c.slot; t < c.num_tiles; t += c.nslots) {
             for (int kb0 = 0; kb0 < c.nkb; kb0 += C::kChunkKBlocks) {
                 const int kb1 = min(c.nkb, kb0 + C::kChunkKBlocks);
-                if (!mbar_wait(&c.bar->acc_empty[acc], aph ^ 1u, c.w, kSiteMmaAccEmpty)) return;
+                if (!wait_pair(&c.bar->acc_empty[acc], aph ^ 1u, c, kSiteMmaAccEmpty)) return;
                 tc_fence_after();
                 const uint32_t d = c.tmem + acc * BN;
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(&c.bar->full[s], ph, c.w, kSiteMmaFull)) return;
+                    if (!wait_pair(&c.bar->full[s], ph, c, kSiteMmaFull)) return;
                     tc_fence_after();
                     const uint32_t sa = smem_u32(c.stage + s * C::kStage);
                     const uint32_t sb = sa + C::kAStage;
@@ -313,14 +488,21 @@ struct Gemm {
                         const uint64_t ad = sdesc_sw128(sa + 32 * k);
                         const uint64_t bd = sdesc_sw128(sb + 32 * k);
                         const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
-                        if (OP == kOpF8) mma_f8(d, ad, bd, idesc, accum);
-                        else mma_f16(d, ad, bd, idesc, accum);
+                        if (PAIR) {
+                            if (OP == kOpF8) mma2_f8(d, ad, bd, idesc, accum);
+                            else mma2_f16(d, ad, bd, idesc, accum);
+                        } else {
+                            if (OP == kOpF8) mma_f8(d, ad, bd, idesc, accum);
+                            else mma_f16(d, ad, bd, idesc, accum);
+                        }
                     }
-                    mma_commit(&c.bar->empty[s]);
+                    if (PAIR) mma2_commit_both(&c.bar->empty[s]);
+                    else mma_commit(&c.bar->empty[s]);
                     if (++s == (uint32_t)C::NSTAGE) { s = 0; ph ^= 1u; }
                 }
-                mma_commit(&c.bar->acc_full[acc]);
-                if (++acc == 2u) { acc = 0; aph ^= 1u; }
+                if (PAIR) mma2_commit_both(&c.bar->acc_full[acc]);
+                else mma_commit(&c.bar->acc_full[acc]);
+                if (++acc == (uint32_t)C::kAccBufs) { acc = 0; aph ^= 1u; }
             }
         }
     }
@@ -395,26 +577,71 @@ struct Gemm {
         }
     }
 
+    // Finish this thread's row from its kColsPerThread accumulator values
+    // (fp32 bits, or exact int32 totals for INT8).
+    template <class T>
+    static __device__ __forceinline__ void finish_row(const GemmArgs &a, int row, bool row_ok, int nb,
+                                                      int half, const T *acc) {
+        auto val = [](T x) -> float {
+            if constexpr (sizeof(T) == 4 && T(-1) < T(0)) return __int2float_rn((int32_t)x);
+            else return __uint_as_float((uint32_t)x);
+        };
+        if (EPI == kEpiStoreS32) {
+            if constexpr (C::kI8) {
+#pragma unroll
+                for (int j = 0; j < C::kChunks32; ++j)
+                    store_s32(a, row, row_ok, nb * BN + chunk_col(j, half),
+                              reinterpret_cast<const int32_t *>(acc) + 32 * j);
+            }
+        } else if (C::kSwiGLU) {
+#pragma unroll
+            for (int j = 0; j < C::kChunks32 / 2; ++j) {
+                float v[32], u[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    v[i] = val(acc[32 * j + i]);
+                    u[i] = val(acc[32 * (j + C::kChunks32 / 2) + i]);
+                }
+                finish32(a, row, row_ok, nb * (BN / 2) + chunk_col(j, half), v, u);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < C::kChunks32; ++j) {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = val(acc[32 * j + i]);
+                finish32(a, row, row_ok, nb * BN + chunk_col(j, half), v, v);
+            }
+        }
+    }
+
+    static __device__ __forceinline__ void release_acc(const Ctx &c, uint32_t acc, int lane) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            if (PAIR) arrive_cluster(leader_addr(&c.bar->acc_empty[acc]));
+            else mbar_arrive(&c.bar->acc_empty[acc]);
+        }
+    }
+
     static __device__ void epilogue(const Ctx &c, const GemmArgs &a) {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         const int e = warp - C::kEpiWarp0, quad = warp & 3, half = e >> 2;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         uint32_t acc = 0, aph = 0;
-        for (int t = blockIdx.x; t < c.num_tiles; t += gridDim.x) {
+        for (int t = c.slot; t < c.num_tiles; t += c.nslots) {
             int mb, nb;
             tile_coords(c, t, mb, nb);
-            const int row = mb * C::BM + quad * 32 + lane;
+            const int row = mb * C::kTileRows + (int)c.rank * C::BM + quad * 32 + lane;
             const bool row_ok = row < a.M;
-            int32_t tot[C::kI8 ? C::kColsPerThread : 1];
-            if (C::kI8) {
+            if constexpr (C::kI8) {
+                int32_t tot[C::kColsPerThread];
 #pragma unroll
                 for (int i = 0; i < C::kColsPerThread; ++i) tot[i] = 0;
-            }
-            for (int kb0 = 0; kb0 < c.nkb; kb0 += C::kChunkKBlocks) {
-                if (!mbar_wait(&c.bar->acc_full[acc], aph, c.w, kSiteEpiAccFull)) return;
-                tc_fence_after();
-                const uint32_t tbase = c.tmem + acc * BN + lane_off;
-                if (C::kI8) {
+                for (int kb0 = 0; kb0 < c.nkb; kb0 += C::kChunkKBlocks) {
+                    if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
+                    tc_fence_after();
+                    const uint32_t tbase = c.tmem + acc * BN + lane_off;
 #pragma unroll
                     for (int j = 0; j < C::kChunks32; ++j) {
                         uint32_t r[32];
@@ -423,89 +650,45 @@ struct Gemm {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) tot[32 * j + i] += __float2int_rn(__uint_as_float(r[i]));
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&c.bar->acc_empty[acc]);
-                    if (++acc == 2u) { acc = 0; aph ^= 1u; }
-                    if (kb0 + C::kChunkKBlocks < c.nkb) continue;  // more chunks of this tile
-                    // the tile's exact int32 accumulators are complete
-                    if (EPI == kEpiStoreS32) {
-#pragma unroll
-                        for (int j = 0; j < C::kChunks32; ++j)
-                            store_s32(a, row, row_ok, nb * BN + chunk_col(j, half), tot + 32 * j);
-                    } else if (C::kSwiGLU) {
-#pragma unroll
-                        for (int j = 0; j < C::kChunks32 / 2; ++j) {
-                            float v[32], u[32];
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                v[i] = __int2float_rn(tot[32 * j + i]);
-                                u[i] = __int2float_rn(tot[32 * (j + C::kChunks32 / 2) + i]);
-                            }
-                            finish32(a, row, row_ok, nb * (BN / 2) + chunk_col(j, half), v, u);
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < C::kChunks32; ++j) {
-                            float v[32];
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = __int2float_rn(tot[32 * j + i]);
-                            finish32(a, row, row_ok, nb * BN + chunk_col(j, half), v, v);
-                        }
-                    }
-                } else {
-                    if (C::kSwiGLU) {
-#pragma unroll
-                        for (int j = 0; j < C::kChunks32 / 2; ++j) {
-                            uint32_t rg[32], ru[32];
-                            tmem_ld32(tbase + chunk_col(j, half), rg);
-                            tmem_ld32(tbase + chunk_col(j + C::kChunks32 / 2, half), ru);
-                            tmem_ld_wait();
-                            float v[32], u[32];
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                v[i] = __uint_as_float(rg[i]);
-                                u[i] = __uint_as_float(ru[i]);
-                            }
-                            finish32(a, row, row_ok, nb * (BN / 2) + chunk_col(j, half), v, u);
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < C::kChunks32; ++j) {
-                            uint32_t r[32];
-                            tmem_ld32(tbase + chunk_col(j, half), r);
-                            tmem_ld_wait();
-                            float v[32];
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                            finish32(a, row, row_ok, nb * BN + chunk_col(j, half), v, v);
-                        }
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&c.bar->acc_empty[acc]);
-                    if (++acc == 2u) { acc = 0; aph ^= 1u; }
+                    release_acc(c, acc, lane);
+                    if (++acc == (uint32_t)C::kAccBufs) { acc = 0; aph ^= 1u; }
                 }
+                // the tile's exact int32 accumulators are complete
+                finish_row(a, row, row_ok, nb, half, tot);
+            } else {
+                if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
+                tc_fence_after();
+                const uint32_t tbase = c.tmem + acc * BN + lane_off;
+                uint32_t v[C::kColsPerThread];
+#pragma unroll
+                for (int j = 0; j < C::kChunks32; ++j)
+                    tmem_ld32(tbase + chunk_col(j, half), *reinterpret_cast<uint32_t(*)[32]>(v + 32 * j));
+                tmem_ld_wait();
+                release_acc(c, acc, lane);  // the MMA may refill the buffer while this row is finished
+                if (++acc == (uint32_t)C::kAccBufs) { acc = 0; aph ^= 1u; }
+                finish_row(a, row, row_ok, nb, half, v);
             }
         }
     }
 };
 
-template <int OP, int EPI, int BN>
-__global__ void __launch_bounds__(Cfg<OP, EPI, BN>::kThreads, 1)
+template <int OP, int EPI, int BN, bool PAIR>
+__global__ void __launch_bounds__(Cfg<OP, EPI, BN, PAIR>::kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const GemmArgs args) {
-    using C = Cfg<OP, EPI, BN>;
-    using G = Gemm<OP, EPI, BN>;
+    using C = Cfg<OP, EPI, BN, PAIR>;
+    using G = Gemm<OP, EPI, BN, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((base + 1023u) & ~1023u) - base);
     Barriers *bar = reinterpret_cast<Barriers *>(smem + C::NSTAGE * C::kStage + C::NRAW * C::kRawStage);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? cluster_rank() : 0u;
 
     if (threadIdx.x == 0) {
+        const int full_arrivals = C::kFullArrivals + ((PAIR && C::kI8 && rank == 0) ? 1 : 0);
         for (int s = 0; s < C::NSTAGE; ++s) {
-            mbar_init(&bar->full[s], C::kI8 ? C::kConvWarps : 1);
+            mbar_init(&bar->full[s], full_arrivals);
             mbar_init(&bar->empty[s], 1);
         }
         for (int s = 0; s < C::NRAW; ++s) {
@@ -514,7 +697,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar->acc_full[s], 1);
-            mbar_init(&bar->acc_empty[s], 8);
+            mbar_init(&bar->acc_empty[s], C::kAccEmptyArrivals);
         }
         mbar_init(&bar->drain, 1);
         bar->abort = 0;
@@ -525,19 +708,42 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(&bar->tmem_slot, C::kTmemCols);
-        tmem_relinquish();
+        if (PAIR) {
+            // both CTAs of the pair issue the allocation; it pairs up across the
+            // two CTAs and returns the same columns in each
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                         ::"r"(smem_u32(&bar->tmem_slot)), "r"(C::kTmemCols) : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            tmem_alloc(&bar->tmem_slot, C::kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // both CTAs' barriers and TMEM are set up
     tc_fence_after();
 
     typename G::Ctx c;
     c.stage = smem;
     c.raw = smem + C::NSTAGE * C::kStage;
     c.bar = bar;
-    c.tmem = bar->tmem_slot;
-    c.num_m = (args.M + C::BM - 1) / C::BM;
+    const uint32_t own_tmem = bar->tmem_slot;
+    if (PAIR) {
+        uint32_t lt;
+        asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(lt) : "r"(leader_addr(&bar->tmem_slot)));
+        c.tmem = lt;
+    } else {
+        c.tmem = own_tmem;
+    }
+    if (args.dbg && threadIdx.x == 0) {
+        args.dbg[2 * blockIdx.x] = (int)own_tmem;
+        args.dbg[2 * blockIdx.x + 1] = (int)c.tmem;
+    }
+    c.rank = rank;
+    c.slot = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    c.nslots = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    c.num_m = (args.M + C::kTileRows - 1) / C::kTileRows;
     c.num_n = (args.N + C::kOutColsPerTile - 1) / C::kOutColsPerTile;
     c.num_tiles = c.num_m * c.num_n;
     c.nkb = C::kI8 ? (args.K + 63) / 64 : (args.K + C::BK - 1) / C::BK;
@@ -546,6 +752,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     c.w.status = args.status;
 
     uint32_t fills[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    const bool issues_mma = !PAIR || rank == 0;
     if (warp < C::kEpiWarp0) {
         // INT8: control and converter warps hand registers to the epilogue
         // warps, which hold the int32 totals
@@ -556,13 +763,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 G::drain_copies(c, fills, args.status);
             }
         } else if (warp == 1) {
-            if (lane == 0) {
+            if (lane == 0 && issues_mma) {
                 G::mma_issuer(c);
                 // wind down: wait until every MMA issued by this thread completed
-                mma_commit(&bar->drain);
+                if (PAIR) mma2_commit_local(&bar->drain);
+                else mma_commit(&bar->drain);
                 mbar_wait_drain(&bar->drain, 0, 200000000ull, args.status);
+            } else if (lane == 0 && PAIR && C::kI8) {
+                G::forwarder(c);
             }
-        } else if (C::kI8) {
+        } else if (C::kI8 && warp < 2 + C::kConvWarps) {
             G::converter(c, threadIdx.x - 64);
         }
     } else {
@@ -571,62 +781,106 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) {
+        if (bar->abort) {  // let copies still signalling the other CTA land first
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 2000000ull) {
+            }
+        }
+        cluster_sync();
+    }
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(c.tmem, C::kTmemCols);
+        if (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(own_tmem),
+                         "r"(C::kTmemCols) : "memory");
+        else
+            tmem_dealloc(own_tmem, C::kTmemCols);
     }
 }
 
-template <int OP, int EPI, int BN>
-cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
-                       int num_sms, cudaStream_t st) {
-    using C = Cfg<OP, EPI, BN>;
-    auto kern = gemm_kernel<OP, EPI, BN>;
+template <int OP, int EPI, int BN, bool PAIR>
+int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num_sms,
+               cudaStream_t st) {
+    using C = Cfg<OP, EPI, BN, PAIR>;
+    const CUtensorMapDataType dt =
+        (OP == kOpBF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    // INT8: raw 64-byte rows, no swizzle (converters re-lay them out);
+    // native: 128-byte rows in the 128-byte swizzle the MMA descriptors expect.
+    const uint32_t box_k = C::kI8 ? 64u : (uint32_t)C::BK;
+    const CUtensorMapSwizzle sw = C::kI8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+    CUtensorMap ta, tb;
+    int rc = internal_make_tmap(&ta, dt, A.base, A.inner, A.rows, A.pitch, box_k, C::BM, sw);
+    if (rc) return rc;
+    rc = internal_make_tmap(&tb, dt, B.base, B.inner, B.rows, B.pitch, box_k,
+                            C::kSwiGLU ? BN / 2 : C::kBRows, sw);
+    if (rc) return rc;
+    auto kern = gemm_kernel<OP, EPI, BN, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    const int num_m = (args.M + C::BM - 1) / C::BM;
+    if (e != cudaSuccess) return internal_cuda_error(e, "gemm smem attribute");
+    const int num_m = (args.M + C::kTileRows - 1) / C::kTileRows;
     const int num_n = (args.N + C::kOutColsPerTile - 1) / C::kOutColsPerTile;
     const int tiles = num_m * num_n;
-    const int grid = tiles < num_sms ? tiles : num_sms;
-    kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tmA, tmB, args);
-    return cudaGetLastError();
+    if (PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(C::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // persistent pairs: no more than can be resident at once
+        static int max_pairs = -1;
+        if (max_pairs < 0) {
+            cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+            max_pairs = (e == cudaSuccess && n > 0) ? n : num_sms / 2;
+        }
+        const int pairs = tiles < max_pairs ? tiles : max_pairs;
+        cfg.gridDim = dim3(2 * pairs, 1, 1);
+        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, args);
+    } else {
+        const int grid = tiles < num_sms ? tiles : num_sms;
+        kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(ta, tb, args);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return internal_cuda_error(e, "gemm launch");
+    return 0;
 }
 
 }  // namespace
 
-int gemm_smem_bytes(int op, int bn) {
-    if (op == kOpI8) return Cfg<kOpI8, kEpiScaleBias, 256>::kSmemBytes;
-    if (op == kOpF8) return Cfg<kOpF8, kEpiScaleBias, 256>::kSmemBytes;
-    if (bn == 64) return Cfg<kOpBF16, kEpiStoreBF16, 64>::kSmemBytes;
-    if (bn == 128) return Cfg<kOpBF16, kEpiStoreBF16, 128>::kSmemBytes;
-    return Cfg<kOpBF16, kEpiStoreBF16, 256>::kSmemBytes;
-}
+bool gemm_uses_pair(int bn, int M, int num_sms) { return bn == 256 && M > 128 && num_sms >= 2; }
 
-cudaError_t launch_gemm(int op, int epi, int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                        const GemmArgs &args, int num_sms, cudaStream_t st) {
+int launch_gemm(int op, int epi, int bn, const Operand &A, const Operand &B, const GemmArgs &args,
+                int num_sms, cudaStream_t st) {
+    const bool pair = gemm_uses_pair(bn, args.M, num_sms);
+#define CLEF_GEMM(OPV, EPIV, BNV)                                                        \
+    return pair ? launch_one<OPV, EPIV, BNV, true>(A, B, args, num_sms, st)              \
+                : launch_one<OPV, EPIV, BNV, false>(A, B, args, num_sms, st)
     if (op == kOpI8 && bn == 256) {
-        switch (epi) {
-            case kEpiScaleBias: return launch_one<kOpI8, kEpiScaleBias, 256>(tmA, tmB, args, num_sms, st);
-            case kEpiSwiGLU: return launch_one<kOpI8, kEpiSwiGLU, 256>(tmA, tmB, args, num_sms, st);
-            case kEpiStoreS32: return launch_one<kOpI8, kEpiStoreS32, 256>(tmA, tmB, args, num_sms, st);
-            default: break;
-        }
+        if (epi == kEpiScaleBias) CLEF_GEMM(kOpI8, kEpiScaleBias, 256);
+        if (epi == kEpiSwiGLU) CLEF_GEMM(kOpI8, kEpiSwiGLU, 256);
+        if (epi == kEpiStoreS32) CLEF_GEMM(kOpI8, kEpiStoreS32, 256);
     } else if (op == kOpF8 && bn == 256) {
-        switch (epi) {
-            case kEpiScaleBias: return launch_one<kOpF8, kEpiScaleBias, 256>(tmA, tmB, args, num_sms, st);
-            case kEpiSwiGLU: return launch_one<kOpF8, kEpiSwiGLU, 256>(tmA, tmB, args, num_sms, st);
-            default: break;
-        }
+        if (epi == kEpiScaleBias) CLEF_GEMM(kOpF8, kEpiScaleBias, 256);
+        if (epi == kEpiSwiGLU) CLEF_GEMM(kOpF8, kEpiSwiGLU, 256);
     } else if (op == kOpBF16) {
         if (epi == kEpiStoreBF16) {
-            if (bn == 64) return launch_one<kOpBF16, kEpiStoreBF16, 64>(tmA, tmB, args, num_sms, st);
-            if (bn == 128) return launch_one<kOpBF16, kEpiStoreBF16, 128>(tmA, tmB, args, num_sms, st);
-            if (bn == 256) return launch_one<kOpBF16, kEpiStoreBF16, 256>(tmA, tmB, args, num_sms, st);
+            if (bn == 64) return launch_one<kOpBF16, kEpiStoreBF16, 64, false>(A, B, args, num_sms, st);
+            if (bn == 128) return launch_one<kOpBF16, kEpiStoreBF16, 128, false>(A, B, args, num_sms, st);
+            if (bn == 256) CLEF_GEMM(kOpBF16, kEpiStoreBF16, 256);
         } else if (epi == kEpiAddBF16 && bn == 256) {
-            return launch_one<kOpBF16, kEpiAddBF16, 256>(tmA, tmB, args, num_sms, st);
+            CLEF_GEMM(kOpBF16, kEpiAddBF16, 256);
         }
     }
-    return cudaErrorInvalidValue;
+#undef CLEF_GEMM
+    return internal_cuda_error(cudaErrorInvalidValue, "no GEMM instantiation for this operand/epilogue/width");
 }
 
 }  // namespace clef

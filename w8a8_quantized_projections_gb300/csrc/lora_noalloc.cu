@@ -110,12 +110,6 @@ extern "C" int clef_lora_add_noalloc(const void *x, int64_t ldx, const void *A, 
 
     const int bn = r_pad == 64 ? 64 : (r_pad == 128 ? 128 : 256);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    CUtensorMap tx, ta, tt, tb;
-    if ((rc = internal_make_tmap_bf16(&tx, x, K, M, ldx * 2, 128))) return rc;
-    if ((rc = internal_make_tmap_bf16(&ta, A, K, r, K * 2, bn))) return rc;
-    if ((rc = internal_make_tmap_bf16(&tt, t, r_pad, M, r_pad * 2, 128))) return rc;
-    if ((rc = internal_make_tmap_bf16(&tb, B, r, N, r * 2, 256))) return rc;
-
     GemmArgs a1 = {};
     a1.M = (int)M;
     a1.N = (int)r_pad;
@@ -124,23 +118,18 @@ extern "C" int clef_lora_add_noalloc(const void *x, int64_t ldx, const void *A, 
     a1.ldo = r_pad;
     a1.status = status;
     a1.wait_limit_ns = 1000000000ull;
-    cudaError_t e = launch_gemm(kOpBF16, kEpiStoreBF16, bn, tx, ta, a1, num_sms, st);
-    if (e == cudaSuccess) {
-        GemmArgs a2 = {};
-        a2.M = (int)M;
-        a2.N = (int)N;
-        a2.K = (int)r_pad;
-        a2.out = y;
-        a2.ldo = ldy;
-        a2.status = status;
-        a2.wait_limit_ns = 1000000000ull;
-        e = launch_gemm(kOpBF16, kEpiAddBF16, 256, tt, tb, a2, num_sms, st);
-    }
-    if (e != cudaSuccess) {
-        char buf[160];
-        snprintf(buf, sizeof buf, "clef_lora_add_noalloc launch: %s", cudaGetErrorString(e));
-        internal_set_error(buf);
-        return CLEF_ERR_CUDA;
-    }
-    return CLEF_OK;
+    rc = launch_gemm(kOpBF16, kEpiStoreBF16, bn, Operand{x, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2},
+                     Operand{A, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2}, a1, num_sms, st);
+    if (rc) return rc;
+    GemmArgs a2 = {};
+    a2.M = (int)M;
+    a2.N = (int)N;
+    a2.K = (int)r_pad;
+    a2.out = y;
+    a2.ldo = ldy;
+    a2.status = status;
+    a2.wait_limit_ns = 1000000000ull;
+    return launch_gemm(kOpBF16, kEpiAddBF16, 256,
+                       Operand{t, (uint64_t)r_pad, (uint64_t)M, (uint64_t)r_pad * 2},
+                       Operand{B, (uint64_t)r, (uint64_t)N, (uint64_t)r * 2}, a2, num_sms, st);
 }
