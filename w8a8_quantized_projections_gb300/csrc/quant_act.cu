@@ -44,11 +44,14 @@ __device__ __forceinline__ void wht128_lanes(float (&v)[32], int lane) {
     }
 #pragma unroll
     for (int s = 1; s <= 2; s <<= 1) {   // strides 32 and 64
-        const bool upper = (lane & s) != 0; // this lane holds the i+h half
+        // The lane holding index i computes v[i] + v[i+h]; its partner holding
+        // i+h computes v[i] - v[i+h].  Both are one fma with an exact +-1
+        // product, so each is the single rounded add or subtract itself.
+        const float sgn = (lane & s) ? -1.0f : 1.0f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const float o = __shfl_xor_sync(kFull, v[j], s);
-            v[j] = upper ? __fsub_rn(o, v[j]) : __fadd_rn(v[j], o);
+            v[j] = __fmaf_rn(sgn, v[j], o);
         }
     }
     const float c = hadamard_c();
@@ -70,9 +73,13 @@ __device__ __forceinline__ void load_chunk(const uint16_t *p, float (&v)[32]) {
     }
 }
 
-__device__ __forceinline__ uint32_t pack_s8x4(int a, int b, int c, int d) {
-    return (uint32_t)(a & 0xFF) | ((uint32_t)(b & 0xFF) << 8) | ((uint32_t)(c & 0xFF) << 16) |
-           ((uint32_t)(d & 0xFF) << 24);
+// Four int32 codes (each already within [-127, 127]) packed as bytes q0..q3,
+// two conversions with saturation: hi = {q2, q3}, then {q0, q1} below it.
+__device__ __forceinline__ uint32_t pack_s8x4(int q0, int q1, int q2, int q3) {
+    uint32_t hi, w;
+    asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(q3), "r"(q2), "r"(0));
+    asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(w) : "r"(q1), "r"(q0), "r"(hi));
+    return w;
 }
 
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
@@ -81,8 +88,10 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return r;
 }
 
-template <int MODE, int C>
-__global__ void __launch_bounds__(1024) quant_act_kernel(const uint16_t *__restrict__ x,
+// MAXT / MINB: launch bounds.  Rows of up to 18,432 elements (576 threads)
+// are compiled for two resident CTAs per SM, so two rows stream at once.
+template <int MODE, int C, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB) quant_act_kernel(const uint16_t *__restrict__ x,
                                                          int64_t K, int64_t ldx,
                                                          uint8_t *__restrict__ q,
                                                          float *__restrict__ scale) {
@@ -128,7 +137,7 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const uint16_t *__restr
 
     const float qmax = kInt8 ? 127.0f : 448.0f;
     const bool zero_row = !(amax > 0.0f);
-    const float r = zero_row ? 0.0f : __fdiv_rn(qmax, amax);
+    const float r = zero_row ? 0.0f : __fdiv_rn(qmax, amax);  // zero row: every v * 0 = 0
     if (tid == 0) scale[m] = zero_row ? 0.0f : __fdiv_rn(amax, qmax);
 
     uint8_t *qr = q + m * K;
@@ -140,12 +149,11 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const uint16_t *__restr
         if (kInt8) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
+                // |v * r| <= 127 * (1 + 2^-23) for every v of the row, so the
+                // round-half-even conversion never leaves [-127, 127].
                 int t[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    int qi = zero_row ? 0 : __float2int_rn(__fmul_rn(v[c][4 * i + k], r));
-                    t[k] = max(-127, min(127, qi));
-                }
+                for (int k = 0; k < 4; ++k) t[k] = __float2int_rn(__fmul_rn(v[c][4 * i + k], r));
                 w[i] = pack_s8x4(t[0], t[1], t[2], t[3]);
             }
         } else {
@@ -170,13 +178,16 @@ template <int MODE>
 cudaError_t launch_mode(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q,
                         float *scale, cudaStream_t st) {
     const int64_t nchunk = K / 32;
-    if (nchunk <= 1024) {
+    if (nchunk <= 576) {
         const int T = (int)((nchunk + 31) / 32 * 32);
-        quant_act_kernel<MODE, 1><<<(unsigned)M, T, 0, st>>>(x, K, ldx, q, scale);
+        quant_act_kernel<MODE, 1, 576, 2><<<(unsigned)M, T, 0, st>>>(x, K, ldx, q, scale);
+    } else if (nchunk <= 1024) {
+        const int T = (int)((nchunk + 31) / 32 * 32);
+        quant_act_kernel<MODE, 1, 1024, 1><<<(unsigned)M, T, 0, st>>>(x, K, ldx, q, scale);
     } else {
         const int64_t per = (nchunk + 1) / 2;
         const int T = (int)((per + 31) / 32 * 32);
-        quant_act_kernel<MODE, 2><<<(unsigned)M, T, 0, st>>>(x, K, ldx, q, scale);
+        quant_act_kernel<MODE, 2, 1024, 1><<<(unsigned)M, T, 0, st>>>(x, K, ldx, q, scale);
     }
     return cudaGetLastError();
 }
