@@ -28,35 +28,87 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 
 __device__ __forceinline__ float hadamard_c() { return __uint_as_float(0x3DB504F3u); }
 
+// Packed fp32 pairs (sm_100 family): each lane of add/sub/mul/fma.rn.f32x2 is
+// the IEEE round-to-nearest-even operation on that lane alone, so results are
+// bit-identical to the scalar operations while issuing half as many.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unf2(uint64_t p, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // Rotate this thread's 32 values as part of a 128-block spread over lanes
-// (lane & 3) = 0..3 holding block positions 32*(lane & 3) + j.
+// (lane & 3) = 0..3 holding block positions 32*(lane & 3) + j.  The values are
+// held as pairs p[k] = (v[k], v[k+16]): strides 1..8 pair p[k] with p[k+h] in
+// both halves at once, stride 16 is the pair's own two halves, and strides 32
+// and 64 exchange with lanes xor 1 and xor 2.
 __device__ __forceinline__ void wht128_lanes(float (&v)[32], int lane) {
+    uint64_t p[16];
 #pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
+    for (int k = 0; k < 16; ++k) p[k] = f2(v[k], v[k + 16]);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            if ((j & h) == 0) {
-                const float a = v[j], b = v[j + h];
-                v[j] = __fadd_rn(a, b);
-                v[j + h] = __fsub_rn(a, b);
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if ((k & h) == 0) {
+                const uint64_t a = p[k], b = p[k + h];
+                p[k] = add2(a, b);
+                p[k + h] = sub2(a, b);
             }
         }
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {   // stride 16
+        float a, b;
+        unf2(p[k], a, b);
+        v[k] = __fadd_rn(a, b);
+        v[k + 16] = __fsub_rn(a, b);
     }
 #pragma unroll
     for (int s = 1; s <= 2; s <<= 1) {   // strides 32 and 64
         // The lane holding index i computes v[i] + v[i+h]; its partner holding
         // i+h computes v[i] - v[i+h].  Both are one fma with an exact +-1
         // product, so each is the single rounded add or subtract itself.
-        const float sgn = (lane & s) ? -1.0f : 1.0f;
+        const float sg = (lane & s) ? -1.0f : 1.0f;
+        const uint64_t sgn = f2(sg, sg);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float o = __shfl_xor_sync(kFull, v[j], s);
-            v[j] = __fmaf_rn(sgn, v[j], o);
+        for (int k = 0; k < 16; ++k) {
+            const float oa = __shfl_xor_sync(kFull, v[k], s);
+            const float ob = __shfl_xor_sync(kFull, v[k + 16], s);
+            const uint64_t r = fma2(sgn, f2(v[k], v[k + 16]), f2(oa, ob));
+            unf2(r, v[k], v[k + 16]);
         }
     }
     const float c = hadamard_c();
+    const uint64_t c2 = f2(c, c);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(v[j], c);
+    for (int k = 0; k < 16; ++k) {
+        const uint64_t r = mul2(f2(v[k], v[k + 16]), c2);
+        unf2(r, v[k], v[k + 16]);
+    }
 }
 
 __device__ __forceinline__ void load_chunk(const uint16_t *p, float (&v)[32]) {
@@ -151,10 +203,12 @@ __global__ void __launch_bounds__(MAXT, MINB) quant_act_kernel(const uint16_t *_
             for (int i = 0; i < 8; ++i) {
                 // |v * r| <= 127 * (1 + 2^-23) for every v of the row, so the
                 // round-half-even conversion never leaves [-127, 127].
-                int t[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) t[k] = __float2int_rn(__fmul_rn(v[c][4 * i + k], r));
-                w[i] = pack_s8x4(t[0], t[1], t[2], t[3]);
+                const uint64_t r2 = f2(r, r);
+                float u[4];
+                unf2(mul2(f2(v[c][4 * i], v[c][4 * i + 1]), r2), u[0], u[1]);
+                unf2(mul2(f2(v[c][4 * i + 2], v[c][4 * i + 3]), r2), u[2], u[3]);
+                w[i] = pack_s8x4(__float2int_rn(u[0]), __float2int_rn(u[1]), __float2int_rn(u[2]),
+                                 __float2int_rn(u[3]));
             }
         } else {
 #pragma unroll
