@@ -208,6 +208,16 @@ int clef_poll_status(void);
  */
 void clef_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * clef_test_force_timeout -- test knob for the device-side failure path.
+ * While on (non-zero), the W8A8/FP8/LoRA GEMM kernels launched afterwards
+ * make their MMA issuer wait on a barrier that nothing signals; the wait runs
+ * out after the clef_set_wait_limit_ns limit, CLEF_ERR_TIMEOUT is recorded in
+ * the status word and the kernel winds down (their outputs are then
+ * undefined).  Off by default.
+ */
+void clef_test_force_timeout(int on);
+
 /* Human-readable name of a status code (static string). */
 const char *clef_status_string(int status);
 

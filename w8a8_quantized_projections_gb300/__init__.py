@@ -245,3 +245,11 @@ def poll_status() -> int:
 
 def set_wait_limit_ns(ns: int) -> None:
     library().clef_set_wait_limit_ns(int(ns))
+
+
+def test_force_timeout(on: bool) -> None:
+    """Test knob: make the GEMM kernels' MMA issuer wait on a barrier nothing signals."""
+    L = library()
+    L.clef_test_force_timeout.argtypes = [C.c_int]
+    L.clef_test_force_timeout.restype = None
+    L.clef_test_force_timeout(1 if on else 0)

@@ -32,6 +32,7 @@ struct DeviceState {
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
 std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
+std::atomic<int> g_force_timeout{0};
 thread_local char g_last_err[256] = "";
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -125,6 +126,7 @@ GemmArgs base_args(const DeviceState *d, int64_t M, int64_t N, int64_t K) {
     a.K = (int)K;
     a.status = d->status;
     a.wait_limit_ns = g_wait_limit_ns.load();
+    a.force_timeout = g_force_timeout.load();
     return a;
 }
 
@@ -315,6 +317,8 @@ int clef_poll_status(void) {
 }
 
 void clef_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
+
+void clef_test_force_timeout(int on) { g_force_timeout.store(on ? 1 : 0); }
 
 const char *clef_status_string(int status) {
     switch (status) {

@@ -40,6 +40,7 @@ struct GemmArgs {
     unsigned int *status;    // device status word
     uint64_t wait_limit_ns;
     int *dbg;                // optional: per CTA, its own TMEM base and the one it uses
+    int force_timeout;       // test knob: make the MMA issuer's wait run out
 };
 
 // A row-major 2-D operand: rows of `inner` elements, `pitch` bytes apart.

@@ -105,6 +105,7 @@ struct Barriers {
     uint64_t raw_full[8], raw_empty[8];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t drain;
+    uint64_t never;      // nothing arrives here: the forced-timeout test waits on it
     uint32_t tmem_slot;
     int abort;
 };
@@ -303,6 +304,7 @@ struct Gemm {
         uint32_t rank;       // rank in the CTA pair (0 in single mode)
         int slot, nslots;    // tile-loop start and stride
         int num_m, num_n, num_tiles, nkb;
+        int force_timeout;   // test knob: the MMA issuer waits on a barrier nothing signals
         WaitCtx w;
     };
 
@@ -472,6 +474,10 @@ struct Gemm {
         constexpr uint32_t afmt = (OP == kOpBF16) ? 1u : 0u;  // F16 / BF16 / E4M3
         constexpr uint32_t idesc = idesc_f32acc(afmt, afmt, C::kTileRows, BN);
         uint32_t s = 0, ph = 0, acc = 0, aph = 0;
+        if (c.force_timeout) {
+            mbar_wait(&c.bar->never, 0, c.w, kSiteMmaFull);  // runs out; sets the abort flag
+            return;
+        }
         for (int t = c.slot; t < c.num_tiles; t += c.nslots) {
             for (int kb0 = 0; kb0 < c.nkb; kb0 += C::kChunkKBlocks) {
                 const int kb1 = min(c.nkb, kb0 + C::kChunkKBlocks);
@@ -700,6 +706,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             mbar_init(&bar->acc_empty[s], C::kAccEmptyArrivals);
         }
         mbar_init(&bar->drain, 1);
+        mbar_init(&bar->never, 1);
         bar->abort = 0;
         fence_barrier_init();
     }
@@ -747,6 +754,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     c.num_n = (args.N + C::kOutColsPerTile - 1) / C::kOutColsPerTile;
     c.num_tiles = c.num_m * c.num_n;
     c.nkb = C::kI8 ? (args.K + 63) / 64 : (args.K + C::BK - 1) / C::BK;
+    c.force_timeout = args.force_timeout;
     c.w.limit_ns = args.wait_limit_ns;
     c.w.abort = &bar->abort;
     c.w.status = args.status;
