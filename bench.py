@@ -324,11 +324,10 @@ def main():
     for key, lst in events.items():
         kt[key] = [a.elapsed_time(b) / 1e3 for a, b in lst]
     gemm_keys = [k for k in kt if k[0] == "gemm"]
-    proj = {p.name: p for p in cfg.projections}
+    units = {u[0]: u for u in layer.units()}   # name -> (name, weight rows, K, ops)
     dom = max(gemm_keys, key=lambda k: sum(kt[k]))
-    dom_p = proj[dom[1]]
+    dom_name, dom_rows, dom_K, dom_ops = units[dom[1]]
     dom_t = statistics.mean(kt[dom])
-    dom_ops = dom_p.ops(cfg.M)
     achieved = dom_ops / dom_t / 1e12
     q_bytes = 0
     q_time = 0.0
@@ -349,13 +348,13 @@ def main():
         "dtype": "fp8" if cfg.scheme == "fp8" else "int8", "data": "synthetic",
         "config": workload_config(cfg),
         "roofline": {
-            "kernel": f"{'fp8' if cfg.scheme == 'fp8' else 'w8a8'} {dom_p.name} GEMM "
-                      f"({cfg.M}x{dom_p.weight_rows}x{dom_p.K})",
+            "kernel": f"{'fp8' if cfg.scheme == 'fp8' else 'w8a8'} {dom_name} GEMM "
+                      f"({cfg.M}x{dom_rows}x{dom_K})",
             "bound": "tensor", "achieved": achieved,
             "peak": bf16_peak * (2.0 if cfg.scheme == "fp8" else 1.0),
             "unit": "TFLOP/s",
             "frac": achieved / (bf16_peak * (2.0 if cfg.scheme == "fp8" else 1.0)),
-            "traffic": measured_traffic(cfg, dom_p.name),
+            "traffic": measured_traffic(cfg, dom_name),
             "traffic_unit": "bytes per launch",
             "peak_source": (f"{peak_src} bf16 dense burst x2 (fp8 nominal ratio)" if cfg.scheme == "fp8"
                             else f"{peak_src} bf16 dense burst (INT8 runs exactly on the fp16 tensor "

@@ -218,6 +218,19 @@ void clef_set_wait_limit_ns(uint64_t ns);
  */
 void clef_test_force_timeout(int on);
 
+/*
+ * clef_set_quant_staging -- which quantizer kernel clef_quant_act launches
+ * afterwards.  Two kernels compute the same codes and scales bit for bit: a
+ * persistent one that stages rows in shared memory through TMA (for row
+ * lengths that are a multiple of 64 and at most 32768) and a one-CTA-per-row
+ * one (every row length).  mode 1 (default): the staged kernel for calls of
+ * at least 8 rows per SM, where it streams faster; mode 2: the staged kernel
+ * wherever the row length allows; mode 0: always the per-row kernel.  Other
+ * values are clamped to this range.  The switch exists so that each kernel
+ * can be tested and timed.
+ */
+void clef_set_quant_staging(int mode);
+
 /* Human-readable name of a status code (static string). */
 const char *clef_status_string(int status);
 

@@ -40,9 +40,19 @@ def special_rows(x: np.ndarray) -> np.ndarray:
 
 # ------------------------------------------------------------------ quantizer
 
+@pytest.fixture(params=[2, 0], ids=["staged", "per_row"])
+def staging(request):
+    """Run a quantizer test with the TMA-staged persistent kernel (wherever the
+    row length allows it, whatever the row count) and with the
+    one-CTA-per-row kernel."""
+    clef.set_quant_staging(request.param)
+    yield request.param
+    clef.set_quant_staging(1)
+
+
 @pytest.mark.parametrize("M,K", [(298, 2048), (1, 128), (5, 384), (130, 5120), (1502, 17408),
-                                 (2270, 6144), (3, 40960)])
-def test_quant_int8_h128_bitexact(orc, M, K):
+                                 (2270, 6144), (3, 40960), (12000, 5120), (2, 128 * 131)])
+def test_quant_int8_h128_bitexact(orc, staging, M, K):
     x = special_rows(S.activation(0, f"t/q8/{M}x{K}", M, K))
     q, s = clef.quant_act(bf16_dev(x), "int8_h128")
     rq, rs = par_rows(lambda a, b: orc.quant_int8_h128(x[a:b]), M)
@@ -50,7 +60,7 @@ def test_quant_int8_h128_bitexact(orc, M, K):
     assert np.array_equal(host(q), rq)
 
 
-def test_quant_strided_rows(orc):
+def test_quant_strided_rows(orc, staging):
     M, K, ld = 37, 1024, 1536
     big = S.activation(0, "t/q8/strided", M, ld)
     xt = bf16_dev(big)[:, :K]
@@ -60,8 +70,10 @@ def test_quant_strided_rows(orc):
 
 
 @pytest.mark.parametrize("mode", ["fp8", "fp8_h128"])
-@pytest.mark.parametrize("M,K", [(1502, 4096), (7, 12288), (33, 640), (1, 128)])
-def test_quant_fp8_bitexact(orc, mode, M, K):
+@pytest.mark.parametrize("M,K", [(1502, 4096), (7, 12288), (33, 640), (1, 128), (9, 96)])
+def test_quant_fp8_bitexact(orc, staging, mode, M, K):
+    if mode == "fp8_h128" and K % 128:
+        pytest.skip("the rotated mode needs whole 128-blocks")
     x = special_rows(S.activation(0, f"t/q8f/{M}x{K}", M, K))
     q, s = clef.quant_act(bf16_dev(x), mode)
     rq, rs = par_rows(lambda a, b: orc.quant_fp8(x[a:b], rotate=(mode == "fp8_h128")), M)
@@ -152,6 +164,26 @@ def test_w8a8_gateup_swiglu(orc, M, N, K):
     h = bf16_host(clef.w8a8_gateup_swiglu(dev(qx), dev(sx), dev(qw), dev(sw), bf16_dev(b)))
     ref = par_rows(lambda a, c: orc.int8_gateup_swiglu(qx[a:c], sx[a:c], qw, sw, b), M)
     assert_bf16_within(h, ref, 1.0, "swiglu")
+
+
+def test_w8a8_gateup_swiglu_wide_gate_range(orc):
+    """Gate values from about -200 to +200 (gate scales spread over four
+    decades), so silu meets its saturated ends: exp(-g) overflowing to
+    infinity, denominators beyond 2^126, and silu(g) = g."""
+    M, N, K = 130, 256, 256
+    rng = np.random.default_rng(5)
+    qx = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    qw = rng.integers(-127, 128, (2 * N, K)).astype(np.int8)
+    sx = np.ones(M, np.float32)
+    sw = np.empty(2 * N, np.float32)
+    sw[:N] = (10.0 ** np.linspace(-6, -2.3, N)).astype(np.float32)
+    sw[N:] = np.float32(1e-4)
+    b = S.bias(0, "t/gu/wide/b", 2 * N)
+    h = bf16_host(clef.w8a8_gateup_swiglu(dev(qx), dev(sx), dev(qw), dev(sw), bf16_dev(b)))
+    ref = orc.int8_gateup_swiglu(qx, sx, qw, sw, b)
+    g = (qx.astype(np.int64) @ qw[:N].T.astype(np.int64)) * sw[:N].astype(np.float64)
+    assert g.min() < -90 and g.max() > 90
+    assert_bf16_within(h, ref, 1.0, "swiglu wide gate")
 
 
 def test_swiglu_bf16(orc):

@@ -22,7 +22,7 @@ from . import build as _build
 __all__ = [
     "ClefError", "library", "library_path", "quant_act", "w8a8_linear", "w8a8_gateup_swiglu",
     "fp8_linear", "fp8_gateup_swiglu", "lora_add", "lora_add_noalloc", "swiglu_bf16", "w8a8_gemm_s32",
-    "poll_status", "set_wait_limit_ns", "ACT_MODES",
+    "poll_status", "set_wait_limit_ns", "set_quant_staging", "ACT_MODES",
 ]
 
 ACT_MODES = {"int8_h128": 0, "fp8": 1, "fp8_h128": 2}
@@ -245,6 +245,16 @@ def poll_status() -> int:
 
 def set_wait_limit_ns(ns: int) -> None:
     library().clef_set_wait_limit_ns(int(ns))
+
+
+def set_quant_staging(mode: int) -> None:
+    """Choose the quantizer kernel: 1 (default) the TMA-staged persistent one
+    for large calls, 2 the staged one wherever the row length suits it, 0
+    always the one-CTA-per-row kernel."""
+    L = library()
+    L.clef_set_quant_staging.argtypes = [C.c_int]
+    L.clef_set_quant_staging.restype = None
+    L.clef_set_quant_staging(int(mode))
 
 
 def test_force_timeout(on: bool) -> None:

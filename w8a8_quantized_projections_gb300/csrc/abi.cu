@@ -33,6 +33,7 @@ DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
 std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
 std::atomic<int> g_force_timeout{0};
+std::atomic<int> g_quant_staging{1};
 thread_local char g_last_err[256] = "";
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -195,6 +196,32 @@ int internal_make_tmap(CUtensorMap *m, CUtensorMapDataType dt, const void *base,
     return make_tmap(m, dt, base, inner, rows, pitch_bytes, box_inner, box_rows, sw);
 }
 
+int internal_make_tmap_nd(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *base,
+                          const uint64_t *dims, const uint64_t *strides, const uint32_t *box,
+                          CUtensorMapSwizzle sw) {
+    if (rank < 1 || rank > 5) return arg_fail("tensor-map rank");
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    if (!g_encode) {
+        snprintf(g_last_err, sizeof g_last_err, "tensor-map encoder not initialised (no device set-up)");
+        return CLEF_ERR_CUDA;
+    }
+    CUresult r = g_encode(m, dt, (cuuint32_t)rank, const_cast<void *>(base), d, st, b, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_err, sizeof g_last_err, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+        return CLEF_ERR_INVALID_ARG;
+    }
+    return CLEF_OK;
+}
+
 int internal_cuda_error(cudaError_t e, const char *what) { return cuda_fail(e, what); }
 
 void internal_set_error(const char *msg) { snprintf(g_last_err, sizeof g_last_err, "%s", msg); }
@@ -221,8 +248,14 @@ int clef_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, int mode, v
     DeviceState *d = nullptr;
     int rc = device_state(&d);
     if (rc) return rc;
+    QuantEnv env;
+    env.num_sms = d->num_sms;
+    env.status = d->status;
+    env.wait_limit_ns = g_wait_limit_ns.load();
+    env.staging = g_quant_staging.load();
     cudaError_t e = launch_quant_act(mode, static_cast<const uint16_t *>(x), M, K, ldx,
-                                     static_cast<uint8_t *>(q), scale, static_cast<cudaStream_t>(stream));
+                                     static_cast<uint8_t *>(q), scale, env,
+                                     static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CLEF_OK : cuda_fail(e, "quantizer launch");
 }
 
@@ -319,6 +352,8 @@ int clef_poll_status(void) {
 void clef_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
 
 void clef_test_force_timeout(int on) { g_force_timeout.store(on ? 1 : 0); }
+
+void clef_set_quant_staging(int mode) { g_quant_staging.store(mode < 0 ? 0 : (mode > 2 ? 2 : mode)); }
 
 const char *clef_status_string(int status) {
     switch (status) {

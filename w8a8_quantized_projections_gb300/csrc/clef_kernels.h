@@ -10,8 +10,19 @@ namespace clef {
 
 enum ActMode : int { kActInt8H128 = 0, kActFp8 = 1, kActFp8H128 = 2 };
 
+// What the quantizer launch needs from the device set-up.  staging: 0 =
+// always the one-CTA-per-row kernel; 1 = the persistent TMA-staged kernel for
+// calls of at least 8 rows per SM whose row length suits it; 2 = the staged
+// kernel wherever the row length suits it.
+struct QuantEnv {
+    int num_sms;
+    unsigned int *status;
+    uint64_t wait_limit_ns;
+    int staging;
+};
+
 cudaError_t launch_quant_act(int mode, const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
-                             uint8_t *q, float *scale, cudaStream_t st);
+                             uint8_t *q, float *scale, const QuantEnv &env, cudaStream_t st);
 
 // Operand kinds of the tensor-core GEMM.
 enum GemmOp : int {
@@ -68,6 +79,11 @@ int internal_device(int *num_sms, unsigned int **status);
 int internal_make_tmap(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
                        uint64_t rows, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows,
                        CUtensorMapSwizzle sw);
+// rank-dimensional tensor map: dims[0] innermost, strides[i] = byte pitch of
+// dimension i + 1, box[i] elements per copy; zero fill outside the tensor.
+int internal_make_tmap_nd(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *base,
+                          const uint64_t *dims, const uint64_t *strides, const uint32_t *box,
+                          CUtensorMapSwizzle sw);
 void internal_set_error(const char *msg);
 int internal_cuda_error(cudaError_t e, const char *what);  // records the text, returns CLEF_ERR_CUDA
 

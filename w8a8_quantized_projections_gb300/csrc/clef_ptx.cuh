@@ -18,7 +18,7 @@ enum : unsigned int {
 // Site codes recorded in bits 8..15 of the status word on a timeout.
 enum WaitSite : unsigned int {
     kSiteTmaEmpty = 1, kSiteMmaFull = 2, kSiteMmaAccEmpty = 3, kSiteEpiAccFull = 4,
-    kSiteConvRaw = 5, kSiteConvEmpty = 6, kSiteDrain = 7,
+    kSiteConvRaw = 5, kSiteConvEmpty = 6, kSiteDrain = 7, kSiteQuantFull = 8,
 };
 
 // The library-owned device status word lives in abi.cu; kernels receive its

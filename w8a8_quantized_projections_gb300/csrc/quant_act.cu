@@ -1,8 +1,17 @@
 // quant_act.cu -- per-token activation quantizer (HBM-bound).
 //
-// One CTA per row.  Each thread owns one 32-element chunk of the row (two
-// chunks for rows longer than 32768): four 16-byte loads of bf16, widened to
-// fp32 in registers.  A 128-block of the row spans four neighbouring lanes,
+// Two kernels compute the same thing.  The staged kernel (rows whose length
+// is a multiple of 64 and fits the shared-memory ring, which covers every
+// projection width of the workloads) is persistent: each CTA owns a ring of
+// row slots in shared memory that TMA fills several rows ahead (128-byte
+// swizzled, so that the threads' 16-byte reads are free of bank conflicts),
+// and several CTAs share an SM, so HBM sees a steady stream of row reads
+// while earlier rows are rotated and coded.  The fallback kernel runs one
+// CTA per row with direct 16-byte loads.
+//
+// In both, each thread owns one 32-element chunk of the row (two chunks for
+// rows longer than 32768 in the fallback): four 16-byte pieces of bf16,
+// widened to fp32 in registers.  A 128-block of the row spans four neighbouring lanes,
 // so the Walsh-Hadamard butterfly runs its strides 1..16 inside a thread and
 // strides 32 and 64 as lane exchanges (xor 1, xor 2), in the fixed order
 // 1, 2, 4, ..., 64 with explicitly rounded fp32 add/sub (no contraction),
@@ -19,6 +28,7 @@
 #include <cuda_runtime.h>
 
 #include "clef_kernels.h"
+#include "clef_ptx.cuh"
 
 namespace clef {
 
@@ -140,6 +150,41 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return r;
 }
 
+// Codes of one 32-element chunk (r = qmax / amax of the row), written as two
+// 16-byte stores.
+template <bool kInt8>
+__device__ __forceinline__ void store_codes(const float (&v)[32], float r, bool zero_row,
+                                            uint8_t *dst8) {
+    uint32_t w[8];
+    if (kInt8) {
+        const uint64_t r2 = f2(r, r);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            // |v * r| <= 127 * (1 + 2^-23) for every v of the row, so the
+            // round-half-even conversion never leaves [-127, 127].
+            float u[4];
+            unf2(mul2(f2(v[4 * i], v[4 * i + 1]), r2), u[0], u[1]);
+            unf2(mul2(f2(v[4 * i + 2], v[4 * i + 3]), r2), u[2], u[3]);
+            w[i] = pack_s8x4(__float2int_rn(u[0]), __float2int_rn(u[1]), __float2int_rn(u[2]),
+                             __float2int_rn(u[3]));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (zero_row) {
+                w[i] = 0u;
+            } else {
+                const float *u = &v[4 * i];
+                w[i] = e4m3x2(__fmul_rn(u[0], r), __fmul_rn(u[1], r)) |
+                       (e4m3x2(__fmul_rn(u[2], r), __fmul_rn(u[3], r)) << 16);
+            }
+        }
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(dst8);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
 // MAXT / MINB: launch bounds.  Rows of up to 18,432 elements (576 threads)
 // are compiled for two resident CTAs per SM, so two rows stream at once.
 template <int MODE, int C, int MAXT, int MINB>
@@ -197,40 +242,229 @@ __global__ void __launch_bounds__(MAXT, MINB) quant_act_kernel(const uint16_t *_
     for (int c = 0; c < C; ++c) {
         const int ch = tid + c * blockDim.x;
         if (ch >= nchunk) continue;
-        uint32_t w[8];
-        if (kInt8) {
+        store_codes<kInt8>(v[c], r, zero_row, qr + 32 * (int64_t)ch);
+    }
+}
+
+// ---------------------------------------------------------------- staged kernel
+
+constexpr int kMaxSlots = 8;
+
+// 3-D tile load (row view [M][K/64][64] of bf16) into shared memory.
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m, int32_t c0,
+                                            int32_t c1, int32_t c2, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2),
+          "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Persistent quantizer.  CTA b handles rows b, b + G, b + 2G, ... (G = grid
+// size); slot it % nslot of its ring holds the row of iteration it.  A row
+// is K/64 128-byte lines of 64 bf16, copied as nbox boxes of box_rows lines
+// with the 128-byte swizzle: 16-byte unit u of line l lands at unit
+// u ^ (l & 7).  Thread t owns chunk t (32 elements), the half t & 1 of line
+// t >> 1, so its four pieces sit at units (4 (t & 1) + j) ^ ((t >> 1) & 7):
+// every quarter-warp's eight 16-byte reads hit eight different bank groups.
+// One block barrier per row: it publishes the warps' absmax (double-buffered
+// by row parity) and certifies that every thread has read the slot, after
+// which thread 0 refills it with the row nslot iterations ahead.
+template <int MODE, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB)
+quant_staged_kernel(const __grid_constant__ CUtensorMap tmx, int M, int K, int nslot,
+                    uint32_t slot_stride, int nbox, int box_rows, uint8_t *__restrict__ q,
+                    float *__restrict__ scale, unsigned int *status, uint64_t limit_ns) {
+    constexpr bool kRotate = (MODE == kActInt8H128 || MODE == kActFp8H128);
+    constexpr bool kInt8 = (MODE == kActInt8H128);
+    extern __shared__ uint8_t dyn[];
+    __shared__ uint64_t full[kMaxSlots];
+    __shared__ float red[2][32];
+    __shared__ int abort_flag;
+
+    const uint32_t base = smem_u32(dyn);
+    uint8_t *ring = dyn + (((base + 1023u) & ~1023u) - base);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nw = (int)(blockDim.x >> 5);
+    const int nchunk = K >> 5;
+    const uint32_t row_bytes = (uint32_t)K * 2u;
+
+    if (tid == 0) {
+        for (int s = 0; s < nslot; ++s) mbar_init(&full[s], 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    WaitCtx w;
+    w.limit_ns = limit_ns;
+    w.abort = &abort_flag;
+    w.status = status;
+
+    auto issue = [&](int slot, int m) {
+        uint8_t *dst = ring + (uint32_t)slot * slot_stride;
+        mbar_arrive_expect_tx(&full[slot], row_bytes);
+        for (int b = 0; b < nbox; ++b)
+            tma_load_3d(dst + (uint32_t)(b * box_rows) * 128u, &tmx, 0, b * box_rows, m, &full[slot]);
+    };
+    if (tid == 0) {
+        tma_prefetch_desc(&tmx);
+        for (int s = 0; s < nslot; ++s) {
+            const int m = (int)blockIdx.x + s * (int)gridDim.x;
+            if (m < M) issue(s, m);
+        }
+    }
+
+    const bool active = tid < nchunk;
+    const uint32_t line = (uint32_t)(tid >> 1);
+    uint32_t off[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                // |v * r| <= 127 * (1 + 2^-23) for every v of the row, so the
-                // round-half-even conversion never leaves [-127, 127].
-                const uint64_t r2 = f2(r, r);
-                float u[4];
-                unf2(mul2(f2(v[c][4 * i], v[c][4 * i + 1]), r2), u[0], u[1]);
-                unf2(mul2(f2(v[c][4 * i + 2], v[c][4 * i + 3]), r2), u[2], u[3]);
-                w[i] = pack_s8x4(__float2int_rn(u[0]), __float2int_rn(u[1]), __float2int_rn(u[2]),
-                                 __float2int_rn(u[3]));
+    for (int j = 0; j < 4; ++j) off[j] = line * 128u + (((uint32_t)((tid & 1) * 4 + j) ^ (line & 7u)) << 4);
+
+    int it = 0;
+    for (int m = (int)blockIdx.x; m < M; m += (int)gridDim.x, ++it) {
+        const int slot = it % nslot;
+        mbar_wait(&full[slot], (uint32_t)(it / nslot) & 1u, w, kSiteQuantFull);
+        float v[32];
+        if (active) {
+            const uint32_t src = smem_u32(ring) + (uint32_t)slot * slot_stride;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t a0, a1, a2, a3;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(src + off[j]));
+                const uint32_t ws[4] = {a0, a1, a2, a3};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    v[8 * j + 2 * k] = __uint_as_float(ws[k] << 16);
+                    v[8 * j + 2 * k + 1] = __uint_as_float(ws[k] & 0xFFFF0000u);
+                }
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if (zero_row) {
-                    w[i] = 0u;
-                } else {
-                    const float *u = &v[c][4 * i];
-                    w[i] = e4m3x2(__fmul_rn(u[0], r), __fmul_rn(u[1], r)) |
-                           (e4m3x2(__fmul_rn(u[2], r), __fmul_rn(u[3], r)) << 16);
+            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+        }
+        // whole 128-blocks are active or inactive together (nchunk % 4 == 0
+        // in the rotated modes), and every lane of the warp exists
+        if (kRotate) wht128_lanes(v, lane);
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, sh));
+        if (lane == 0) red[it & 1][warp] = amax;
+        __syncthreads();
+        if (abort_flag) break;
+        if (tid == 0) {
+            const int mn = m + nslot * (int)gridDim.x;
+            if (mn < M) {
+                fence_proxy_async_smem();
+                issue(slot, mn);
+            }
+        }
+        amax = red[it & 1][0];
+        for (int k = 1; k < nw; ++k) amax = fmaxf(amax, red[it & 1][k]);
+
+        const float qmax = kInt8 ? 127.0f : 448.0f;
+        const bool zero_row = !(amax > 0.0f);
+        const float r = zero_row ? 0.0f : __fdiv_rn(qmax, amax);  // zero row: every v * 0 = 0
+        if (tid == 0) scale[m] = zero_row ? 0.0f : __fdiv_rn(amax, qmax);
+        if (active) store_codes<kInt8>(v, r, zero_row, q + (int64_t)m * K + 32 * tid);
+    }
+    if (abort_flag && tid == 0) {
+        // let the copies already issued into the ring land before the CTA exits
+        for (int k = it; k < it + nslot; ++k) {
+            const int m = (int)blockIdx.x + k * (int)gridDim.x;
+            if (m >= M) break;
+            const uint32_t a = smem_u32(&full[k % nslot]);
+            const uint64_t t0 = globaltimer_ns();
+            for (uint32_t n = 0;; ++n) {
+                if (mbar_try_wait(a, (uint32_t)(k / nslot) & 1u)) break;
+                if ((n & 63u) == 63u && globaltimer_ns() - t0 > 200000000ull) {
+                    record_status(status, kStatusTimeout | (kSiteDrain << 8));
+                    break;
                 }
             }
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(qr + 32 * (int64_t)ch);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
     }
+}
+
+// Staged launch plan: slots per CTA and CTAs per SM for a row of K elements,
+// or false when the row does not suit the staged kernel.
+struct StagedPlan {
+    int threads, nslot, nbox, box_rows, ctas_per_sm;
+    uint32_t slot_stride, smem;
+};
+
+bool staged_plan(int64_t K, StagedPlan &p) {
+    if (K % 64 != 0 || K / 32 > 1024) return false;
+    const int lines = (int)(K / 64);
+    int nbox = (lines + 255) / 256;
+    // several boxes per row start on 1024-byte boundaries (whole swizzle atoms)
+    while (nbox <= 8 && nbox > 1 && (lines % nbox != 0 || (lines / nbox) % 8 != 0)) ++nbox;
+    if (nbox > 8) return false;
+    p.nbox = nbox;
+    p.box_rows = lines / nbox;
+    p.threads = (int)((K / 32 + 31) / 32 * 32);
+    p.slot_stride = (uint32_t)((K * 2 + 1023) / 1024 * 1024);
+    // about 1,152 threads per SM (registers for 56 per thread), 220 KB of ring
+    const uint32_t budget = 220u * 1024u;
+    int want = 1152 / p.threads;
+    want = want < 1 ? 1 : (want > 8 ? 8 : want);
+    for (int P = want; P >= 1; --P) {
+        const uint32_t per = budget / (uint32_t)P;
+        if (per < 1024u + 2u * p.slot_stride) continue;
+        int S = (int)((per - 1024u) / p.slot_stride);
+        if (S > kMaxSlots) S = kMaxSlots;
+        p.nslot = S;
+        p.ctas_per_sm = P;
+        p.smem = (uint32_t)S * p.slot_stride + 1024u;
+        return true;
+    }
+    return false;
+}
+
+template <int MODE, int MAXT, int MINB>
+cudaError_t launch_staged(const StagedPlan &p, const uint16_t *x, int64_t M, int64_t K,
+                          int64_t ldx, uint8_t *q, float *scale, const QuantEnv &env,
+                          cudaStream_t st) {
+    CUtensorMap tm;
+    const uint64_t dims[3] = {64, (uint64_t)(K / 64), (uint64_t)M};
+    const uint64_t strides[2] = {128, (uint64_t)ldx * 2};
+    const uint32_t box[3] = {64, (uint32_t)p.box_rows, 1};
+    if (internal_make_tmap_nd(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    auto kern = quant_staged_kernel<MODE, MAXT, MINB>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+    if (e != cudaSuccess) return e;
+    // resident CTAs per SM, cached per row length (K / 64 <= 512 here)
+    static int resident_by_lines[513] = {0};
+    int resident = resident_by_lines[K / 64];
+    if (resident == 0) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kern, p.threads, p.smem);
+        if (e != cudaSuccess) return e;
+        if (resident < 1) return cudaErrorInvalidConfiguration;
+        resident_by_lines[K / 64] = resident;
+    }
+    const int per_sm = resident < p.ctas_per_sm ? resident : p.ctas_per_sm;
+    const int64_t want = (int64_t)per_sm * env.num_sms;
+    const int grid = (int)(M < want ? M : want);
+    kern<<<grid, p.threads, p.smem, st>>>(tm, (int)M, (int)K, p.nslot, p.slot_stride, p.nbox,
+                                          p.box_rows, q, scale, env.status, env.wait_limit_ns);
+    return cudaGetLastError();
 }
 
 template <int MODE>
 cudaError_t launch_mode(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q,
-                        float *scale, cudaStream_t st) {
+                        float *scale, const QuantEnv &env, cudaStream_t st) {
+    StagedPlan p;
+    // a few rows per SM or fewer: the per-row kernel starts sooner
+    const bool want = env.staging == 2 || (env.staging == 1 && M >= 8 * (int64_t)env.num_sms);
+    if (want && staged_plan(K, p)) {
+        if (p.threads <= 576) return launch_staged<MODE, 576, 2>(p, x, M, K, ldx, q, scale, env, st);
+        return launch_staged<MODE, 1024, 1>(p, x, M, K, ldx, q, scale, env, st);
+    }
     const int64_t nchunk = K / 32;
     if (nchunk <= 576) {
         const int T = (int)((nchunk + 31) / 32 * 32);
@@ -249,11 +483,11 @@ cudaError_t launch_mode(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, ui
 }  // namespace
 
 cudaError_t launch_quant_act(int mode, const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
-                             uint8_t *q, float *scale, cudaStream_t st) {
+                             uint8_t *q, float *scale, const QuantEnv &env, cudaStream_t st) {
     switch (mode) {
-        case kActInt8H128: return launch_mode<kActInt8H128>(x, M, K, ldx, q, scale, st);
-        case kActFp8: return launch_mode<kActFp8>(x, M, K, ldx, q, scale, st);
-        case kActFp8H128: return launch_mode<kActFp8H128>(x, M, K, ldx, q, scale, st);
+        case kActInt8H128: return launch_mode<kActInt8H128>(x, M, K, ldx, q, scale, env, st);
+        case kActFp8: return launch_mode<kActFp8>(x, M, K, ldx, q, scale, env, st);
+        case kActFp8H128: return launch_mode<kActFp8H128>(x, M, K, ldx, q, scale, env, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -8,6 +8,15 @@ model card's Quantization table describes), packs gate and up side by side
 and preallocates every activation-code, scale, scratch and output buffer so
 that a ``step`` launches kernels only.
 
+Consecutive plain projections that read the same activation (q, k and v read
+the same hidden state) are packed the same way: their weight rows, scales
+and biases are stacked at set-up and one GEMM call writes all of their
+outputs into one [M][N_q + N_k + N_v] buffer, of which each projection's
+output is a column slice.  Every output element is the same function of the
+same row and column as in separate calls (per-row scales, per-output-channel
+weight scales, no split of K), so packing changes no bit; it only gives the
+small k and v projections the tile count of one wide GEMM.
+
 A step runs, per distinct activation tensor, one quantizer call, then per
 projection one GEMM call (gate/up with the fused SwiGLU epilogue).  With
 runtime LoRA pairs, every adapted projection adds ``bf16(x A^T) B^T`` after
@@ -28,28 +37,57 @@ from . import (fp8_gateup_swiglu, fp8_linear, lora_add, lora_pad, quant_act, swi
 class QuantizedLayer:
     def __init__(self, cfg, weights: Dict[str, Tuple[torch.Tensor, Optional[torch.Tensor]]],
                  lora: Optional[Dict[str, Tuple[torch.Tensor, torch.Tensor]]] = None,
-                 device="cuda"):
+                 device="cuda", pack_shared_input: bool = True):
         """weights: projection name -> (W bf16 [rows][K], bias bf16 [rows] or None);
-        lora: name (or name + "/gate", name + "/up" for gate/up) -> (A, B)."""
+        lora: name (or name + "/gate", name + "/up" for gate/up) -> (A, B);
+        pack_shared_input: run consecutive plain projections of one activation
+        as one packed GEMM."""
         self.cfg = cfg
         self.M = cfg.M
         self.fp8 = cfg.scheme == "fp8"
         self.mode = "fp8" if self.fp8 else "int8_h128"
         self.lora = lora or {}
-        self.w = {}
-        for p in cfg.projections:
-            W, b = weights[p.name]
-            qw, sw = quant_act(W, self.mode)
-            self.w[p.name] = (qw, sw, b)
-        torch.cuda.synchronize()
         M = self.M
+        self.groups = _groups(cfg.projections, weights) if pack_shared_input else \
+            [[p] for p in cfg.projections]
+        # quantized weights per launch unit; self.w[name] are row views of them
+        self.w = {}
+        self.unit_w = []
+        for g in self.groups:
+            if len(g) == 1:
+                W, b = weights[g[0].name]
+            else:
+                W = torch.cat([weights[p.name][0] for p in g], dim=0)
+                bs = [weights[p.name][1] for p in g]
+                b = None if bs[0] is None else torch.cat(bs, dim=0)
+            qw, sw = quant_act(W, self.mode)
+            self.unit_w.append((qw, sw, b))
+            r0 = 0
+            for p in g:
+                r1 = r0 + p.weight_rows
+                self.w[p.name] = (qw[r0:r1], sw[r0:r1], None if b is None else b[r0:r1])
+                r0 = r1
+        torch.cuda.synchronize()
         code = torch.uint8 if self.fp8 else torch.int8
         self.q = {}
         for name, K in cfg.activations():
             self.q[name] = (torch.empty((M, K), dtype=code, device=device),
                             torch.empty((M,), dtype=torch.float32, device=device))
         self.out = {}
+        self.unit_out = []
+        for g in self.groups:
+            if len(g) > 1:
+                packed = torch.empty((M, sum(p.N for p in g)), dtype=torch.bfloat16, device=device)
+                self.unit_out.append(packed)
+                c0 = 0
+                for p in g:
+                    self.out[p.name] = packed[:, c0:c0 + p.N]
+                    c0 += p.N
+            else:
+                self.unit_out.append(None)
         for p in cfg.projections:
+            if p.name in self.out:
+                continue
             if p.kind == "gateup":
                 self.out[p.name] = torch.empty((M, p.N), dtype=torch.bfloat16, device=device)
                 if self.lora:
@@ -67,10 +105,18 @@ class QuantizedLayer:
             if r_pad not in self.t:
                 self.t[r_pad] = torch.empty((M, r_pad), dtype=torch.bfloat16, device=device)
 
+    def units(self):
+        """The GEMM launches of a step: (event name, weight rows, K, 2*M*rows*K)."""
+        out = []
+        for g in self.groups:
+            rows = sum(p.weight_rows for p in g)
+            out.append((_unit_name(g), rows, g[0].K, 2 * self.M * rows * g[0].K))
+        return out
+
     def launches_per_step(self) -> int:
-        n = len(self.cfg.activations())
+        n = len(self.cfg.activations()) + len(self.groups)
         for p in self.cfg.projections:
-            n += 1 + (1 if p.chained else 0)
+            n += 1 if p.chained else 0
             if self.lora:
                 n += 4 if p.kind == "gateup" else 2   # each LoRA add is two GEMM launches
                 if p.kind == "gateup":
@@ -91,8 +137,20 @@ class QuantizedLayer:
             with ev("quant", name):
                 quant_act(acts[name], self.mode, q=qx, scale=sx)
         prev_h = None
-        for p in self.cfg.projections:
-            qw, sw, b = self.w[p.name]
+        for gi, g in enumerate(self.groups):
+            if len(g) > 1:
+                qw, sw, b = self.unit_w[gi]
+                qx, sx = self.q[g[0].act]
+                with ev("gemm", _unit_name(g)):
+                    lin(qx, sx, qw, sw, b, y=self.unit_out[gi])
+                for p in g:
+                    if self.lora and p.name in self.lora:
+                        A, B = self.lora[p.name]
+                        with ev("lora", p.name):
+                            lora_add(acts[p.act], A, B, self.out[p.name], t_scratch=self._t(A))
+                continue
+            p = g[0]
+            qw, sw, b = self.unit_w[gi]
             if p.chained:
                 qx, sx = self.q[p.act]
                 with ev("quant", p.act):
@@ -129,6 +187,25 @@ class QuantizedLayer:
 
     def _t(self, A):
         return self.t[lora_pad(A.shape[0])]
+
+
+def _unit_name(group) -> str:
+    return "+".join(p.name for p in group)
+
+
+def _groups(projections, weights):
+    """Runs of consecutive plain, unchained projections reading the same
+    activation with the same K (and all with or all without bias)."""
+    groups = []
+    for p in projections:
+        g = groups[-1] if groups else None
+        if (g is not None and p.kind == "linear" and not p.chained and g[-1].kind == "linear"
+                and not g[-1].chained and g[-1].act == p.act and g[-1].K == p.K
+                and (weights[g[-1].name][1] is None) == (weights[p.name][1] is None)):
+            g.append(p)
+        else:
+            groups.append([p])
+    return groups
 
 
 class _Rec:
