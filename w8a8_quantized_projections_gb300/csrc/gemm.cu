@@ -56,7 +56,6 @@ template <int OP, int EPI, int BN_, bool PAIR>
 struct Cfg {
     static constexpr int BM = 128;                         // A rows per CTA
     static constexpr int BN = BN_;                         // accumulator columns
-    static constexpr bool kPair = PAIR;
     static constexpr int kTileRows = PAIR ? 2 * BM : BM;   // output rows per tile
     static constexpr bool kI8 = (OP == kOpI8);
     // Every MMA operand k-block is 128 bytes of K: 64 fp16/bf16 or 128 e4m3.
@@ -80,18 +79,26 @@ struct Cfg {
     static constexpr int kChunkKBlocks = kI8 ? 16 : (1 << 30);  // 1024 K per exact chunk
     static constexpr int kConvWarps = kI8 ? 6 : 0;
     static constexpr int kEpiWarp0 = kI8 ? 8 : 4;
-    static constexpr int kNumWarps = kEpiWarp0 + 8;
+    // Epilogue warps: 16 for the FP8 SwiGLU epilogue (exp and an IEEE
+    // division per output must keep pace with a k-loop less than half as long
+    // as INT8's: 120 -> 102 us on 1502 x 24576 x 4096), 8 otherwise (the
+    // INT8 int32 totals take most registers; the scale/bias epilogue is light
+    // and more warps only crowd the producer and MMA warps' schedulers).
+    // kParts warps share each TMEM lane quadrant, splitting the tile's columns.
+    static constexpr int kEpiWarps = (!kI8 && BN_ == 256 && EPI == kEpiSwiGLU) ? 16 : 8;
+    static constexpr int kParts = kEpiWarps / 4;
+    static constexpr int kNumWarps = kEpiWarp0 + kEpiWarps;
     static constexpr int kThreads = kNumWarps * 32;
     static constexpr int kAccBufs = 2;                     // double-buffered accumulator
     static constexpr int kTmemCols = kAccBufs * BN;
-    static constexpr int kColsPerThread = BN / 2;          // columns one epilogue thread owns
+    static constexpr int kColsPerThread = BN / kParts;     // columns one epilogue thread owns
     static constexpr int kChunks32 = kColsPerThread / 32;
     static constexpr bool kSwiGLU = (EPI == kEpiSwiGLU);
     static constexpr int kOutColsPerTile = kSwiGLU ? BN / 2 : BN;
     // full[s]: TMA (native) or the local converter warps (INT8); in pair mode
     // the leader's barrier also counts the peer's forwarded readiness.
     static constexpr int kFullArrivals = kI8 ? kConvWarps : 1;
-    static constexpr int kAccEmptyArrivals = 8 * (PAIR ? 2 : 1);
+    static constexpr int kAccEmptyArrivals = kEpiWarps * (PAIR ? 2 : 1);
     static constexpr int kSmemBytes = NSTAGE * kStage + NRAW * kRawStage + 1024 + 512;
     static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
     static_assert(!PAIR || BN == 256, "pair mode uses 256-wide tiles");
@@ -518,10 +525,10 @@ struct Gemm {
     static __device__ __forceinline__ int chunk_col(int j, int half) {
         if (C::kSwiGLU) {
             constexpr int kHalfChunks = C::kChunks32 / 2;
-            return j < kHalfChunks ? half * (BN / 4) + 32 * j
-                                   : BN / 2 + half * (BN / 4) + 32 * (j - kHalfChunks);
+            return j < kHalfChunks ? half * (BN / 2 / C::kParts) + 32 * j
+                                   : BN / 2 + half * (BN / 2 / C::kParts) + 32 * (j - kHalfChunks);
         }
-        return half * (BN / 2) + 32 * j;
+        return half * (BN / C::kParts) + 32 * j;
     }
 
     // Finish 32 consecutive output columns n0.. of one row from 32 fp32
