@@ -76,19 +76,22 @@ struct Cfg {
     // latency (measured against 3 + 8 and 5 + 4: 1502 x 34816 x 5120 in 414
     // against 432 and 426 us).
     static constexpr int NRAW = kI8 ? (PAIR ? 6 : 5) : 0;
-    static constexpr int NSTAGE_RAWFREE = (kSmemBudget - NRAW * kRawStage) / kStage;
-    static constexpr int NSTAGE = kI8 ? (PAIR ? 4 : 2) : (NSTAGE_RAWFREE > 8 ? 8 : NSTAGE_RAWFREE);
-    static constexpr int kChunkKBlocks = kI8 ? 16 : (1 << 30);  // 1024 K per exact chunk
-    static constexpr int kConvWarps = kI8 ? 6 : 0;
-    static constexpr int kEpiWarp0 = kI8 ? 8 : 4;
     // Epilogue warps: 16 for the FP8 SwiGLU epilogue (exp and an IEEE
     // division per output must keep pace with a k-loop less than half as long
     // as INT8's: 120 -> 102 us on 1502 x 24576 x 4096), 8 otherwise (the
     // INT8 int32 totals take most registers; the scale/bias epilogue is light
     // and more warps only crowd the producer and MMA warps' schedulers).
     // kParts warps share each TMEM lane quadrant, splitting the tile's columns.
-    static constexpr int kEpiWarps = (!kI8 && BN_ == 256 && EPI == kEpiSwiGLU) ? 16 : 8;
+    static constexpr int kEpiWarps = (!kI8 && BN_ == 256 && (EPI == kEpiSwiGLU)) ? 16 : 8;
     static constexpr int kParts = kEpiWarps / 4;
+    // Read-modify-write epilogue (y += acc): a 32 x 32 fp32 transpose buffer
+    // per epilogue warp, so that y is read and written in row segments.
+    static constexpr int kEpiStage = (EPI == kEpiAddBF16) ? kEpiWarps * 4096 : 0;
+    static constexpr int NSTAGE_RAWFREE = (kSmemBudget - NRAW * kRawStage - kEpiStage) / kStage;
+    static constexpr int NSTAGE = kI8 ? (PAIR ? 4 : 2) : (NSTAGE_RAWFREE > 8 ? 8 : NSTAGE_RAWFREE);
+    static constexpr int kChunkKBlocks = kI8 ? 16 : (1 << 30);  // 1024 K per exact chunk
+    static constexpr int kConvWarps = kI8 ? 6 : 0;
+    static constexpr int kEpiWarp0 = kI8 ? 8 : 4;
     static constexpr int kNumWarps = kEpiWarp0 + kEpiWarps;
     static constexpr int kThreads = kNumWarps * 32;
     static constexpr int kAccBufs = 2;                     // double-buffered accumulator
@@ -101,7 +104,7 @@ struct Cfg {
     // the leader's barrier also counts the peer's forwarded readiness.
     static constexpr int kFullArrivals = kI8 ? kConvWarps : 1;
     static constexpr int kAccEmptyArrivals = kEpiWarps * (PAIR ? 2 : 1);
-    static constexpr int kSmemBytes = NSTAGE * kStage + NRAW * kRawStage + 1024 + 512;
+    static constexpr int kSmemBytes = NSTAGE * kStage + NRAW * kRawStage + kEpiStage + 1024 + 512;
     static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
     static_assert(!PAIR || BN == 256, "pair mode uses 256-wide tiles");
     static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
@@ -308,6 +311,7 @@ struct Gemm {
     struct Ctx {
         uint8_t *stage;      // NSTAGE x (A tile, B tile), 1024-aligned
         uint8_t *raw;        // NRAW x (raw A, raw B) for INT8
+        uint8_t *epi;        // kEpiStage bytes of epilogue transpose buffers
         Barriers *bar;
         uint32_t tmem;       // accumulator base (the leader's allocation in pair mode)
         uint32_t rank;       // rank in the CTA pair (0 in single mode)
@@ -630,6 +634,63 @@ struct Gemm {
         }
     }
 
+    // y = bf16(float(y) + acc) for the warp's 32 rows (row0 .. row0 + 31, one
+    // per lane in the accumulator): each 32-column chunk goes through the
+    // warp's transpose buffer (row-major, 16-byte unit u of row r at
+    // u ^ (r & 7): conflict-free both ways), after which lane l handles columns
+    // 8 (l & 3) .. + 7 of rows (l >> 2) + 8 i, so every warp access to y covers
+    // 64 contiguous bytes of eight rows instead of 16 bytes of 32 rows.
+    static __device__ __forceinline__ void load_y_chunk(const GemmArgs &a, int row0, int nb, int half,
+                                                        int j, uint4 (&yin)[4]) {
+        const int lane = threadIdx.x & 31;
+        const uint16_t *out = static_cast<const uint16_t *>(a.out);
+        const int n = nb * BN + chunk_col(j, half) + 8 * (lane & 3);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = row0 + (lane >> 2) + 8 * i;
+            yin[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < a.M && n < a.N) yin[i] = *reinterpret_cast<const uint4 *>(out + (int64_t)r * a.ldo + n);
+        }
+    }
+
+    static __device__ __forceinline__ void finish_add_chunk(const Ctx &c, const GemmArgs &a, int row0,
+                                                            int nb, int half, int j,
+                                                            const uint32_t (&v)[32],
+                                                            const uint4 (&yin)[4]) {
+        const int lane = threadIdx.x & 31, e = (int)(threadIdx.x >> 5) - C::kEpiWarp0;
+        const uint32_t buf = smem_u32(c.epi) + (uint32_t)e * 4096u;
+        const int cg = lane & 3;
+        uint16_t *out = static_cast<uint16_t *>(a.out);
+        const int n = nb * BN + chunk_col(j, half) + 8 * cg;
+        const uint32_t rowbuf = buf + (uint32_t)lane * 128u;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            sts128(rowbuf + (((uint32_t)u ^ (uint32_t)(lane & 7)) << 4), v[4 * u], v[4 * u + 1],
+                   v[4 * u + 2], v[4 * u + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int rr = (lane >> 2) + 8 * i;
+            const uint32_t rb = buf + (uint32_t)rr * 128u;
+            const uint4 p0 = lds128(rb + (((uint32_t)(2 * cg) ^ (uint32_t)(rr & 7)) << 4));
+            const uint4 p1 = lds128(rb + (((uint32_t)(2 * cg + 1) ^ (uint32_t)(rr & 7)) << 4));
+            const uint32_t acc8[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            const uint32_t ow[4] = {yin[i].x, yin[i].y, yin[i].z, yin[i].w};
+            float y[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                y[2 * k] = __fadd_rn(bf16_lo(ow[k]), __uint_as_float(acc8[2 * k]));
+                y[2 * k + 1] = __fadd_rn(bf16_hi(ow[k]), __uint_as_float(acc8[2 * k + 1]));
+            }
+            const int r = row0 + rr;
+            if (r < a.M && n < a.N)
+                *reinterpret_cast<uint4 *>(out + (int64_t)r * a.ldo + n) =
+                    make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                               pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+        }
+        __syncwarp();   // the buffer is rewritten by the next chunk
+    }
+
     static __device__ __forceinline__ void release_acc(const Ctx &c, uint32_t acc, int lane) {
         tc_fence_before();
         __syncwarp();
@@ -644,6 +705,8 @@ struct Gemm {
         const int e = warp - C::kEpiWarp0, quad = warp & 3, half = e >> 2;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         uint32_t acc = 0, aph = 0;
+        uint4 yin[(EPI == kEpiAddBF16) ? C::kChunks32 : 1][4];   // y += acc: y pieces in flight
+        (void)yin;
         for (int t = c.slot; t < c.num_tiles; t += c.nslots) {
             int mb, nb;
             tile_coords(c, t, mb, nb);
@@ -670,6 +733,27 @@ struct Gemm {
                 }
                 // the tile's exact int32 accumulators are complete
                 finish_row(a, row, row_ok, nb, half, tot);
+            } else if constexpr (EPI == kEpiAddBF16) {
+                // y += acc: this lane's y pieces of the whole tile are requested
+                // before the accumulator is awaited (requesting the next tile's
+                // pieces during this one measured slower), then each 32-column
+                // chunk is read from TMEM and finished through the transpose buffer
+#pragma unroll
+                for (int j = 0; j < C::kChunks32; ++j) load_y_chunk(a, row - lane, nb, half, j, yin[j]);
+                if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
+                tc_fence_after();
+                const uint32_t tbase = c.tmem + acc * BN + lane_off;
+#pragma unroll
+                for (int j = 0; j < C::kChunks32; ++j) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + chunk_col(j, half), v);
+                    tmem_ld_wait();
+                    if (j == C::kChunks32 - 1) {
+                        release_acc(c, acc, lane);
+                        if (++acc == (uint32_t)C::kAccBufs) { acc = 0; aph ^= 1u; }
+                    }
+                    finish_add_chunk(c, a, row - lane, nb, half, j, v, yin[j]);
+                }
             } else {
                 if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
                 tc_fence_after();
@@ -743,6 +827,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     typename G::Ctx c;
     c.stage = smem;
     c.raw = smem + C::NSTAGE * C::kStage;
+    c.epi = reinterpret_cast<uint8_t *>(bar) + 512;
     c.bar = bar;
     const uint32_t own_tmem = bar->tmem_slot;
     if (PAIR) {
