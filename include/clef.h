@@ -155,6 +155,29 @@ int clef_lora_add(const void *x, int64_t ldx, const void *A, const void *B,
                   void *t_scratch, void *y, int64_t ldy, void *stream);
 
 /*
+ * clef_lora_gateup_swiglu -- runtime LoRA on the gate and up projections
+ * [LORA], followed by the MLP product [USAGE], in one pass over the base
+ * gate/up values: with t_g = bf16(x A_gate^T) and t_u = bf16(x A_up^T) as in
+ * clef_lora_add,
+ *   g[m][n] = bf16((float)y_gu[m][n]     + sum_j t_g[m][j] * B_gate[n][j])
+ *   u[m][n] = bf16((float)y_gu[m][N + n] + sum_j t_u[m][j] * B_up[n][j])
+ *   h[m][n] = bf16(silu(g) * u)   (fp32, silu(g) = g / (1 + exp(-g)))
+ * -- the same rounded operations as two clef_lora_add calls on the halves of
+ * y_gu followed by clef_swiglu_bf16, without writing g and u back.
+ * x: bf16 [M][K], row pitch ldx; A_gate, A_up: bf16 [r][K] dense; B_gate,
+ * B_up: bf16 [N][r] dense; t_scratch: bf16 [M][2 r_pad] dense scratch
+ * (r_pad = r rounded up to 64; receives t_g then t_u); y_gu: bf16 [M][2N]
+ * base gate values then up values (the output of clef_w8a8_linear on the
+ * packed weight), row pitch ld_gu, read only; h: bf16 [M][N], row pitch ldh.
+ * Requirements: K % 8 == 0, r % 8 == 0, 0 < r <= 1024, N % 8 == 0,
+ *   ldx >= K, ld_gu >= 2N, ldh >= N, all pitches multiples of 8.
+ */
+int clef_lora_gateup_swiglu(const void *x, int64_t ldx, const void *A_gate, const void *B_gate,
+                            const void *A_up, const void *B_up, int64_t M, int64_t K, int64_t N,
+                            int64_t r, void *t_scratch, const void *y_gu, int64_t ld_gu,
+                            void *h, int64_t ldh, void *stream);
+
+/*
  * clef_swiglu_bf16 -- the unfused MLP reading (fuse_mlp off in [USAGE]):
  * y_gu holds bf16 gate values in columns 0..N-1 and up values in N..2N-1
  * (row pitch ldg); h[m][n] = bf16(silu(float(g)) * float(u)).

@@ -95,18 +95,27 @@ def test_workload_full_size(orc, index, pack):
             rq = host(gq)[rows]
             rs = host(gs)[rows]
         if p.kind == "gateup" and lora:
+            # the packed base gate|up values (bit-exact INT8 linear)
             packed = bf16_host(out[p.name + "/packed"])[rows]
             base = (orc.fp8_linear if fp8 else orc.int8_linear)(rq, rs, wq, ws, bias)
+            assert np.array_equal(packed, base), "packed gate/up base"
+            # the adapters' adds, through lora_add on the sampled rows (row-invariant
+            # kernels), against the oracle; then the unfused SwiGLU against the oracle
             x = acts_np[p.act][rows]
+            upd = bf16_dev(packed)
             for half, sl in (("gate", slice(0, p.N)), ("up", slice(p.N, 2 * p.N))):
                 A, B = lora_np[p.name + "/" + half]
+                clef.lora_add(bf16_dev(x), bf16_dev(A), bf16_dev(B), upd[:, sl])
                 t_ref = orc.lora_t(x, A)
                 y_ref = orc.lora_y(t_ref, B, np.ascontiguousarray(base[:, sl]))
                 tol = lora_y_bound(t_ref, B, y_ref, p.K, clef.lora_pad(A.shape[0]), x, A)
-                d = np.abs(S.bf16_bits_to_f64(packed[:, sl]) - S.bf16_bits_to_f64(y_ref))
+                d = np.abs(S.bf16_bits_to_f64(bf16_host(upd)[:, sl]) - S.bf16_bits_to_f64(y_ref))
                 assert np.all(d <= tol), f"{p.name}/{half} lora: excess {(d - tol).max():.3g}"
+            h_unfused = bf16_host(clef.swiglu_bf16(upd))
+            assert_bf16_within(h_unfused, orc.swiglu_bf16(bf16_host(upd)), 1.0, "unfused swiglu")
+            # the fused LoRA gate/up + SwiGLU of the step gives the same values
             h = bf16_host(out[p.name])[rows]
-            assert_bf16_within(h, orc.swiglu_bf16(packed), 1.0, "unfused swiglu")
+            assert np.array_equal(S.bf16_bits_to_f64(h), S.bf16_bits_to_f64(h_unfused)), "fused lora swiglu"
             h_gpu = out[p.name]
         elif p.kind == "gateup":
             h = bf16_host(out[p.name])[rows]

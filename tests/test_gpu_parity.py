@@ -186,6 +186,25 @@ def test_w8a8_gateup_swiglu_wide_gate_range(orc):
     assert_bf16_within(h, ref, 1.0, "swiglu wide gate")
 
 
+@pytest.mark.parametrize("M,K,N,r", [(300, 1024, 512, 256), (130, 512, 264, 48), (1, 128, 8, 8),
+                                     (600, 2048, 1024, 128)])
+def test_lora_gateup_swiglu_equals_unfused(M, K, N, r):
+    """The fused gate/up LoRA + SwiGLU call gives the values of two lora_add
+    calls on the halves followed by swiglu_bf16 (the same rounded operations;
+    the other adapter's columns meet zeros, which add nothing)."""
+    x = bf16_dev(S.activation(0, f"t/lgu/{M}/x", M, K))
+    Ag, Bg = (bf16_dev(a) for a in S.lora_pair(0, f"t/lgu/{M}/g", r, K, N))
+    Au, Bu = (bf16_dev(a) for a in S.lora_pair(0, f"t/lgu/{M}/u", r, K, N))
+    y = bf16_dev(S.normal_bf16(0, f"t/lgu/{M}/y", (M, 2 * N), 2.0))
+    h = bf16_host(clef.lora_gateup_swiglu(x, Ag, Bg, Au, Bu, y))
+    upd = y.clone()
+    clef.lora_add(x, Ag, Bg, upd[:, :N])
+    clef.lora_add(x, Au, Bu, upd[:, N:])
+    ref = bf16_host(clef.swiglu_bf16(upd))
+    assert np.array_equal(S.bf16_bits_to_f64(h), S.bf16_bits_to_f64(ref))
+    assert np.array_equal(bf16_host(y), S.normal_bf16(0, f"t/lgu/{M}/y", (M, 2 * N), 2.0)), "y_gu read only"
+
+
 def test_swiglu_bf16(orc):
     M, N = 300, 1024
     y = S.normal_bf16(0, "t/sw/y", (M, 2 * N), 3.0)
@@ -229,6 +248,28 @@ def test_fp8_linear(orc, M, N, K):
     y = bf16_host(clef.fp8_linear(gqx, gsx, gqw, gsw, bf16_dev(b)))
     ref = par_rows(lambda a, c: orc.fp8_linear(qx[a:c], sx[a:c], qw, sw, b), M)
     assert_rms_close(y, ref, 1e-2, "fp8_linear")
+
+
+@pytest.mark.parametrize("mode", ["int8_h128", "fp8"])
+def test_packed_projections_equal_separate_calls(mode):
+    """q|k|v packed into one GEMM (weight rows, scales and biases stacked) give
+    each projection's outputs bit for bit as separate calls do."""
+    M, K = 300, 1024
+    widths = [768, 256, 256]
+    x = S.activation(0, "t/pack/x", M, K)
+    ws = [S.weight(0, f"t/pack/w{i}", n, K) for i, n in enumerate(widths)]
+    bs = [S.bias(0, f"t/pack/b{i}", n) for i, n in enumerate(widths)]
+    lin = clef.w8a8_linear if mode == "int8_h128" else clef.fp8_linear
+    qx, sx = clef.quant_act(bf16_dev(x), mode)
+    packed_w = bf16_dev(np.concatenate(ws, axis=0))
+    qw, sw = clef.quant_act(packed_w, mode)
+    y_packed = host(lin(qx, sx, qw, sw, bf16_dev(np.concatenate(bs))).view(torch.int16))
+    c0 = 0
+    for w, b, n in zip(ws, bs, widths):
+        qwi, swi = clef.quant_act(bf16_dev(w), mode)
+        yi = host(lin(qx, sx, qwi, swi, bf16_dev(b)).view(torch.int16))
+        assert np.array_equal(yi, y_packed[:, c0:c0 + n])
+        c0 += n
 
 
 def test_fp8_gateup_swiglu(orc):

@@ -21,7 +21,8 @@ from . import build as _build
 
 __all__ = [
     "ClefError", "library", "library_path", "quant_act", "w8a8_linear", "w8a8_gateup_swiglu",
-    "fp8_linear", "fp8_gateup_swiglu", "lora_add", "lora_add_noalloc", "swiglu_bf16", "w8a8_gemm_s32",
+    "fp8_linear", "fp8_gateup_swiglu", "lora_add", "lora_add_noalloc", "lora_gateup_swiglu", "swiglu_bf16",
+    "w8a8_gemm_s32",
     "poll_status", "set_wait_limit_ns", "set_quant_staging", "ACT_MODES",
 ]
 
@@ -62,6 +63,8 @@ def library():
                 "clef_lora_add": [vp, i64, vp, vp, i64, i64, i64, i64, vp, vp, i64, vp],
                 "clef_lora_add_noalloc": [vp, i64, vp, vp, i64, i64, i64, i64, vp, i64, vp],
                 "clef_swiglu_bf16": [vp, i64, i64, i64, vp, i64, vp],
+                "clef_lora_gateup_swiglu": [vp, i64, vp, vp, vp, vp, i64, i64, i64, i64, vp, vp, i64,
+                                            vp, i64, vp],
                 "clef_w8a8_gemm_s32": [vp, vp, i64, i64, i64, vp, i64, vp],
                 "clef_poll_status": [],
                 "clef_abi_version": [],
@@ -224,6 +227,32 @@ def lora_add_noalloc(x, A, B, y, stream=None):
     _call("clef_lora_add_noalloc", _ptr(x), _rows(x, "x"), _ptr(A), _ptr(B), M, K, N, r,
           _ptr(y), _rows(y, "y"), _stream(x, stream))
     return y
+
+
+def lora_gateup_swiglu(x, A_gate, B_gate, A_up, B_up, y_gu, h=None, t_scratch=None, stream=None):
+    """h = bf16(silu(g) * u) with g, u the gate and up halves of y_gu after
+    their LoRA adds (each as lora_add computes it).  y_gu is read only."""
+    for t, n in ((x, "x"), (A_gate, "A_gate"), (B_gate, "B_gate"), (A_up, "A_up"), (B_up, "B_up"),
+                 (y_gu, "y_gu")):
+        _cuda(t, n, (torch.bfloat16,))
+    for t, n in ((A_gate, "A_gate"), (B_gate, "B_gate"), (A_up, "A_up"), (B_up, "B_up")):
+        _dense(t, n)
+    M, K = x.shape
+    r = A_gate.shape[0]
+    N = B_gate.shape[0]
+    if (A_gate.shape != (r, K) or A_up.shape != (r, K) or B_gate.shape != (N, r) or B_up.shape != (N, r)
+            or y_gu.shape != (M, 2 * N)):
+        raise ValueError("LoRA gate/up shapes disagree")
+    if t_scratch is None:
+        t_scratch = torch.empty((M, 2 * lora_pad(r)), dtype=torch.bfloat16, device=x.device)
+    _dense(t_scratch, "t_scratch")
+    if h is None:
+        h = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _cuda(h, "h", (torch.bfloat16,))
+    _call("clef_lora_gateup_swiglu", _ptr(x), _rows(x, "x"), _ptr(A_gate), _ptr(B_gate), _ptr(A_up),
+          _ptr(B_up), M, K, N, r, _ptr(t_scratch), _ptr(y_gu), _rows(y_gu, "y_gu"), _ptr(h), _rows(h, "h"),
+          _stream(x, stream))
+    return h
 
 
 def swiglu_bf16(y_gu, h=None, stream=None):

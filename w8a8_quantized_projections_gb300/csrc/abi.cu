@@ -322,6 +322,57 @@ int clef_lora_add(const void *x, int64_t ldx, const void *A, const void *B, int6
                        Operand{B, (uint64_t)r, (uint64_t)N, (uint64_t)r * 2}, a2, d->num_sms, st);
 }
 
+int clef_lora_gateup_swiglu(const void *x, int64_t ldx, const void *A_gate, const void *B_gate,
+                            const void *A_up, const void *B_up, int64_t M, int64_t K, int64_t N,
+                            int64_t r, void *t_scratch, const void *y_gu, int64_t ld_gu, void *h,
+                            int64_t ldh, void *stream) {
+    if (M < 0 || M > kMaxDim) return arg_fail("M out of range");
+    if (K <= 0 || K > kMaxDim || K % 8 != 0) return arg_fail("K must be positive and a multiple of 8");
+    if (N <= 0 || 2 * N > kMaxDim || N % 8 != 0) return arg_fail("N must be positive and a multiple of 8");
+    if (r <= 0 || r > 1024 || r % 8 != 0) return arg_fail("rank must be in (0, 1024] and a multiple of 8");
+    if (ldx < K || ldx % 8 != 0) return arg_fail("ldx must be >= K and a multiple of 8");
+    if (ld_gu < 2 * N || ld_gu % 8 != 0) return arg_fail("ld_gu must be >= 2N and a multiple of 8");
+    if (ldh < N || ldh % 8 != 0) return arg_fail("ldh must be >= N and a multiple of 8");
+    if (M == 0) return CLEF_OK;
+    if (!x || !A_gate || !B_gate || !A_up || !B_up || !t_scratch || !y_gu || !h)
+        return arg_fail("null pointer");
+    if (!aligned16(x) || !aligned16(A_gate) || !aligned16(B_gate) || !aligned16(A_up) ||
+        !aligned16(B_up) || !aligned16(t_scratch) || !aligned16(y_gu) || !aligned16(h))
+        return arg_fail("pointers must be 16-byte aligned");
+    DeviceState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc) return rc;
+    const int64_t r_pad = (r + 63) / 64 * 64;
+    const int bn = r_pad == 64 ? 64 : (r_pad == 128 ? 128 : 256);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // stage 1: t = [bf16(x A_gate^T) | bf16(x A_up^T)], [M][2 r_pad]
+    for (int half = 0; half < 2; ++half) {
+        GemmArgs a1 = base_args(d, M, r_pad, K);
+        a1.out = static_cast<uint16_t *>(t_scratch) + half * r_pad;
+        a1.ldo = 2 * r_pad;
+        rc = launch_gemm(kOpBF16, kEpiStoreBF16, bn, Operand{x, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2},
+                         Operand{half ? A_up : A_gate, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2}, a1,
+                         d->num_sms, st);
+        if (rc) return rc;
+    }
+    // stage 2: one GEMM over K = 2 r_pad; gate rows see B_gate in the first
+    // r_pad columns and zeros after (past the end of B_gate), up rows zeros
+    // first (before the start of B_up) and B_up after, so each half sums only
+    // its own adapter's products; the epilogue adds them to the base gate and
+    // up values and forms h
+    GemmArgs a2 = base_args(d, M, N, 2 * r_pad);
+    a2.n_half = (int)N;
+    a2.aux = y_gu;
+    a2.ld_aux = ld_gu;
+    a2.k_shift = (int)r_pad;
+    a2.out = h;
+    a2.ldo = ldh;
+    const Operand Bu{B_up, (uint64_t)r, (uint64_t)N, (uint64_t)r * 2};
+    return launch_gemm(kOpBF16, kEpiLoraSwiGLU, 256,
+                       Operand{t_scratch, (uint64_t)(2 * r_pad), (uint64_t)M, (uint64_t)(2 * r_pad) * 2},
+                       Operand{B_gate, (uint64_t)r, (uint64_t)N, (uint64_t)r * 2}, a2, d->num_sms, st, &Bu);
+}
+
 int clef_swiglu_bf16(const void *y_gu, int64_t M, int64_t N, int64_t ldg, void *h, int64_t ldh,
                      void *stream) {
     if (M < 0 || M > kMaxDim) return arg_fail("M out of range");

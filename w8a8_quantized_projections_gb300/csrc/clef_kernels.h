@@ -38,6 +38,9 @@ enum GemmEpi : int {
     kEpiStoreBF16 = 2,  // t = bf16(acc)
     kEpiAddBF16 = 3,    // y = bf16(float(y) + acc), y read and written
     kEpiStoreS32 = 4,   // acc as int32 (INT8 operands only)
+    kEpiLoraSwiGLU = 5, // gate/up LoRA adds then SwiGLU: g = bf16(yg + acc_g),
+                        // u = bf16(yu + acc_u), h = bf16(silu(g) * u); yg|yu read
+                        // from aux, h written to out (bf16 operands only)
 };
 
 struct GemmArgs {
@@ -52,6 +55,12 @@ struct GemmArgs {
     uint64_t wait_limit_ns;
     int *dbg;                // optional: per CTA, its own TMEM base and the one it uses
     int force_timeout;       // test knob: make the MMA issuer's wait run out
+    // kEpiLoraSwiGLU: the base gate|up values (bf16 [M][2 * n_half], pitch
+    // ld_aux elements), and the K offset of the up half's factor: up rows of
+    // the B operand come from the second tensor map at K coordinate k - k_shift
+    const void *aux;
+    int64_t ld_aux;
+    int k_shift;
 };
 
 // A row-major 2-D operand: rows of `inner` elements, `pitch` bytes apart.
@@ -64,7 +73,7 @@ struct Operand {
 // the chosen tile mode and launches on st.  bn selects the tile width (256 for
 // the W8A8 GEMMs; 64/128/256 for the LoRA rank).  Returns a clef_status code.
 int launch_gemm(int op, int epi, int bn, const Operand &A, const Operand &B, const GemmArgs &args,
-                int num_sms, cudaStream_t st);
+                int num_sms, cudaStream_t st, const Operand *B2 = nullptr);
 
 // Whether a launch with this width and row count uses CTA pairs.
 bool gemm_uses_pair(int bn, int M, int num_sms);

@@ -86,7 +86,8 @@ struct Cfg {
     static constexpr int kParts = kEpiWarps / 4;
     // Read-modify-write epilogue (y += acc): a 32 x 32 fp32 transpose buffer
     // per epilogue warp, so that y is read and written in row segments.
-    static constexpr int kEpiStage = (EPI == kEpiAddBF16) ? kEpiWarps * 4096 : 0;
+    static constexpr bool kLoraSwi = (EPI == kEpiLoraSwiGLU);
+    static constexpr int kEpiStage = (EPI == kEpiAddBF16) ? kEpiWarps * 4096 : (kLoraSwi ? kEpiWarps * 8192 : 0);
     static constexpr int NSTAGE_RAWFREE = (kSmemBudget - NRAW * kRawStage - kEpiStage) / kStage;
     static constexpr int NSTAGE = kI8 ? (PAIR ? 4 : 2) : (NSTAGE_RAWFREE > 8 ? 8 : NSTAGE_RAWFREE);
     static constexpr int kChunkKBlocks = kI8 ? 16 : (1 << 30);  // 1024 K per exact chunk
@@ -98,7 +99,7 @@ struct Cfg {
     static constexpr int kTmemCols = kAccBufs * BN;
     static constexpr int kColsPerThread = BN / kParts;     // columns one epilogue thread owns
     static constexpr int kChunks32 = kColsPerThread / 32;
-    static constexpr bool kSwiGLU = (EPI == kEpiSwiGLU);
+    static constexpr bool kSwiGLU = (EPI == kEpiSwiGLU || EPI == kEpiLoraSwiGLU);  // gate|up tile
     static constexpr int kOutColsPerTile = kSwiGLU ? BN / 2 : BN;
     // full[s]: TMA (native) or the local converter warps (INT8); in pair mode
     // the leader's barrier also counts the peer's forwarded readiness.
@@ -175,6 +176,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&p);
 }
+
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -335,13 +338,19 @@ struct Gemm {
 
     // Row of the weight operand that this CTA's B stage starts with.
     static __device__ __forceinline__ int b_row(const Ctx &c, const GemmArgs &a, int nb, int half) {
+        if (C::kLoraSwi) return nb * (BN / 2);   // each half from its own tensor map
         if (C::kSwiGLU) return (half ? a.n_half : 0) + nb * (BN / 2);
         return nb * BN + (int)c.rank * C::kBRows;
     }
 
     // ---------------------------------------------------------------- producer
-    static __device__ void producer(const Ctx &c, const CUtensorMap *tmA, const CUtensorMap *tmB,
-                                    const GemmArgs &a, uint32_t (&fills)[8]) {
+    static __device__ void producer(const Ctx &c, const CUtensorMap *tmA, const CUtensorMap *tmB0,
+                                    const CUtensorMap *tmB2, const GemmArgs &a, uint32_t (&fills)[8]) {
+        // B operand of the gate (half 0) and up (half 1) rows: LoRA gate/up
+        // reads the up factor from its own map, shifted along K
+        auto bmap = [&](int h) { return (C::kLoraSwi && h) ? tmB2 : tmB0; };
+        auto bk = [&](int h, int k0) { return (C::kLoraSwi && h) ? k0 - a.k_shift : k0; };
+        const CUtensorMap *tmB = tmB0;
         static_assert(C::NRAW <= 8 && C::NSTAGE <= 8, "fill bookkeeping");
         uint32_t s = 0, ph = 0;
         const int nstage = C::kI8 ? C::NRAW : C::NSTAGE;
@@ -374,14 +383,15 @@ struct Gemm {
                         const uint32_t lfull = leader_addr(&c.bar->full[s]);
                         if (c.rank == 0) mbar_arrive_expect_tx(&c.bar->full[s], 2 * C::kStage);
                         tma_load_2d_pair(sa, tmA, k0, row_a, lfull);
-                        tma_load_2d_pair(sb, tmB, k0, b_row(c, a, nb, (int)c.rank), lfull);
+                        tma_load_2d_pair(sb, bmap((int)c.rank), bk((int)c.rank, k0), b_row(c, a, nb, (int)c.rank),
+                                         lfull);
                     } else {
                         uint64_t *full = &c.bar->full[s];
                         mbar_arrive_expect_tx(full, C::kStage);
                         tma_load_2d(sa, tmA, k0, row_a, full);
                         if (C::kSwiGLU) {
-                            tma_load_2d(sb, tmB, k0, b_row(c, a, nb, 0), full);
-                            tma_load_2d(sb + (BN / 2) * 128, tmB, k0, b_row(c, a, nb, 1), full);
+                            tma_load_2d(sb, bmap(0), bk(0, k0), b_row(c, a, nb, 0), full);
+                            tma_load_2d(sb + (BN / 2) * 128, bmap(1), bk(1, k0), b_row(c, a, nb, 1), full);
                         } else {
                             tma_load_2d(sb, tmB, k0, b_row(c, a, nb, 0), full);
                         }
@@ -691,6 +701,80 @@ struct Gemm {
         __syncwarp();   // the buffer is rewritten by the next chunk
     }
 
+    // LoRA gate/up + SwiGLU: base gate and up pieces of chunk pair p (gate
+    // chunk p and up chunk p + kChunks32 / 2 of the tile) for this lane's rows
+    // (l >> 2) + 8 i and columns 8 (l & 3) .. + 7, as finish_add_chunk lays them out.
+    static __device__ __forceinline__ void load_gu_chunk(const GemmArgs &a, int row0, int nb, int half,
+                                                         int p, uint4 (&yg)[4], uint4 (&yu)[4]) {
+        const int lane = threadIdx.x & 31;
+        const uint16_t *base = static_cast<const uint16_t *>(a.aux);
+        const int n = nb * (BN / 2) + chunk_col(p, half) + 8 * (lane & 3);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = row0 + (lane >> 2) + 8 * i;
+            yg[i] = make_uint4(0u, 0u, 0u, 0u);
+            yu[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < a.M && n < a.N) {
+                const uint16_t *src = base + (int64_t)r * a.ld_aux + n;
+                yg[i] = *reinterpret_cast<const uint4 *>(src);
+                yu[i] = *reinterpret_cast<const uint4 *>(src + a.n_half);
+            }
+        }
+    }
+
+    // g = bf16(yg + acc_g), u = bf16(yu + acc_u), h = bf16(silu(g) * u) for one
+    // chunk pair, both accumulator chunks transposed through the warp's two
+    // 32 x 32 buffers; the same rounded operations as the LoRA add followed by
+    // the unfused SwiGLU kernel.
+    static __device__ __forceinline__ void finish_lora_swiglu(const Ctx &c, const GemmArgs &a, int row0,
+                                                              int nb, int half, int p,
+                                                              const uint32_t (&vg)[32],
+                                                              const uint32_t (&vu)[32],
+                                                              const uint4 (&yg)[4], const uint4 (&yu)[4]) {
+        const int lane = threadIdx.x & 31, e = (int)(threadIdx.x >> 5) - C::kEpiWarp0;
+        const uint32_t buf = smem_u32(c.epi) + (uint32_t)e * 8192u;
+        const int cg = lane & 3;
+        uint16_t *out = static_cast<uint16_t *>(a.out);
+        const int n = nb * (BN / 2) + chunk_col(p, half) + 8 * cg;
+        const uint32_t rowbuf = buf + (uint32_t)lane * 128u;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const uint32_t off = ((uint32_t)u ^ (uint32_t)(lane & 7)) << 4;
+            sts128(rowbuf + off, vg[4 * u], vg[4 * u + 1], vg[4 * u + 2], vg[4 * u + 3]);
+            sts128(rowbuf + 4096u + off, vu[4 * u], vu[4 * u + 1], vu[4 * u + 2], vu[4 * u + 3]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int rr = (lane >> 2) + 8 * i;
+            const uint32_t rb = buf + (uint32_t)rr * 128u;
+            const uint32_t o0 = ((uint32_t)(2 * cg) ^ (uint32_t)(rr & 7)) << 4;
+            const uint32_t o1 = ((uint32_t)(2 * cg + 1) ^ (uint32_t)(rr & 7)) << 4;
+            const uint4 g0 = lds128(rb + o0), g1 = lds128(rb + o1);
+            const uint4 u0 = lds128(rb + 4096u + o0), u1 = lds128(rb + 4096u + o1);
+            const uint32_t ag[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            const uint32_t au[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            const uint32_t gw[4] = {yg[i].x, yg[i].y, yg[i].z, yg[i].w};
+            const uint32_t uw[4] = {yu[i].x, yu[i].y, yu[i].z, yu[i].w};
+            float h[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float g_lo = bf16_round(__fadd_rn(bf16_lo(gw[k]), __uint_as_float(ag[2 * k])));
+                const float g_hi = bf16_round(__fadd_rn(bf16_hi(gw[k]), __uint_as_float(ag[2 * k + 1])));
+                const float u_lo = bf16_round(__fadd_rn(bf16_lo(uw[k]), __uint_as_float(au[2 * k])));
+                const float u_hi = bf16_round(__fadd_rn(bf16_hi(uw[k]), __uint_as_float(au[2 * k + 1])));
+                h[2 * k] = silu_mul(g_lo, u_lo);
+                h[2 * k + 1] = silu_mul(g_hi, u_hi);
+            }
+            const int r = row0 + rr;
+            if (r < a.M && n < a.N)
+                *reinterpret_cast<uint4 *>(out + (int64_t)r * a.ldo + n) =
+                    make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]),
+                               pack_bf16x2(h[4], h[5]), pack_bf16x2(h[6], h[7]));
+        }
+        __syncwarp();   // the buffers are rewritten by the next chunk pair
+    }
+
     static __device__ __forceinline__ void release_acc(const Ctx &c, uint32_t acc, int lane) {
         tc_fence_before();
         __syncwarp();
@@ -733,6 +817,26 @@ struct Gemm {
                 }
                 // the tile's exact int32 accumulators are complete
                 finish_row(a, row, row_ok, nb, half, tot);
+            } else if constexpr (C::kLoraSwi) {
+                constexpr int kPairs = C::kChunks32 / 2;
+                uint4 yg[kPairs][4], yu[kPairs][4];
+#pragma unroll
+                for (int p = 0; p < kPairs; ++p) load_gu_chunk(a, row - lane, nb, half, p, yg[p], yu[p]);
+                if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
+                tc_fence_after();
+                const uint32_t tbase = c.tmem + acc * BN + lane_off;
+#pragma unroll
+                for (int p = 0; p < kPairs; ++p) {
+                    uint32_t vg[32], vu[32];
+                    tmem_ld32(tbase + chunk_col(p, half), vg);
+                    tmem_ld32(tbase + chunk_col(p + kPairs, half), vu);
+                    tmem_ld_wait();
+                    if (p == kPairs - 1) {
+                        release_acc(c, acc, lane);
+                        if (++acc == (uint32_t)C::kAccBufs) { acc = 0; aph ^= 1u; }
+                    }
+                    finish_lora_swiglu(c, a, row - lane, nb, half, p, vg, vu, yg[p], yu[p]);
+                }
             } else if constexpr (EPI == kEpiAddBF16) {
                 // y += acc: this lane's y pieces of the whole tile are requested
                 // before the accumulator is awaited (requesting the next tile's
@@ -774,6 +878,7 @@ struct Gemm {
 template <int OP, int EPI, int BN, bool PAIR>
 __global__ void __launch_bounds__(Cfg<OP, EPI, BN, PAIR>::kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+            const __grid_constant__ CUtensorMap tmB2,
             const GemmArgs args) {
     using C = Cfg<OP, EPI, BN, PAIR>;
     using G = Gemm<OP, EPI, BN, PAIR>;
@@ -806,6 +911,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (C::kLoraSwi) tma_prefetch_desc(&tmB2);
     }
     if (warp == 1) {
         if (PAIR) {
@@ -861,7 +967,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         if (C::kI8) asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
         if (warp == 0) {
             if (lane == 0) {
-                G::producer(c, &tmA, &tmB, args, fills);
+                G::producer(c, &tmA, &tmB, &tmB2, args, fills);
                 G::drain_copies(c, fills, args.status);
             }
         } else if (warp == 1) {
@@ -903,7 +1009,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 
 template <int OP, int EPI, int BN, bool PAIR>
 int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num_sms,
-               cudaStream_t st) {
+               cudaStream_t st, const Operand *B2 = nullptr) {
     using C = Cfg<OP, EPI, BN, PAIR>;
     const CUtensorMapDataType dt =
         (OP == kOpBF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -917,6 +1023,12 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
     rc = internal_make_tmap(&tb, dt, B.base, B.inner, B.rows, B.pitch, box_k,
                             C::kSwiGLU ? BN / 2 : C::kBRows, sw);
     if (rc) return rc;
+    CUtensorMap tb2 = tb;
+    if (C::kLoraSwi) {
+        if (!B2) return internal_cuda_error(cudaErrorInvalidValue, "LoRA gate/up needs the up factor");
+        rc = internal_make_tmap(&tb2, dt, B2->base, B2->inner, B2->rows, B2->pitch, box_k, BN / 2, sw);
+        if (rc) return rc;
+    }
     auto kern = gemm_kernel<OP, EPI, BN, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return internal_cuda_error(e, "gemm smem attribute");
@@ -945,10 +1057,10 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
         }
         const int pairs = tiles < max_pairs ? tiles : max_pairs;
         cfg.gridDim = dim3(2 * pairs, 1, 1);
-        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, args);
+        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, args);
     } else {
         const int grid = tiles < num_sms ? tiles : num_sms;
-        kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(ta, tb, args);
+        kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(ta, tb, tb2, args);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return internal_cuda_error(e, "gemm launch");
@@ -960,7 +1072,7 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
 bool gemm_uses_pair(int bn, int M, int num_sms) { return bn == 256 && M > 128 && num_sms >= 2; }
 
 int launch_gemm(int op, int epi, int bn, const Operand &A, const Operand &B, const GemmArgs &args,
-                int num_sms, cudaStream_t st) {
+                int num_sms, cudaStream_t st, const Operand *B2) {
     const bool pair = gemm_uses_pair(bn, args.M, num_sms);
 #define CLEF_GEMM(OPV, EPIV, BNV)                                                        \
     return pair ? launch_one<OPV, EPIV, BNV, true>(A, B, args, num_sms, st)              \
@@ -979,6 +1091,10 @@ int launch_gemm(int op, int epi, int bn, const Operand &A, const Operand &B, con
             if (bn == 256) CLEF_GEMM(kOpBF16, kEpiStoreBF16, 256);
         } else if (epi == kEpiAddBF16 && bn == 256) {
             CLEF_GEMM(kOpBF16, kEpiAddBF16, 256);
+        } else if (epi == kEpiLoraSwiGLU && bn == 256) {
+            const bool pr = gemm_uses_pair(bn, args.M, num_sms);
+            return pr ? launch_one<kOpBF16, kEpiLoraSwiGLU, 256, true>(A, B, args, num_sms, st, B2)
+                      : launch_one<kOpBF16, kEpiLoraSwiGLU, 256, false>(A, B, args, num_sms, st, B2);
         }
     }
 #undef CLEF_GEMM

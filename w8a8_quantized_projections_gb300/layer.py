@@ -20,9 +20,9 @@ small k and v projections the tile count of one wide GEMM.
 A step runs, per distinct activation tensor, one quantizer call, then per
 projection one GEMM call (gate/up with the fused SwiGLU epilogue).  With
 runtime LoRA pairs, every adapted projection adds ``bf16(x A^T) B^T`` after
-its GEMM; gate/up is then run as a packed linear (bf16 gate and up), the LoRA
-adds land on each half before the nonlinearity, and the unfused SwiGLU kernel
-forms h.
+its GEMM; gate/up is then run as a packed linear (bf16 gate and up), and one
+call adds the gate and up adapters to their halves and forms h (the same
+rounded operations as two LoRA adds followed by the unfused SwiGLU).
 """
 from __future__ import annotations
 
@@ -30,7 +30,7 @@ from typing import Dict, Optional, Tuple
 
 import torch
 
-from . import (fp8_gateup_swiglu, fp8_linear, lora_add, lora_pad, quant_act, swiglu_bf16,
+from . import (fp8_gateup_swiglu, fp8_linear, lora_add, lora_gateup_swiglu, lora_pad, quant_act,
                w8a8_gateup_swiglu, w8a8_linear)
 
 
@@ -98,12 +98,13 @@ class QuantizedLayer:
             if p.chained:
                 self.q[p.act] = (torch.empty((M, p.K), dtype=code, device=device),
                                  torch.empty((M,), dtype=torch.float32, device=device))
-        # one dense LoRA scratch [M][r_pad] per padded rank in use
+        # one dense LoRA scratch per width in use: [M][r_pad], and [M][2 r_pad]
+        # for the gate/up pair
         self.t = {}
-        for A, _ in self.lora.values():
-            r_pad = lora_pad(A.shape[0])
-            if r_pad not in self.t:
-                self.t[r_pad] = torch.empty((M, r_pad), dtype=torch.bfloat16, device=device)
+        for key, (A, _) in self.lora.items():
+            width = lora_pad(A.shape[0]) * (2 if key.endswith("/gate") or key.endswith("/up") else 1)
+            if width not in self.t:
+                self.t[width] = torch.empty((M, width), dtype=torch.bfloat16, device=device)
 
     def units(self):
         """The GEMM launches of a step: (event name, weight rows, K, 2*M*rows*K)."""
@@ -118,9 +119,7 @@ class QuantizedLayer:
         for p in self.cfg.projections:
             n += 1 if p.chained else 0
             if self.lora:
-                n += 4 if p.kind == "gateup" else 2   # each LoRA add is two GEMM launches
-                if p.kind == "gateup":
-                    n += 1                             # unfused SwiGLU
+                n += 3 if p.kind == "gateup" else 2   # gate/up: two x A^T, one fused add + SwiGLU
         return n
 
     def step(self, acts: Dict[str, torch.Tensor], events=None) -> Dict[str, torch.Tensor]:
@@ -163,14 +162,11 @@ class QuantizedLayer:
                     packed = self.out[p.name + "/packed"]
                     with ev("gemm", p.name):
                         lin(qx, sx, qw, sw, b, y=packed)
-                    x = acts[p.act]
+                    Ag, Bg = self.lora[p.name + "/gate"]
+                    Au, Bu = self.lora[p.name + "/up"]
                     with ev("lora", p.name):
-                        A, B = self.lora[p.name + "/gate"]
-                        lora_add(x, A, B, packed[:, :p.N], t_scratch=self._t(A))
-                        A, B = self.lora[p.name + "/up"]
-                        lora_add(x, A, B, packed[:, p.N:], t_scratch=self._t(A))
-                    with ev("swiglu", p.name):
-                        swiglu_bf16(packed, h=y)
+                        lora_gateup_swiglu(acts[p.act], Ag, Bg, Au, Bu, packed, h=y,
+                                           t_scratch=self.t[2 * lora_pad(Ag.shape[0])])
                 else:
                     with ev("gemm", p.name):
                         gu(qx, sx, qw, sw, b, h=y)
