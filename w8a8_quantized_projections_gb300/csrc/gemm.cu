@@ -182,9 +182,21 @@ __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(_
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ float silu_mul(float g, float u) {
+// silu(g) * u = g / (1 + exp(-g)) * u in fp32, two ways whose bf16 results
+// both stay within one ulp of the correctly rounded libm value.
+// IEEE: CUDA expf and a correctly rounded division.
+__device__ __forceinline__ float silu_mul_ieee(float g, float u) {
     const float d = __fadd_rn(1.0f, expf(-g));
     return __fmul_rn(__fdiv_rn(g, d), u);
+}
+
+// Fast: the hardware exp2 and reciprocal approximations (a few fp32 ulps).
+// Denominators above 2^126 (g below about -87) are scaled by 2^-64 with the
+// numerator, exactly, to keep the fast quotient in its accurate range.
+__device__ __forceinline__ float silu_mul_fast(float g, float u) {
+    const float d = __fadd_rn(1.0f, __expf(-g));
+    const float sc = d > 0x1p126f ? 0x1p-64f : 1.0f;
+    return __fmul_rn(__fdividef(g * sc, d * sc), u);
 }
 
 // Epilogue value of one accumulator: ((acc * sa) * sb) + bias, each rounded.
@@ -547,6 +559,14 @@ struct Gemm {
         return half * (BN / C::kParts) + 32 * j;
     }
 
+    // The fused SwiGLU's silu: the fast form for INT8 (399 against 410 us on
+    // the 1502-token gate/up shape), the IEEE form for FP8, where the fast one
+    // measured slower (103 against 100 us).
+    static __device__ __forceinline__ float silu(float g, float u) {
+        if constexpr (OP == kOpI8) return silu_mul_fast(g, u);
+        else return silu_mul_ieee(g, u);
+    }
+
     // Finish 32 consecutive output columns n0.. of one row from 32 fp32
     // accumulator values (for SwiGLU: gate values v, up values u).
     static __device__ __forceinline__ void finish32(const GemmArgs &a, int row, bool row_ok,
@@ -572,7 +592,7 @@ struct Gemm {
                     const float su[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        y[i] = silu_mul(y[i], scale_bias(u[8 * g + i], sa, su[i], a.bias, nu + i));
+                        y[i] = silu(y[i], scale_bias(u[8 * g + i], sa, su[i], a.bias, nu + i));
                 }
             } else if (EPI == kEpiAddBF16) {
                 const uint4 o = *reinterpret_cast<const uint4 *>(
@@ -763,8 +783,8 @@ struct Gemm {
                 const float g_hi = bf16_round(__fadd_rn(bf16_hi(gw[k]), __uint_as_float(ag[2 * k + 1])));
                 const float u_lo = bf16_round(__fadd_rn(bf16_lo(uw[k]), __uint_as_float(au[2 * k])));
                 const float u_hi = bf16_round(__fadd_rn(bf16_hi(uw[k]), __uint_as_float(au[2 * k + 1])));
-                h[2 * k] = silu_mul(g_lo, u_lo);
-                h[2 * k + 1] = silu_mul(g_hi, u_hi);
+                h[2 * k] = silu_mul_fast(g_lo, u_lo);
+                h[2 * k + 1] = silu_mul_fast(g_hi, u_hi);
             }
             const int r = row0 + rr;
             if (r < a.M && n < a.N)

@@ -15,9 +15,15 @@ namespace {
 __device__ __forceinline__ float lo16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// silu(g) * u = g / (1 + exp(-g)) * u in fp32 with the hardware exp2 and
+// reciprocal approximations (a few fp32 ulps; the bf16 result stays within
+// one ulp of the correctly rounded value).  Denominators above 2^126 are
+// scaled by 2^-64 with the numerator, exactly, to keep the fast quotient in
+// its accurate range.  The fused LoRA gate/up kernel uses the same sequence.
 __device__ __forceinline__ float silu_mul(float g, float u) {
-    const float d = __fadd_rn(1.0f, expf(-g));
-    return __fmul_rn(__fdiv_rn(g, d), u);
+    const float d = __fadd_rn(1.0f, __expf(-g));
+    const float sc = d > 0x1p126f ? 0x1p-64f : 1.0f;
+    return __fmul_rn(__fdividef(g * sc, d * sc), u);
 }
 
 __device__ __forceinline__ uint32_t pack(float lo, float hi) {
