@@ -103,7 +103,17 @@ struct Cfg {
     static constexpr int kOutColsPerTile = kSwiGLU ? BN / 2 : BN;
     // full[s]: TMA (native) or the local converter warps (INT8); in pair mode
     // the leader's barrier also counts the peer's forwarded readiness.
-    static constexpr int kFullArrivals = kI8 ? kConvWarps : 1;
+    // The converter warps form kConvGroups groups of kGroupWarps; group g
+    // widens k-blocks g, g + kConvGroups, ... of the CTA's k-block sequence, so
+    // a warp pays its per-k-block waits, fence and arrives once every
+    // kConvGroups k-blocks (1, 2, 3 groups: 1502 x 34816 x 5120 in 399, 381,
+    // 359 us).  A group's successive k-blocks may lie no more than NSTAGE
+    // apart: each of its waits on a stage barrier then targets the phase just
+    // after one it has seen complete, never two ahead (the parity test of an
+    // mbarrier wait cannot tell those apart).
+    static constexpr int kConvGroups = PAIR ? 3 : 2;   // single CTAs have 2 fp16 stages
+    static constexpr int kGroupWarps = kConvWarps / kConvGroups;
+    static constexpr int kFullArrivals = kI8 ? kGroupWarps : 1;
     static constexpr int kAccEmptyArrivals = kEpiWarps * (PAIR ? 2 : 1);
     static constexpr int kSmemBytes = NSTAGE * kStage + NRAW * kRawStage + kEpiStage + 1024 + 512;
     static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
@@ -111,6 +121,8 @@ struct Cfg {
     static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
     static_assert(kSmemBytes <= 232448, "shared memory");
     static_assert(NSTAGE >= 2, "pipeline depth");
+    static_assert(!kI8 || (kConvWarps % kConvGroups == 0 && kConvGroups <= NSTAGE && kConvGroups <= NRAW),
+                  "converter groups");
 };
 
 struct Barriers {
@@ -435,54 +447,60 @@ struct Gemm {
     // where S = threads / 4 is a multiple of 8, so the 128-byte swizzle phase
     // (row & 7) of a thread's rows is constant and all shared addresses are a
     // per-thread base plus compile-time offsets.
-    static __device__ void converter(const Ctx &c, int ctid) {
-        constexpr int kThr = (C::kI8 ? C::kConvWarps : 6) * 32;  // native ops never call this
+    static __device__ void converter(const Ctx &c, int ctid_all) {
+        constexpr int kThr = (C::kI8 ? C::kGroupWarps : 2) * 32;  // native ops never call this
+        constexpr int kG = C::kI8 ? C::kConvGroups : 1;
         constexpr int kRows = C::BM + C::kBRows;
         constexpr int kPer = (kRows * 4 + kThr - 1) / kThr;     // the last task may be partial
         static_assert(!C::kI8 || (kThr / 4) % 8 == 0, "constant swizzle phase");
         constexpr uint32_t kSrcStep = (kThr / 4) * 64, kDstStep = (kThr / 4) * 128;
+        const int group = ctid_all / kThr, ctid = ctid_all - group * kThr;
         const int row0 = ctid >> 2, piece = ctid & 3, phase = row0 & 7;
         const uint32_t src0 = (uint32_t)(row0 * 64 + piece * 16);
         const uint32_t dst0 = (uint32_t)(row0 * 128 + (((2 * piece) ^ phase) << 4));
         const uint32_t dst1 = (uint32_t)(row0 * 128 + (((2 * piece + 1) ^ phase) << 4));
         const uint32_t raw_base = smem_u32(c.raw), stage_base = smem_u32(c.stage);
         const int lane = threadIdx.x & 31;
-        uint32_t rs = 0, rph = 0, cs = 0, cph = 0;
-        for (int t = c.slot; t < c.num_tiles; t += c.nslots) {
-            for (int kb = 0; kb < c.nkb; ++kb) {
-                if (!mbar_wait(&c.bar->raw_full[rs], rph, c.w, kSiteConvRaw)) return;
-                if (!wait_pair(&c.bar->empty[cs], cph ^ 1u, c, kSiteConvEmpty)) return;
-                const uint32_t src = raw_base + rs * C::kRawStage + src0;
-                const uint32_t dst = stage_base + cs * C::kStage;
-                constexpr int kBatch = kPer >= 4 ? 4 : kPer;  // loads in flight per thread
+        // this CTA's k-blocks in order: tiles slot, slot + nslots, ... times nkb
+        const int tiles = c.slot < c.num_tiles ? (c.num_tiles - 1 - c.slot) / c.nslots + 1 : 0;
+        const int total = tiles * c.nkb;
+        uint32_t rs = (uint32_t)group, rph = 0, cs = (uint32_t)group, cph = 0;
+        for (int kidx = group; kidx < total; kidx += kG) {
+            if (!mbar_wait(&c.bar->raw_full[rs], rph, c.w, kSiteConvRaw)) return;
+            if (!wait_pair(&c.bar->empty[cs], cph ^ 1u, c, kSiteConvEmpty)) return;
+            const uint32_t src = raw_base + rs * C::kRawStage + src0;
+            const uint32_t dst = stage_base + cs * C::kStage;
+            constexpr int kBatch = kPer >= 4 ? 4 : kPer;  // loads in flight per thread
 #pragma unroll
-                for (int j0 = 0; j0 < kPer; j0 += kBatch) {
-                    uint4 w[kBatch];
+            for (int j0 = 0; j0 < kPer; j0 += kBatch) {
+                uint4 w[kBatch];
 #pragma unroll
-                    for (int j = 0; j < kBatch; ++j)
-                        if (j0 + j < kPer && row0 + (kThr / 4) * (j0 + j) < kRows)
-                            w[j] = lds128(src + (j0 + j) * kSrcStep);
+                for (int j = 0; j < kBatch; ++j)
+                    if (j0 + j < kPer && row0 + (kThr / 4) * (j0 + j) < kRows)
+                        w[j] = lds128(src + (j0 + j) * kSrcStep);
 #pragma unroll
-                    for (int j = 0; j < kBatch; ++j) {
-                        if (j0 + j >= kPer || row0 + (kThr / 4) * (j0 + j) >= kRows) continue;
-                        uint32_t f[8];
-                        s8x4_to_f16x4(w[j].x, f[0], f[1]);
-                        s8x4_to_f16x4(w[j].y, f[2], f[3]);
-                        s8x4_to_f16x4(w[j].z, f[4], f[5]);
-                        s8x4_to_f16x4(w[j].w, f[6], f[7]);
-                        sts128(dst + dst0 + (j0 + j) * kDstStep, f[0], f[1], f[2], f[3]);
-                        sts128(dst + dst1 + (j0 + j) * kDstStep, f[4], f[5], f[6], f[7]);
-                    }
+                for (int j = 0; j < kBatch; ++j) {
+                    if (j0 + j >= kPer || row0 + (kThr / 4) * (j0 + j) >= kRows) continue;
+                    uint32_t f[8];
+                    s8x4_to_f16x4(w[j].x, f[0], f[1]);
+                    s8x4_to_f16x4(w[j].y, f[2], f[3]);
+                    s8x4_to_f16x4(w[j].z, f[4], f[5]);
+                    s8x4_to_f16x4(w[j].w, f[6], f[7]);
+                    sts128(dst + dst0 + (j0 + j) * kDstStep, f[0], f[1], f[2], f[3]);
+                    sts128(dst + dst1 + (j0 + j) * kDstStep, f[4], f[5], f[6], f[7]);
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&c.bar->full[cs]);
-                    mbar_arrive(&c.bar->raw_empty[rs]);
-                }
-                if (++rs == (uint32_t)C::NRAW) { rs = 0; rph ^= 1u; }
-                if (++cs == (uint32_t)C::NSTAGE) { cs = 0; cph ^= 1u; }
             }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&c.bar->full[cs]);
+                mbar_arrive(&c.bar->raw_empty[rs]);
+            }
+            // the group's next k-block is kG ahead in both rings (kG <= ring sizes)
+            rs += kG;
+            if (rs >= (uint32_t)C::NRAW) { rs -= C::NRAW; rph ^= 1u; }
+            cs += kG;
+            if (cs >= (uint32_t)C::NSTAGE) { cs -= C::NSTAGE; cph ^= 1u; }
         }
     }
 
@@ -917,7 +935,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
         for (int s = 0; s < C::NRAW; ++s) {
             mbar_init(&bar->raw_full[s], 1);
-            mbar_init(&bar->raw_empty[s], C::kConvWarps);
+            mbar_init(&bar->raw_empty[s], C::kGroupWarps);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar->acc_full[s], 1);
