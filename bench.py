@@ -370,6 +370,26 @@ def main():
         "wall_s_timed_region": wall,
     }
 
+    # ---- the same step replayed from a CUDA graph (launch overhead removed)
+    layer.capture(acts)
+    g_ev = []
+    for _ in range(args.warmup):
+        layer.replay()
+    torch.cuda.synchronize(dev)
+    for _ in range(args.steps):
+        flush.zero_()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        layer.replay()
+        g1.record(stream)
+        g_ev.append((g0, g1))
+    torch.cuda.synchronize(dev)
+    g_t = sum(a.elapsed_time(b) for a, b in g_ev) / 1e3
+    line["graph"] = {"value": ops_step * args.steps / g_t / 1e12, "unit": "TOPS",
+                     "ms_per_step": 1e3 * g_t / args.steps,
+                     "note": "the step captured once in a CUDA graph and replayed (one launch per step)"}
+
     # ---- end to end through the C ABI with host buffers
     if not args.no_e2e:
         line["e2e"] = e2e(args, layer, acts, acts_np, cfg, dev, stream, world, torch)

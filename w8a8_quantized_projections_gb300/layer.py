@@ -181,6 +181,28 @@ class QuantizedLayer:
                                  t_scratch=self._t(A))
         return self.out
 
+    def capture(self, acts: Dict[str, torch.Tensor]) -> "torch.cuda.CUDAGraph":
+        """Record one step on ``acts`` into a CUDA graph (after a warm-up step
+        on a side stream, which performs the library's one-time per-device and
+        per-kernel set-up outside the capture).  ``replay()`` then reruns the
+        step's launches on the same input and output buffers with one launch
+        of the graph; refill the input tensors in place to step on new data."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.step(acts)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.step(acts)
+        self.graph = graph
+        return graph
+
+    def replay(self) -> Dict[str, torch.Tensor]:
+        self.graph.replay()
+        return self.out
+
     def _t(self, A):
         return self.t[lora_pad(A.shape[0])]
 
