@@ -58,6 +58,7 @@ def lib():
             L.orc_e4m3_decode.argtypes = [C.c_uint8]; L.orc_e4m3_decode.restype = C.c_double
             L.orc_e4m3_encode.argtypes = [C.c_float]; L.orc_e4m3_encode.restype = C.c_uint8
             L.orc_quant_fp8.argtypes = [u16p, i64, i64, i64, C.c_int, u8p, f32p]
+            L.orc_quant_static.argtypes = [u16p, i64, i64, i64, C.c_int, C.c_float, C.c_void_p, f32p]
             L.orc_int8_gemm_acc.argtypes = [i8p, i8p, i64, i64, i64, _P(C.c_int32)]
             L.orc_int8_linear.argtypes = [i8p, f32p, i8p, f32p, u16p, i64, i64, i64, u16p, i64]
             L.orc_swiglu_f32.argtypes = [C.c_float, C.c_float]; L.orc_swiglu_f32.restype = C.c_float
@@ -163,6 +164,19 @@ def quant_fp8(x: np.ndarray, rotate: bool = False):
     _check(lib().orc_quant_fp8(_ptr(x, C.c_uint16), M, K, K, int(rotate), _ptr(q, C.c_uint8),
                                _ptr(s, C.c_float)), "quant_fp8")
     return q, s
+
+
+def quant_static(x: np.ndarray, s: float, mode: str = "fp8"):
+    """(codes [M][K], scales [M] all equal to s) with one static scale s:
+    mode "int8_h128" (int8 codes), "fp8" or "fp8_h128" (e4m3 codes as uint8)."""
+    x = _c(x, np.uint16)
+    M, K = x.shape
+    m = {"int8_h128": 0, "fp8": 1, "fp8_h128": 2}[mode]
+    q = np.empty((M, K), np.int8 if m == 0 else np.uint8)
+    sout = np.empty(M, np.float32)
+    _check(lib().orc_quant_static(_ptr(x, C.c_uint16), M, K, K, m, float(np.float32(s)),
+                                  q.ctypes.data_as(C.c_void_p), _ptr(sout, C.c_float)), "quant_static")
+    return q, sout
 
 
 # ---------------------------------------------------------------- GEMMs

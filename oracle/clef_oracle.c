@@ -305,6 +305,47 @@ int orc_quant_fp8(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int rota
     return ORC_OK;
 }
 
+/* Static-scale quantiser: one caller-given scale s > 0 for the whole tensor
+ * (a calibrated scale, in place of the per-token amax of the dynamic modes).
+ * r = fp32(1 / s); v is the rotated row (mode 0: INT8 with block-128
+ * rotation; mode 2: FP8 with rotation) or the row itself (mode 1: FP8);
+ * INT8 codes q = clamp(rne(fp32(v * r)), -127, 127), FP8 codes
+ * e4m3(fp32(v * r)) with saturation to +-448; every row's scale is s. */
+int orc_quant_static(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int mode, float s,
+                     void *q, float *sout)
+{
+    if (M < 0 || K <= 0 || ldx < K || mode < 0 || mode > 2 || !(s > 0.0f) || isinf(s))
+        return ORC_ERR_ARG;
+    const int rotate = (mode != 1);
+    if (rotate && K % 128 != 0)
+        return ORC_ERR_ARG;
+    float *v = (float *)malloc((size_t)K * sizeof(float));
+    if (!v)
+        return ORC_ERR_NOMEM;
+    const float r = 1.0f / s;
+    for (int64_t m = 0; m < M; m++) {
+        if (rotate)
+            orc_rotate_rows_f32(x + m * ldx, 1, K, ldx, v);
+        else
+            for (int64_t k = 0; k < K; k++)
+                v[k] = bf16_to_f32(x[m * ldx + k]);
+        for (int64_t k = 0; k < K; k++) {
+            const float t = v[k] * r;
+            if (mode == 0) {
+                float c = rne_int(t);
+                if (c > 127.0f) c = 127.0f;
+                if (c < -127.0f) c = -127.0f;
+                ((int8_t *)q)[m * K + k] = (int8_t)c;
+            } else {
+                ((uint8_t *)q)[m * K + k] = orc_e4m3_encode(t);
+            }
+        }
+        sout[m] = s;
+    }
+    free(v);
+    return ORC_OK;
+}
+
 /* ------------------------------------------------------------------ */
 /* INT8 GEMM and its fused epilogues                                   */
 /* ------------------------------------------------------------------ */

@@ -184,6 +184,40 @@ def test_int8_codes_are_rint_of_scaled_values(orc):
     assert np.array_equal(np.rint(np.array([0.5, 1.5, 2.5, -0.5, -2.5])), [0, 2, 2, -0, -2])
 
 
+def test_static_int8_codes_are_clamped_rint(orc):
+    """Static scale: codes are numpy's rint of fp32(v * fp32(1/s)) on the
+    (pinned) rotated values, clamped to [-127, 127] (a static scale lets
+    values overflow the range, unlike the per-token one); every row's scale
+    is s.  s = 2^-4 makes v * r exact, s = 0.037 exercises a rounded r."""
+    x = S.activation(0, "pin/static8", 5, 256)
+    v = orc.rotate_rows(x)
+    for sc in (0.0625, 0.037):
+        q, sout = orc.quant_static(x, sc, "int8_h128")
+        r = np.float32(1.0) / np.float32(sc)
+        want = np.clip(np.rint((v * r).astype(np.float32)), -127, 127).astype(np.int8)
+        assert np.array_equal(q, want) and np.all(sout == np.float32(sc))
+        assert (np.abs(v * r) > 127.5).any(), "some values saturate"
+        assert q.min() == -127 and q.max() == 127
+
+
+def test_static_fp8_codes_match_the_encoder_and_saturate(orc):
+    """Static FP8: each code is the (pinned) e4m3 encoding of fp32(v * fp32(1/s)),
+    unrotated and rotated; values beyond 448 * s saturate to +-448; with a
+    power-of-two s the codes equal torch's float8 cast of v / s."""
+    x = S.activation(0, "pin/static8f", 4, 256)
+    for mode, v in (("fp8", S.bf16_bits_to_f64(x).astype(np.float32)), ("fp8_h128", orc.rotate_rows(x))):
+        for sc in (2.0 ** -7, 0.0123):
+            q, sout = orc.quant_static(x, sc, mode)
+            t = (v * (np.float32(1.0) / np.float32(sc))).astype(np.float32)
+            want = np.array([orc.e4m3_encode(float(f)) for f in t.ravel()], np.uint8).reshape(t.shape)
+            assert np.array_equal(q, want) and np.all(sout == np.float32(sc))
+            big = np.abs(t) >= 448
+            assert big.any() and np.all((q[big] & 0x7F) == 0x7E)
+            if sc == 2.0 ** -7:
+                ref = torch.from_numpy(np.clip(t, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+                assert np.array_equal(q, ref)
+
+
 # ------------------------------------------------------------------ e4m3
 
 def _finite_codes():
