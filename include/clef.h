@@ -91,6 +91,20 @@ int clef_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, int mode,
                    void *q, float *scale, void *stream);
 
 /*
+ * clef_quant_act_static -- the quantizer with one static scale s for the
+ * whole tensor (a calibrated scale [INT8: "calibrated scales" of the
+ * Benefits list]) in place of the per-token amax:
+ *   v as in clef_quant_act; r = fp32(1 / s);
+ *   INT8:  q = clamp(rne(fp32(v * r)), -127, 127)
+ *   FP8:   q = e4m3_rn_satfinite(fp32(v * r))   (saturates at +-448)
+ *   scale[m] = s for every row, so the GEMM entry points apply unchanged.
+ * s must be positive and finite; other arguments and requirements as for
+ * clef_quant_act.
+ */
+int clef_quant_act_static(const void *x, int64_t M, int64_t K, int64_t ldx, int mode,
+                          float s, void *q, float *scale, void *stream);
+
+/*
  * clef_w8a8_linear -- W8A8 INT8 linear with the fused scale/bias epilogue
  * [INT8: Benefits, "fuse calibrated scales, biases"].
  *   acc[m][n] = sum_k qx[m][k] * qw[n][k]        (exact int32)

@@ -53,6 +53,11 @@ def test_quant_act_rejects_bad_arguments(args):
     assert clef.library().clef_quant_act(*args) == 1
 
 
+@pytest.mark.parametrize("sc", [0.0, -1.0, float("inf"), float("nan")])
+def test_quant_act_static_rejects_bad_scales(sc):
+    assert clef.library().clef_quant_act_static(FAKE, 4, 128, 128, 1, sc, FAKE, FAKE, S) == 1
+
+
 @pytest.mark.parametrize("name", ["clef_w8a8_linear", "clef_fp8_linear", "clef_w8a8_gateup_swiglu",
                                   "clef_fp8_gateup_swiglu"])
 @pytest.mark.parametrize("bad", ["null_qx", "N8", "K16", "ldy", "align", "sw_align"])

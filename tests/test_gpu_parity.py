@@ -86,6 +86,20 @@ def test_quant_fp8_bitexact(orc, staging, mode, M, K):
                              f"oracle {rq[m, k]:#x}")
 
 
+@pytest.mark.parametrize("mode,sc", [("int8_h128", 0.0625), ("int8_h128", 0.037), ("fp8", 2.0 ** -7),
+                                     ("fp8", 0.0123), ("fp8_h128", 0.0123)])
+@pytest.mark.parametrize("M,K", [(300, 2048), (1502, 5120)])
+def test_quant_static_bitexact(orc, staging, mode, sc, M, K):
+    """Static per-tensor scale: codes (saturating) and scales bit-exact, on
+    both quantizer kernels."""
+    x = S.activation(0, f"t/qs/{M}x{K}", M, K)
+    q, s = clef.quant_act_static(bf16_dev(x), sc, mode)
+    rq, rs = par_rows(lambda a, b: orc.quant_static(x[a:b], sc, mode), M)
+    assert np.array_equal(host(s), rs)
+    got = host(q)
+    assert np.array_equal(got.view(rq.dtype), rq)
+
+
 def test_quant_empty_rows():
     x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
     q, s = clef.quant_act(x, "int8_h128")

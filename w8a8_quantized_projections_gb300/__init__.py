@@ -20,7 +20,7 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "ClefError", "library", "library_path", "quant_act", "w8a8_linear", "w8a8_gateup_swiglu",
+    "ClefError", "library", "library_path", "quant_act", "quant_act_static", "w8a8_linear", "w8a8_gateup_swiglu",
     "fp8_linear", "fp8_gateup_swiglu", "lora_add", "lora_add_noalloc", "lora_gateup_swiglu", "swiglu_bf16",
     "w8a8_gemm_s32",
     "poll_status", "set_wait_limit_ns", "set_quant_staging", "ACT_MODES",
@@ -56,6 +56,7 @@ def library():
             vp, i64, i32 = C.c_void_p, C.c_int64, C.c_int
             sigs = {
                 "clef_quant_act": [vp, i64, i64, i64, i32, vp, vp, vp],
+                "clef_quant_act_static": [vp, i64, i64, i64, i32, C.c_float, vp, vp, vp],
                 "clef_w8a8_linear": [vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp],
                 "clef_w8a8_gateup_swiglu": [vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp],
                 "clef_fp8_linear": [vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp],
@@ -135,6 +136,21 @@ def quant_act(x: torch.Tensor, mode: str = "int8_h128", q=None, scale=None, stre
         scale = torch.empty((M,), dtype=torch.float32, device=x.device)
     _dense(q, "q")
     _call("clef_quant_act", _ptr(x), M, K, ldx, m, _ptr(q), _ptr(scale), _stream(x, stream))
+    return q, scale
+
+
+def quant_act_static(x: torch.Tensor, s: float, mode: str = "fp8", q=None, scale=None, stream=None):
+    """Quantizer with one static scale s for every row: returns (codes, scales = s)."""
+    _cuda(x, "x", (torch.bfloat16,))
+    ldx = _rows(x, "x")
+    M, K = x.shape
+    m = ACT_MODES[mode]
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.int8 if m == 0 else torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _dense(q, "q")
+    _call("clef_quant_act_static", _ptr(x), M, K, ldx, m, float(s), _ptr(q), _ptr(scale), _stream(x, stream))
     return q, scale
 
 

@@ -230,10 +230,12 @@ void internal_set_error(const char *msg) { snprintf(g_last_err, sizeof g_last_er
 
 using namespace clef;
 
-extern "C" {
+namespace {
 
-int clef_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, int mode, void *q,
-                   float *scale, void *stream) {
+// Checks and launch shared by the dynamic and static quantizer entry points
+// (static_s > 0: one static scale for every row).
+int quant_common(const void *x, int64_t M, int64_t K, int64_t ldx, int mode, void *q, float *scale,
+                 float static_s, void *stream) {
     if (mode != CLEF_ACT_INT8_H128 && mode != CLEF_ACT_FP8_E4M3 && mode != CLEF_ACT_FP8_E4M3_H128)
         return arg_fail("unknown quantizer mode");
     if (M < 0 || M > 0x7FFFFFFF) return arg_fail("M out of range");
@@ -253,10 +255,30 @@ int clef_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, int mode, v
     env.status = d->status;
     env.wait_limit_ns = g_wait_limit_ns.load();
     env.staging = g_quant_staging.load();
+    if (static_s > 0.0f) {
+        volatile float one = 1.0f;   // one IEEE fp32 division, as the definition states
+        env.static_r = one / static_s;
+        env.static_s = static_s;
+    }
     cudaError_t e = launch_quant_act(mode, static_cast<const uint16_t *>(x), M, K, ldx,
                                      static_cast<uint8_t *>(q), scale, env,
                                      static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CLEF_OK : cuda_fail(e, "quantizer launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+int clef_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, int mode, void *q,
+                   float *scale, void *stream) {
+    return quant_common(x, M, K, ldx, mode, q, scale, 0.0f, stream);
+}
+
+int clef_quant_act_static(const void *x, int64_t M, int64_t K, int64_t ldx, int mode, float s,
+                          void *q, float *scale, void *stream) {
+    if (!(s > 0.0f) || s > 3.0e38f) return arg_fail("static scale must be positive and finite");
+    return quant_common(x, M, K, ldx, mode, q, scale, s, stream);
 }
 
 int clef_w8a8_linear(const int8_t *qx, const float *sx, const int8_t *qw, const float *sw,

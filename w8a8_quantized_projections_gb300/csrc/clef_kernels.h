@@ -19,6 +19,9 @@ struct QuantEnv {
     unsigned int *status;
     uint64_t wait_limit_ns;
     int staging;
+    // static scale (static_r > 0): codes use r = static_r = fp32(1 / static_s)
+    // for every row and every row's scale is static_s; 0: per-token amax
+    float static_r = 0.0f, static_s = 0.0f;
 };
 
 cudaError_t launch_quant_act(int mode, const uint16_t *x, int64_t M, int64_t K, int64_t ldx,

@@ -152,7 +152,9 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 
 // Codes of one 32-element chunk (r = qmax / amax of the row), written as two
 // 16-byte stores.
-template <bool kInt8>
+// kClamp (static scales, INT8): values may exceed the code range; the
+// saturating pack gives -128 below it, raised to -127 by a signed-byte max.
+template <bool kInt8, bool kClamp = false>
 __device__ __forceinline__ void store_codes(const float (&v)[32], float r, bool zero_row,
                                             uint8_t *dst8) {
     uint32_t w[8];
@@ -167,6 +169,7 @@ __device__ __forceinline__ void store_codes(const float (&v)[32], float r, bool 
             unf2(mul2(f2(v[4 * i + 2], v[4 * i + 3]), r2), u[2], u[3]);
             w[i] = pack_s8x4(__float2int_rn(u[0]), __float2int_rn(u[1]), __float2int_rn(u[2]),
                              __float2int_rn(u[3]));
+            if (kClamp) w[i] = __vmaxs4(w[i], 0x81818181u);
         }
     } else {
 #pragma unroll
@@ -191,7 +194,8 @@ template <int MODE, int C, int MAXT, int MINB>
 __global__ void __launch_bounds__(MAXT, MINB) quant_act_kernel(const uint16_t *__restrict__ x,
                                                          int64_t K, int64_t ldx,
                                                          uint8_t *__restrict__ q,
-                                                         float *__restrict__ scale) {
+                                                         float *__restrict__ scale,
+                                                         float static_r, float static_s) {
     constexpr bool kRotate = (MODE == kActInt8H128 || MODE == kActFp8H128);
     constexpr bool kInt8 = (MODE == kActInt8H128);
     __shared__ float red[32];
@@ -233,16 +237,18 @@ __global__ void __launch_bounds__(MAXT, MINB) quant_act_kernel(const uint16_t *_
     amax = red[0];
 
     const float qmax = kInt8 ? 127.0f : 448.0f;
-    const bool zero_row = !(amax > 0.0f);
-    const float r = zero_row ? 0.0f : __fdiv_rn(qmax, amax);  // zero row: every v * 0 = 0
-    if (tid == 0) scale[m] = zero_row ? 0.0f : __fdiv_rn(amax, qmax);
+    const bool stat = static_r > 0.0f;   // static scale: the row's amax is not used
+    const bool zero_row = !stat && !(amax > 0.0f);
+    const float r = stat ? static_r : (zero_row ? 0.0f : __fdiv_rn(qmax, amax));
+    if (tid == 0) scale[m] = stat ? static_s : (zero_row ? 0.0f : __fdiv_rn(amax, qmax));
 
     uint8_t *qr = q + m * K;
 #pragma unroll
     for (int c = 0; c < C; ++c) {
         const int ch = tid + c * blockDim.x;
         if (ch >= nchunk) continue;
-        store_codes<kInt8>(v[c], r, zero_row, qr + 32 * (int64_t)ch);
+        if (stat) store_codes<kInt8, kInt8>(v[c], r, false, qr + 32 * (int64_t)ch);
+        else store_codes<kInt8>(v[c], r, zero_row, qr + 32 * (int64_t)ch);
     }
 }
 
@@ -275,7 +281,8 @@ template <int MODE, int MAXT, int MINB>
 __global__ void __launch_bounds__(MAXT, MINB)
 quant_staged_kernel(const __grid_constant__ CUtensorMap tmx, int M, int K, int nslot,
                     uint32_t slot_stride, int nbox, int box_rows, uint8_t *__restrict__ q,
-                    float *__restrict__ scale, unsigned int *status, uint64_t limit_ns) {
+                    float *__restrict__ scale, unsigned int *status, uint64_t limit_ns,
+                    float static_r, float static_s) {
     constexpr bool kRotate = (MODE == kActInt8H128 || MODE == kActFp8H128);
     constexpr bool kInt8 = (MODE == kActInt8H128);
     extern __shared__ uint8_t dyn[];
@@ -366,10 +373,14 @@ quant_staged_kernel(const __grid_constant__ CUtensorMap tmx, int M, int K, int n
         for (int k = 1; k < nw; ++k) amax = fmaxf(amax, red[it & 1][k]);
 
         const float qmax = kInt8 ? 127.0f : 448.0f;
-        const bool zero_row = !(amax > 0.0f);
-        const float r = zero_row ? 0.0f : __fdiv_rn(qmax, amax);  // zero row: every v * 0 = 0
-        if (tid == 0) scale[m] = zero_row ? 0.0f : __fdiv_rn(amax, qmax);
-        if (active) store_codes<kInt8>(v, r, zero_row, q + (int64_t)m * K + 32 * tid);
+        const bool stat = static_r > 0.0f;   // static scale: the row's amax is not used
+        const bool zero_row = !stat && !(amax > 0.0f);
+        const float r = stat ? static_r : (zero_row ? 0.0f : __fdiv_rn(qmax, amax));
+        if (tid == 0) scale[m] = stat ? static_s : (zero_row ? 0.0f : __fdiv_rn(amax, qmax));
+        if (active) {
+            if (stat) store_codes<kInt8, kInt8>(v, r, false, q + (int64_t)m * K + 32 * tid);
+            else store_codes<kInt8>(v, r, zero_row, q + (int64_t)m * K + 32 * tid);
+        }
     }
     if (abort_flag && tid == 0) {
         // let the copies already issued into the ring land before the CTA exits
@@ -451,7 +462,8 @@ cudaError_t launch_staged(const StagedPlan &p, const uint16_t *x, int64_t M, int
     const int64_t want = (int64_t)per_sm * env.num_sms;
     const int grid = (int)(M < want ? M : want);
     kern<<<grid, p.threads, p.smem, st>>>(tm, (int)M, (int)K, p.nslot, p.slot_stride, p.nbox,
-                                          p.box_rows, q, scale, env.status, env.wait_limit_ns);
+                                          p.box_rows, q, scale, env.status, env.wait_limit_ns,
+                                          env.static_r, env.static_s);
     return cudaGetLastError();
 }
 
@@ -468,14 +480,17 @@ cudaError_t launch_mode(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, ui
     const int64_t nchunk = K / 32;
     if (nchunk <= 576) {
         const int T = (int)((nchunk + 31) / 32 * 32);
-        quant_act_kernel<MODE, 1, 576, 2><<<(unsigned)M, T, 0, st>>>(x, K, ldx, q, scale);
+        quant_act_kernel<MODE, 1, 576, 2><<<(unsigned)M, T, 0, st>>>(x, K, ldx, q, scale, env.static_r,
+                                                                      env.static_s);
     } else if (nchunk <= 1024) {
         const int T = (int)((nchunk + 31) / 32 * 32);
-        quant_act_kernel<MODE, 1, 1024, 1><<<(unsigned)M, T, 0, st>>>(x, K, ldx, q, scale);
+        quant_act_kernel<MODE, 1, 1024, 1><<<(unsigned)M, T, 0, st>>>(x, K, ldx, q, scale, env.static_r,
+                                                                      env.static_s);
     } else {
         const int64_t per = (nchunk + 1) / 2;
         const int T = (int)((per + 31) / 32 * 32);
-        quant_act_kernel<MODE, 2, 1024, 1><<<(unsigned)M, T, 0, st>>>(x, K, ldx, q, scale);
+        quant_act_kernel<MODE, 2, 1024, 1><<<(unsigned)M, T, 0, st>>>(x, K, ldx, q, scale, env.static_r,
+                                                                      env.static_s);
     }
     return cudaGetLastError();
 }
