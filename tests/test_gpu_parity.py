@@ -51,7 +51,7 @@ def staging(request):
 
 
 @pytest.mark.parametrize("M,K", [(298, 2048), (1, 128), (5, 384), (130, 5120), (1502, 17408),
-                                 (2270, 6144), (3, 40960), (12000, 5120), (2, 128 * 131)])
+                                 (2270, 6144), (3, 40960), (12000, 5120), (2, 128 * 131), (4, 65536)])
 def test_quant_int8_h128_bitexact(orc, staging, M, K):
     x = special_rows(S.activation(0, f"t/q8/{M}x{K}", M, K))
     q, s = clef.quant_act(bf16_dev(x), "int8_h128")
@@ -126,6 +126,22 @@ def test_int8_gemm_s32_bitexact(orc, M, N, K):
     acc = host(clef.w8a8_gemm_s32(dev(qx), dev(qw)))
     ref = par_rows(lambda a, b: orc.int8_gemm_acc(qx[a:b], qw), M)
     assert np.array_equal(acc, ref)
+
+
+def test_int8_gemm_s32_max_depth(orc):
+    """K = 65536, the largest depth the quantizer accepts: all codes 127 give
+    127 * 127 * 65536 = 1,057,030,144 (still an int32), exact through 64
+    fp32 chunks; mixed signs and a random row check the rest."""
+    M, N, K = 3, 24, 65536
+    rng = np.random.default_rng(17)
+    qx = np.full((M, K), 127, np.int8)
+    qx[1] = -127
+    qx[2] = rng.integers(-127, 128, K).astype(np.int8)
+    qw = np.full((N, K), 127, np.int8)
+    qw[5] = rng.integers(-127, 128, K).astype(np.int8)
+    acc = host(clef.w8a8_gemm_s32(dev(qx), dev(qw)))
+    assert acc[0, 0] == 127 * 127 * K and acc[1, 0] == -127 * 127 * K
+    assert np.array_equal(acc, orc.int8_gemm_acc(qx, qw))
 
 
 def test_int8_gemm_s32_adversarial(orc):
