@@ -242,6 +242,33 @@ def workload_config(cfg):
     return d
 
 
+# ---------------------------------------------------------------- replicas (N > 1)
+
+def replica_activations(cfg, acts_np, rank):
+    """Each rank's own batch: rank 0 keeps the workload's seed-0 activations,
+    rank r > 0 draws its own seeded tensors of the same shapes (weights are
+    shared by seed, so every rank runs the same layer)."""
+    if rank == 0:
+        return acts_np
+    return {n: S.activation(rank, f"{cfg.name}/act/{n}", cfg.M, x.shape[1]) for n, x in acts_np.items()}
+
+
+def max_over_ranks(value, world, dist, device):
+    """The largest of the ranks' values (timed seconds): the whole job takes as
+    long as its slowest replica."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tops(ops_per_step, steps, world, seconds):
+    """Throughput of all replicas together: every rank ran `steps` steps."""
+    return ops_per_step * steps * world / seconds / 1e12
+
+
 # ---------------------------------------------------------------- GPU arm
 
 def main():
@@ -267,8 +294,7 @@ def main():
 
     # replicas: each rank works on its own batch (seeded by rank), weights shared by seed
     acts_np, weights_np, lora_np = S.layer_inputs(cfg, seed=0)
-    if rank:
-        acts_np = {n: S.activation(rank, f"{cfg.name}/act/{n}", cfg.M, x.shape[1]) for n, x in acts_np.items()}
+    acts_np = replica_activations(cfg, acts_np, rank)
 
     def bf(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
@@ -311,13 +337,9 @@ def main():
     if status:
         raise RuntimeError(f"device status word reported {status}")
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
-    t_sum = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([t_sum], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_sum = float(t.item())
+    t_sum = max_over_ranks(sum(step_ms) / 1e3, world, dist, dev)
     ops_step = cfg.gemm_ops()
-    value = ops_step * args.steps * world / t_sum / 1e12
+    value = whole_job_tops(ops_step, args.steps, world, t_sum)
 
     # per-kernel times
     kt = {}
