@@ -440,36 +440,75 @@ def proj_input_K(cfg, act):
     raise KeyError(act)
 
 
+def weight_bytes(layer):
+    """Bytes of quantized weights one step reads (codes and scales)."""
+    return sum(qw.numel() * qw.element_size() + sw.numel() * sw.element_size()
+               for qw, sw, _ in layer.unit_w)
+
+
 def e2e(args, layer, acts, acts_np, cfg, dev, stream, world, torch):
-    """Same metric with host buffers: each step copies its activations in from
-    pinned host memory and the step's final output back, inside the timing."""
+    """Same metric with host buffers: every step copies its activations in
+    from pinned host memory and its final output back, inside the timing.
+    The copies run on a second stream, pipelined with the compute: step i+1's
+    inputs are copied into the other of two device input sets while step i
+    computes, and step i's output is read back while step i+1's first kernels
+    run (its last projection waits for that read before overwriting the
+    output buffer)."""
     host_in = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).pin_memory()
                for k, v in acts_np.items()}
     last = cfg.projections[-1].name
     out_dev = layer.out[last]
     host_out = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
-    dev_in = {k: torch.empty_like(v) for k, v in acts.items()}
+    dev_in = [{k: torch.empty_like(v) for k, v in acts.items()} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = host_out.numel() * host_out.element_size()
-    for _ in range(2):
-        for k in dev_in:
-            dev_in[k].copy_(host_in[k], non_blocking=True)
-        layer.step(dev_in)
-        host_out.copy_(out_dev, non_blocking=True)
+    copy = torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
+
+    def run(n):
+        in_ready = [ev(), ev()]
+        used = [None, None]          # step that last read input set b has finished
+        read_back = None             # the previous step's output has been read
+        with torch.cuda.stream(copy):
+            for k in dev_in[0]:
+                dev_in[0][k].copy_(host_in[k], non_blocking=True)
+            in_ready[0].record(copy)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:            # next step's inputs, into the other set
+                with torch.cuda.stream(copy):
+                    if used[1 - b] is not None:
+                        copy.wait_event(used[1 - b])
+                    for k in dev_in[1 - b]:
+                        dev_in[1 - b][k].copy_(host_in[k], non_blocking=True)
+                    in_ready[1 - b].record(copy)
+            stream.wait_event(in_ready[b])
+            layer.step(dev_in[b], final_wait=read_back)
+            done = ev()
+            done.record(stream)
+            used[b] = done
+            with torch.cuda.stream(copy):
+                copy.wait_event(done)
+                host_out.copy_(out_dev, non_blocking=True)
+                read_back = ev()
+                read_back.record(copy)
+        stream.wait_event(read_back)
+
+    run(2)
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        for k in dev_in:
-            dev_in[k].copy_(host_in[k], non_blocking=True)
-        layer.step(dev_in)
-        host_out.copy_(out_dev, non_blocking=True)
+    run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     t = e0.elapsed_time(e1) / 1e3
     return {"value": cfg.gemm_ops() * args.steps * world / t / 1e12, "unit": "TOPS",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "note": "input copies of step i+1 and the read-back of step i overlap the compute "
+                    "on a second stream; every step's copies are inside the timed region; no "
+                    "L2 flush between steps (each step streams all weights, "
+                    f"{weight_bytes(layer) / 1e6:.0f} MB, against a 126 MB L2)"}
 
 
 if __name__ == "__main__":

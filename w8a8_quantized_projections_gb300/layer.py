@@ -122,12 +122,16 @@ class QuantizedLayer:
                 n += 3 if p.kind == "gateup" else 2   # gate/up: two x A^T, one fused add + SwiGLU
         return n
 
-    def step(self, acts: Dict[str, torch.Tensor], events=None) -> Dict[str, torch.Tensor]:
+    def step(self, acts: Dict[str, torch.Tensor], events=None,
+             final_wait: Optional[torch.cuda.Event] = None) -> Dict[str, torch.Tensor]:
         """acts: activation name -> bf16 [M][K].  Returns the output buffers.
 
         events: optional dict; when given, CUDA events are recorded on the
         current stream around every launch, under keys ("quant", name) and
-        ("gemm", name), as (start, end) pairs appended to lists."""
+        ("gemm", name), as (start, end) pairs appended to lists.
+        final_wait: optional CUDA event the current stream waits for before the
+        step's last projection writes its output (e.g. the read-back of the
+        previous step's output on another stream)."""
         ev = _Rec(events)
         lin = fp8_linear if self.fp8 else w8a8_linear
         gu = fp8_gateup_swiglu if self.fp8 else w8a8_gateup_swiglu
@@ -136,7 +140,10 @@ class QuantizedLayer:
             with ev("quant", name):
                 quant_act(acts[name], self.mode, q=qx, scale=sx)
         prev_h = None
+        last = len(self.groups) - 1
         for gi, g in enumerate(self.groups):
+            if gi == last and final_wait is not None:
+                torch.cuda.current_stream().wait_event(final_wait)
             if len(g) > 1:
                 qw, sw, b = self.unit_w[gi]
                 qx, sx = self.q[g[0].act]
