@@ -123,7 +123,9 @@ int clef_w8a8_linear(const int8_t *qx, const float *sx, const int8_t *qw, const 
  * "MLP SwiGLU"].  qw_gu: int8 [2N][K] with the gate rows 0..N-1 followed by
  * the up rows N..2N-1; sw_gu, bias_gu: [2N] in the same order (bias may be
  * NULL).  With g, u the unrounded fp32 epilogue values of rows n and N+n:
- *   h[m][n] = bf16(g / (1 + expf(-g)) * u)
+ *   h[m][n] = bf16(g / (1 + exp(-g)) * u)
+ * evaluated in fp32 with the hardware exp2 and reciprocal approximations
+ * (the bf16 result is within one ulp of the correctly rounded value).
  * h: bf16 [M][N], row pitch ldh.  Requirements as clef_w8a8_linear.
  */
 int clef_w8a8_gateup_swiglu(const int8_t *qx, const float *sx, const int8_t *qw_gu,
@@ -144,7 +146,8 @@ int clef_fp8_linear(const void *qx, const float *sx, const void *qw, const float
 
 /*
  * clef_fp8_gateup_swiglu -- the FP8 counterpart of clef_w8a8_gateup_swiglu
- * (the paired SwiGLU epilogue of [USAGE] over the FP8 scheme of [FP8]).
+ * (the paired SwiGLU epilogue of [USAGE] over the FP8 scheme of [FP8]); its
+ * silu uses CUDA expf and a correctly rounded division.
  */
 int clef_fp8_gateup_swiglu(const void *qx, const float *sx, const void *qw_gu,
                            const float *sw_gu, const void *bias_gu,
@@ -175,7 +178,8 @@ int clef_lora_add(const void *x, int64_t ldx, const void *A, const void *B,
  * clef_lora_add,
  *   g[m][n] = bf16((float)y_gu[m][n]     + sum_j t_g[m][j] * B_gate[n][j])
  *   u[m][n] = bf16((float)y_gu[m][N + n] + sum_j t_u[m][j] * B_up[n][j])
- *   h[m][n] = bf16(silu(g) * u)   (fp32, silu(g) = g / (1 + exp(-g)))
+ *   h[m][n] = bf16(silu(g) * u)   (fp32, silu(g) = g / (1 + exp(-g)) as in
+ *                                  clef_swiglu_bf16)
  * -- the same rounded operations as two clef_lora_add calls on the halves of
  * y_gu followed by clef_swiglu_bf16, without writing g and u back.
  * x: bf16 [M][K], row pitch ldx; A_gate, A_up: bf16 [r][K] dense; B_gate,
@@ -194,7 +198,9 @@ int clef_lora_gateup_swiglu(const void *x, int64_t ldx, const void *A_gate, cons
 /*
  * clef_swiglu_bf16 -- the unfused MLP reading (fuse_mlp off in [USAGE]):
  * y_gu holds bf16 gate values in columns 0..N-1 and up values in N..2N-1
- * (row pitch ldg); h[m][n] = bf16(silu(float(g)) * float(u)).
+ * (row pitch ldg); h[m][n] = bf16(silu(float(g)) * float(u)), silu(g) =
+ * g / (1 + exp(-g)) in fp32 with the hardware exp2 and reciprocal
+ * approximations (within one bf16 ulp of the correctly rounded value).
  * Requirements: N % 8 == 0, ldg >= 2N, ldg % 8 == 0, ldh >= N, ldh % 8 == 0.
  */
 int clef_swiglu_bf16(const void *y_gu, int64_t M, int64_t N, int64_t ldg,
