@@ -392,6 +392,9 @@ def main():
         "wall_s_timed_region": wall,
     }
 
+    # ---- the quantizer streaming: alone on 16 records of the widest activation
+    line["quantizer"]["stream"] = quantizer_stream(cfg, acts_np, dev, stream, flush, hbm_gbs, clef, torch)
+
     # ---- the same step replayed from a CUDA graph (launch overhead removed)
     layer.capture(acts)
     g_ev = []
@@ -438,6 +441,36 @@ def proj_input_K(cfg, act):
         if p.act == act:
             return p.K
     raise KeyError(act)
+
+
+def quantizer_stream(cfg, acts_np, dev, stream, flush, hbm_gbs, clef, torch, records=16, reps=20):
+    """The workload's quantizer on `records` x M rows of its widest activation
+    (the batched size of the pages' throughput note), L2 flushed before each
+    call: its streaming bandwidth, apart from the start-up cost that dominates
+    the step's small calls."""
+    K = max(x.shape[1] for x in acts_np.values())
+    rows = records * cfg.M
+    mode = "fp8" if cfg.scheme == "fp8" else "int8_h128"
+    x = torch.empty((rows, K), dtype=torch.bfloat16, device=dev).normal_()
+    q = torch.empty((rows, K), dtype=torch.uint8 if mode == "fp8" else torch.int8, device=dev)
+    s = torch.empty((rows,), dtype=torch.float32, device=dev)
+    clef.quant_act(x, mode, q=q, scale=s)
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        clef.quant_act(x, mode, q=q, scale=s)
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize(dev)
+    t = statistics.median(a.elapsed_time(b) for a, b in ts) / 1e3
+    gbs = (3 * rows * K + 4 * rows) / t / 1e9
+    del x, q, s
+    return {"rows": rows, "K": K, "achieved": gbs, "unit": "GB/s", "peak": hbm_gbs, "frac": gbs / hbm_gbs,
+            "note": "the same kernel alone on 16 records of the widest activation, median of "
+                    f"{reps} calls with L2 flushed; the step's calls are start-up bound"}
 
 
 def weight_bytes(layer):
