@@ -449,7 +449,7 @@ def quantizer_stream(cfg, acts_np, dev, stream, flush, hbm_gbs, clef, torch, rec
     call: its streaming bandwidth, apart from the start-up cost that dominates
     the step's small calls."""
     K = max(x.shape[1] for x in acts_np.values())
-    rows = records * cfg.M
+    rows = max(cfg.M, min(records * cfg.M, 24032))   # at most 24,032 rows (under 1 GB of bf16 at K = 17408)
     mode = "fp8" if cfg.scheme == "fp8" else "int8_h128"
     x = torch.empty((rows, K), dtype=torch.bfloat16, device=dev).normal_()
     q = torch.empty((rows, K), dtype=torch.uint8 if mode == "fp8" else torch.int8, device=dev)
@@ -469,8 +469,8 @@ def quantizer_stream(cfg, acts_np, dev, stream, flush, hbm_gbs, clef, torch, rec
     gbs = (3 * rows * K + 4 * rows) / t / 1e9
     del x, q, s
     return {"rows": rows, "K": K, "achieved": gbs, "unit": "GB/s", "peak": hbm_gbs, "frac": gbs / hbm_gbs,
-            "note": "the same kernel alone on 16 records of the widest activation, median of "
-                    f"{reps} calls with L2 flushed; the step's calls are start-up bound"}
+            "note": f"the same kernel alone on {rows} rows of the widest activation, median of "
+                    f"{reps} calls with L2 flushed; the step's own calls are start-up bound"}
 
 
 def weight_bytes(layer):
