@@ -448,7 +448,7 @@ def quantizer_stream(cfg, acts_np, dev, stream, flush, hbm_gbs, clef, torch, rec
     (the batched size of the pages' throughput note), L2 flushed before each
     call: its streaming bandwidth, apart from the start-up cost that dominates
     the step's small calls."""
-    K = max(x.shape[1] for x in acts_np.values())
+    K = max(p.K for p in cfg.projections)    # the widest projection input (h for the MLP)
     rows = max(cfg.M, min(records * cfg.M, 24032))   # at most 24,032 rows (under 1 GB of bf16 at K = 17408)
     mode = "fp8" if cfg.scheme == "fp8" else "int8_h128"
     x = torch.empty((rows, K), dtype=torch.bfloat16, device=dev).normal_()
