@@ -449,7 +449,9 @@ def quantizer_stream(cfg, acts_np, dev, stream, flush, hbm_gbs, clef, torch, rec
     call: its streaming bandwidth, apart from the start-up cost that dominates
     the step's small calls."""
     K = max(p.K for p in cfg.projections)    # the widest projection input (h for the MLP)
-    rows = max(cfg.M, min(records * cfg.M, 24032))   # at most 24,032 rows (under 1 GB of bf16 at K = 17408)
+    # 16 records, but at least 512 MB of bf16 input (4x the 126 MB L2) and at most 1 GB
+    rows = max(cfg.M * records, -(-(512 << 20) // (2 * K)))
+    rows = min(rows, (1 << 30) // (2 * K))
     mode = "fp8" if cfg.scheme == "fp8" else "int8_h128"
     x = torch.empty((rows, K), dtype=torch.bfloat16, device=dev).normal_()
     q = torch.empty((rows, K), dtype=torch.uint8 if mode == "fp8" else torch.int8, device=dev)
