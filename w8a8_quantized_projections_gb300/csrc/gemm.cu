@@ -87,7 +87,9 @@ struct Cfg {
     // Read-modify-write epilogue (y += acc): a 32 x 32 fp32 transpose buffer
     // per epilogue warp, so that y is read and written in row segments.
     static constexpr bool kLoraSwi = (EPI == kEpiLoraSwiGLU);
-    static constexpr int kEpiStage = (EPI == kEpiAddBF16) ? kEpiWarps * 4096 : (kLoraSwi ? kEpiWarps * 8192 : 0);
+    // y += acc: two y tiles (BM x BN bf16) that TMA loads and stores, double-buffered
+    static constexpr int kYTile = BM * BN * 2;
+    static constexpr int kEpiStage = (EPI == kEpiAddBF16) ? 2 * kYTile : (kLoraSwi ? kEpiWarps * 8192 : 0);
     static constexpr int NSTAGE_RAWFREE = (kSmemBudget - NRAW * kRawStage - kEpiStage) / kStage;
     static constexpr int NSTAGE = kI8 ? (PAIR ? 4 : 2) : (NSTAGE_RAWFREE > 8 ? 8 : NSTAGE_RAWFREE);
     static constexpr int kChunkKBlocks = kI8 ? 16 : (1 << 30);  // 1024 K per exact chunk
@@ -131,6 +133,8 @@ struct Barriers {
     uint64_t acc_full[2], acc_empty[2];
     uint64_t drain;
     uint64_t never;      // nothing arrives here: the forced-timeout test waits on it
+    uint64_t ybar[2];    // y += acc: the y tile in buffer b has landed
+    uint64_t epi_done;   // y += acc: every epilogue warp has written the tile's y
     uint32_t tmem_slot;
     int abort;
 };
@@ -315,6 +319,20 @@ __device__ __forceinline__ void mma2_commit_local(uint64_t *bar) {
                  ::"r"(smem_u32(bar)) : "memory");
 }
 
+// TMA tile store from shared memory (bulk-group completion) and its waits.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, const void *smem_src, int32_t c0,
+                                             int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+        ::"l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // TMA tile load into this CTA's shared memory whose completion is counted on
 // a barrier that may live in the peer CTA (shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorMap *m, int32_t c0,
@@ -338,7 +356,8 @@ struct Gemm {
     struct Ctx {
         uint8_t *stage;      // NSTAGE x (A tile, B tile), 1024-aligned
         uint8_t *raw;        // NRAW x (raw A, raw B) for INT8
-        uint8_t *epi;        // kEpiStage bytes of epilogue transpose buffers
+        uint8_t *epi;        // kEpiStage bytes of epilogue buffers
+        const CUtensorMap *tmC;  // y += acc: the y (output) tensor map
         Barriers *bar;
         uint32_t tmem;       // accumulator base (the leader's allocation in pair mode)
         uint32_t rank;       // rank in the CTA pair (0 in single mode)
@@ -688,55 +707,69 @@ struct Gemm {
     // u ^ (r & 7): conflict-free both ways), after which lane l handles columns
     // 8 (l & 3) .. + 7 of rows (l >> 2) + 8 i, so every warp access to y covers
     // 64 contiguous bytes of eight rows instead of 16 bytes of 32 rows.
-    static __device__ __forceinline__ void load_y_chunk(const GemmArgs &a, int row0, int nb, int half,
-                                                        int j, uint4 (&yin)[4]) {
-        const int lane = threadIdx.x & 31;
-        const uint16_t *out = static_cast<const uint16_t *>(a.out);
-        const int n = nb * BN + chunk_col(j, half) + 8 * (lane & 3);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = row0 + (lane >> 2) + 8 * i;
-            yin[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (r < a.M && n < a.N) yin[i] = *reinterpret_cast<const uint4 *>(out + (int64_t)r * a.ldo + n);
-        }
+    // y += acc through TMA.  The CTA's y tile (its BM rows of the tile, BN
+    // columns) moves as BN / 64 boxes of 64 columns x BM rows with the 128-byte
+    // swizzle: box k of buffer b at epi + b * kYTile + k * BM * 128, row r's
+    // 16-byte unit u at r * 128 + ((u ^ (r & 7)) << 4).  Boxes wholly past the
+    // tensor's rows or columns are neither loaded nor stored.
+    static __device__ __forceinline__ int y_row0(const Ctx &c, int t) {
+        int mb, nb;
+        tile_coords(c, t, mb, nb);
+        return mb * C::kTileRows + (int)c.rank * C::BM;
     }
 
-    static __device__ __forceinline__ void finish_add_chunk(const Ctx &c, const GemmArgs &a, int row0,
-                                                            int nb, int half, int j,
-                                                            const uint32_t (&v)[32],
-                                                            const uint4 (&yin)[4]) {
-        const int lane = threadIdx.x & 31, e = (int)(threadIdx.x >> 5) - C::kEpiWarp0;
-        const uint32_t buf = smem_u32(c.epi) + (uint32_t)e * 4096u;
-        const int cg = lane & 3;
-        uint16_t *out = static_cast<uint16_t *>(a.out);
-        const int n = nb * BN + chunk_col(j, half) + 8 * cg;
-        const uint32_t rowbuf = buf + (uint32_t)lane * 128u;
+    static __device__ void y_tile_load(const Ctx &c, const GemmArgs &a, int t, int b) {
+        int mb, nb;
+        tile_coords(c, t, mb, nb);
+        const int r0 = y_row0(c, t), c0 = nb * BN;
+        uint64_t *bar = &c.bar->ybar[b];
+        int boxes = 0;
+        if (r0 < a.M)
+            for (int k = 0; k < BN / 64; ++k) boxes += (c0 + 64 * k < a.N) ? 1 : 0;
+        if (boxes == 0) {
+            mbar_arrive(bar);
+            return;
+        }
+        mbar_arrive_expect_tx(bar, (uint32_t)(boxes * C::BM * 128));
+        uint8_t *dst = c.epi + b * C::kYTile;
+        for (int k = 0; k < BN / 64; ++k)
+            if (c0 + 64 * k < a.N) tma_load_2d(dst + k * C::BM * 128, c.tmC, c0 + 64 * k, r0, bar);
+    }
+
+    static __device__ void y_tile_store(const Ctx &c, const GemmArgs &a, int t, int b) {
+        int mb, nb;
+        tile_coords(c, t, mb, nb);
+        const int r0 = y_row0(c, t), c0 = nb * BN;
+        if (r0 < a.M) {
+            const uint8_t *src = c.epi + b * C::kYTile;
+            for (int k = 0; k < BN / 64; ++k)
+                if (c0 + 64 * k < a.N) tma_store_2d(c.tmC, src + k * C::BM * 128, c0 + 64 * k, r0);
+        }
+        bulk_commit();
+    }
+
+    // This thread's row (TMEM lane) rl of the tile: y[rl][cols of chunk j] +=
+    // acc chunk v, in place in buffer b.
+    static __device__ __forceinline__ void add_chunk_smem(const Ctx &c, int b, int rl, int half, int j,
+                                                          const uint32_t (&v)[32]) {
+        const int col = chunk_col(j, half);          // 32-aligned column within the tile
+        const uint32_t box = smem_u32(c.epi) + (uint32_t)(b * C::kYTile) +
+                             (uint32_t)((col >> 6) * C::BM * 128) + (uint32_t)rl * 128u;
+        const int u0 = (col & 63) >> 3;              // first 16-byte unit of the chunk (0 or 4)
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-            sts128(rowbuf + (((uint32_t)u ^ (uint32_t)(lane & 7)) << 4), v[4 * u], v[4 * u + 1],
-                   v[4 * u + 2], v[4 * u + 3]);
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int rr = (lane >> 2) + 8 * i;
-            const uint32_t rb = buf + (uint32_t)rr * 128u;
-            const uint4 p0 = lds128(rb + (((uint32_t)(2 * cg) ^ (uint32_t)(rr & 7)) << 4));
-            const uint4 p1 = lds128(rb + (((uint32_t)(2 * cg + 1) ^ (uint32_t)(rr & 7)) << 4));
-            const uint32_t acc8[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-            const uint32_t ow[4] = {yin[i].x, yin[i].y, yin[i].z, yin[i].w};
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t addr = box + ((uint32_t)((u0 + q) ^ (rl & 7)) << 4);
+            const uint4 w = lds128(addr);
+            const uint32_t ow[4] = {w.x, w.y, w.z, w.w};
             float y[8];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                y[2 * k] = __fadd_rn(bf16_lo(ow[k]), __uint_as_float(acc8[2 * k]));
-                y[2 * k + 1] = __fadd_rn(bf16_hi(ow[k]), __uint_as_float(acc8[2 * k + 1]));
+                y[2 * k] = __fadd_rn(bf16_lo(ow[k]), __uint_as_float(v[8 * q + 2 * k]));
+                y[2 * k + 1] = __fadd_rn(bf16_hi(ow[k]), __uint_as_float(v[8 * q + 2 * k + 1]));
             }
-            const int r = row0 + rr;
-            if (r < a.M && n < a.N)
-                *reinterpret_cast<uint4 *>(out + (int64_t)r * a.ldo + n) =
-                    make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                               pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+            sts128(addr, pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                   pack_bf16x2(y[6], y[7]));
         }
-        __syncwarp();   // the buffer is rewritten by the next chunk
     }
 
     // LoRA gate/up + SwiGLU: base gate and up pieces of chunk pair p (gate
@@ -823,12 +856,26 @@ struct Gemm {
     }
 
     static __device__ void epilogue(const Ctx &c, const GemmArgs &a) {
+        int yiter = 0, yloads = 0;
+        epilogue_tiles(c, a, yiter, yloads);
+        if constexpr (EPI == kEpiAddBF16) {
+            const int e = (int)(threadIdx.x >> 5) - C::kEpiWarp0, lane = threadIdx.x & 31;
+            if (e == 0 && lane == 0) {
+                // every TMA store has finished before the CTA's shared memory goes
+                // away, and a y load still in flight (after an abort) has landed
+                bulk_wait_all();
+                for (int k = yiter; k < yloads; ++k)
+                    mbar_wait_drain(&c.bar->ybar[k & 1], (uint32_t)(k >> 1) & 1u, 200000000ull, a.status);
+            }
+        }
+    }
+
+    // yiter: y tiles finished; yloads: y tile loads issued (y += acc only).
+    static __device__ void epilogue_tiles(const Ctx &c, const GemmArgs &a, int &yiter, int &yloads) {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         const int e = warp - C::kEpiWarp0, quad = warp & 3, half = e >> 2;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         uint32_t acc = 0, aph = 0;
-        uint4 yin[(EPI == kEpiAddBF16) ? C::kChunks32 : 1][4];   // y += acc: y pieces in flight
-        (void)yin;
         for (int t = c.slot; t < c.num_tiles; t += c.nslots) {
             int mb, nb;
             tile_coords(c, t, mb, nb);
@@ -876,14 +923,25 @@ struct Gemm {
                     finish_lora_swiglu(c, a, row - lane, nb, half, p, vg, vu, yg[p], yu[p]);
                 }
             } else if constexpr (EPI == kEpiAddBF16) {
-                // y += acc: this lane's y pieces of the whole tile are requested
-                // before the accumulator is awaited (requesting the next tile's
-                // pieces during this one measured slower), then each 32-column
-                // chunk is read from TMEM and finished through the transpose buffer
-#pragma unroll
-                for (int j = 0; j < C::kChunks32; ++j) load_y_chunk(a, row - lane, nb, half, j, yin[j]);
+                // y += acc: the tile's y arrives by TMA (loaded one tile ahead into
+                // the other buffer), each thread adds its accumulator row in place,
+                // and the tile leaves by TMA once every epilogue thread is done
+                const int b = yiter & 1;
+                if (e == 0 && lane == 0) {
+                    if (yiter == 0) {
+                        y_tile_load(c, a, t, b);
+                        ++yloads;
+                    }
+                    const int tn = t + c.nslots;
+                    if (tn < c.num_tiles) {
+                        bulk_wait_read_all();   // the other buffer's last store has read it
+                        y_tile_load(c, a, tn, b ^ 1);
+                        ++yloads;
+                    }
+                }
                 if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
                 tc_fence_after();
+                if (!mbar_wait(&c.bar->ybar[b], (uint32_t)(yiter >> 1) & 1u, c.w, kSiteEpiAccFull)) return;
                 const uint32_t tbase = c.tmem + acc * BN + lane_off;
 #pragma unroll
                 for (int j = 0; j < C::kChunks32; ++j) {
@@ -894,8 +952,16 @@ struct Gemm {
                         release_acc(c, acc, lane);
                         if (++acc == (uint32_t)C::kAccBufs) { acc = 0; aph ^= 1u; }
                     }
-                    finish_add_chunk(c, a, row - lane, nb, half, j, v, yin[j]);
+                    add_chunk_smem(c, b, quad * 32 + lane, half, j, v);
                 }
+                fence_proxy_async_smem();   // the tile's smem writes, before the TMA store reads them
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c.bar->epi_done);
+                if (e == 0 && lane == 0) {
+                    if (!mbar_wait(&c.bar->epi_done, (uint32_t)yiter & 1u, c.w, kSiteEpiAccFull)) return;
+                    y_tile_store(c, a, t, b);
+                }
+                ++yiter;
             } else {
                 if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
                 tc_fence_after();
@@ -916,14 +982,15 @@ struct Gemm {
 template <int OP, int EPI, int BN, bool PAIR>
 __global__ void __launch_bounds__(Cfg<OP, EPI, BN, PAIR>::kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-            const __grid_constant__ CUtensorMap tmB2,
+            const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
             const GemmArgs args) {
     using C = Cfg<OP, EPI, BN, PAIR>;
     using G = Gemm<OP, EPI, BN, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((base + 1023u) & ~1023u) - base);
-    Barriers *bar = reinterpret_cast<Barriers *>(smem + C::NSTAGE * C::kStage + C::NRAW * C::kRawStage);
+    Barriers *bar = reinterpret_cast<Barriers *>(smem + C::NSTAGE * C::kStage + C::NRAW * C::kRawStage +
+                                                 C::kEpiStage);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = PAIR ? cluster_rank() : 0u;
 
@@ -942,6 +1009,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             mbar_init(&bar->acc_empty[s], C::kAccEmptyArrivals);
         }
         mbar_init(&bar->drain, 1);
+        mbar_init(&bar->ybar[0], 1);
+        mbar_init(&bar->ybar[1], 1);
+        mbar_init(&bar->epi_done, C::kEpiWarps);
         mbar_init(&bar->never, 1);
         bar->abort = 0;
         fence_barrier_init();
@@ -950,6 +1020,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         if (C::kLoraSwi) tma_prefetch_desc(&tmB2);
+        if (EPI == kEpiAddBF16) tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         if (PAIR) {
@@ -971,7 +1042,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     typename G::Ctx c;
     c.stage = smem;
     c.raw = smem + C::NSTAGE * C::kStage;
-    c.epi = reinterpret_cast<uint8_t *>(bar) + 512;
+    c.epi = smem + C::NSTAGE * C::kStage + C::NRAW * C::kRawStage;   // 1024-aligned
+    c.tmC = &tmC;
     c.bar = bar;
     const uint32_t own_tmem = bar->tmem_slot;
     if (PAIR) {
@@ -1061,7 +1133,13 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
     rc = internal_make_tmap(&tb, dt, B.base, B.inner, B.rows, B.pitch, box_k,
                             C::kSwiGLU ? BN / 2 : C::kBRows, sw);
     if (rc) return rc;
-    CUtensorMap tb2 = tb;
+    CUtensorMap tb2 = tb, tc = tb;
+    if (EPI == kEpiAddBF16) {   // y tiles: 64-column boxes of BM rows, 128-byte swizzle
+        rc = internal_make_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, args.out, (uint64_t)args.N,
+                                (uint64_t)args.M, (uint64_t)args.ldo * 2, 64, C::BM,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc) return rc;
+    }
     if (C::kLoraSwi) {
         if (!B2) return internal_cuda_error(cudaErrorInvalidValue, "LoRA gate/up needs the up factor");
         rc = internal_make_tmap(&tb2, dt, B2->base, B2->inner, B2->rows, B2->pitch, box_k, BN / 2, sw);
@@ -1095,10 +1173,10 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
         }
         const int pairs = tiles < max_pairs ? tiles : max_pairs;
         cfg.gridDim = dim3(2 * pairs, 1, 1);
-        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, args);
+        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, tc, args);
     } else {
         const int grid = tiles < num_sms ? tiles : num_sms;
-        kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(ta, tb, tb2, args);
+        kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(ta, tb, tb2, tc, args);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return internal_cuda_error(e, "gemm launch");
