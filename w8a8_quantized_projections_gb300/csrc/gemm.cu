@@ -82,14 +82,14 @@ struct Cfg {
     // INT8 int32 totals take most registers; the scale/bias epilogue is light
     // and more warps only crowd the producer and MMA warps' schedulers).
     // kParts warps share each TMEM lane quadrant, splitting the tile's columns.
-    static constexpr int kEpiWarps = (!kI8 && BN_ == 256 && (EPI == kEpiSwiGLU)) ? 16 : 8;
+    static constexpr int kEpiWarps = (!kI8 && BN_ == 256 && (EPI == kEpiSwiGLU || EPI == kEpiLoraSwiGLU)) ? 16 : 8;
     static constexpr int kParts = kEpiWarps / 4;
     // Read-modify-write epilogue (y += acc): a 32 x 32 fp32 transpose buffer
     // per epilogue warp, so that y is read and written in row segments.
     static constexpr bool kLoraSwi = (EPI == kEpiLoraSwiGLU);
     // y += acc: two y tiles (BM x BN bf16) that TMA loads and stores, double-buffered
     static constexpr int kYTile = BM * BN * 2;
-    static constexpr int kEpiStage = (EPI == kEpiAddBF16) ? 2 * kYTile : (kLoraSwi ? kEpiWarps * 8192 : 0);
+    static constexpr int kEpiStage = (EPI == kEpiAddBF16 || kLoraSwi) ? 2 * kYTile : 0;
     static constexpr int NSTAGE_RAWFREE = (kSmemBudget - NRAW * kRawStage - kEpiStage) / kStage;
     static constexpr int NSTAGE = kI8 ? (PAIR ? 4 : 2) : (NSTAGE_RAWFREE > 8 ? 8 : NSTAGE_RAWFREE);
     static constexpr int kChunkKBlocks = kI8 ? 16 : (1 << 30);  // 1024 K per exact chunk
@@ -357,7 +357,8 @@ struct Gemm {
         uint8_t *stage;      // NSTAGE x (A tile, B tile), 1024-aligned
         uint8_t *raw;        // NRAW x (raw A, raw B) for INT8
         uint8_t *epi;        // kEpiStage bytes of epilogue buffers
-        const CUtensorMap *tmC;  // y += acc: the y (output) tensor map
+        const CUtensorMap *tmC;  // y += acc: the y tensor map; LoRA gate/up: the base g|u map
+        const CUtensorMap *tmD;  // LoRA gate/up: the h tensor map
         Barriers *bar;
         uint32_t tmem;       // accumulator base (the leader's allocation in pair mode)
         uint32_t rank;       // rank in the CTA pair (0 in single mode)
@@ -772,78 +773,73 @@ struct Gemm {
         }
     }
 
-    // LoRA gate/up + SwiGLU: base gate and up pieces of chunk pair p (gate
-    // chunk p and up chunk p + kChunks32 / 2 of the tile) for this lane's rows
-    // (l >> 2) + 8 i and columns 8 (l & 3) .. + 7, as finish_add_chunk lays them out.
-    static __device__ __forceinline__ void load_gu_chunk(const GemmArgs &a, int row0, int nb, int half,
-                                                         int p, uint4 (&yg)[4], uint4 (&yu)[4]) {
-        const int lane = threadIdx.x & 31;
-        const uint16_t *base = static_cast<const uint16_t *>(a.aux);
-        const int n = nb * (BN / 2) + chunk_col(p, half) + 8 * (lane & 3);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = row0 + (lane >> 2) + 8 * i;
-            yg[i] = make_uint4(0u, 0u, 0u, 0u);
-            yu[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (r < a.M && n < a.N) {
-                const uint16_t *src = base + (int64_t)r * a.ld_aux + n;
-                yg[i] = *reinterpret_cast<const uint4 *>(src);
-                yu[i] = *reinterpret_cast<const uint4 *>(src + a.n_half);
-            }
+    // LoRA gate/up + SwiGLU through TMA.  Buffer b holds the tile's base gate
+    // columns (boxes 0, 1: g|u columns nb * 128 .. + 127) and up columns (boxes
+    // 2, 3: the same columns + n_half), laid out as the y tiles of y += acc; h
+    // is written over the gate boxes and stored from there.
+    static __device__ void gu_tile_load(const Ctx &c, const GemmArgs &a, int t, int b) {
+        int mb, nb;
+        tile_coords(c, t, mb, nb);
+        const int r0 = y_row0(c, t), g0 = nb * (BN / 2);
+        uint64_t *bar = &c.bar->ybar[b];
+        int boxes = 0;
+        if (r0 < a.M)
+            for (int k = 0; k < 2; ++k) boxes += (g0 + 64 * k < a.N) ? 2 : 0;
+        if (boxes == 0) {
+            mbar_arrive(bar);
+            return;
+        }
+        mbar_arrive_expect_tx(bar, (uint32_t)(boxes * C::BM * 128));
+        uint8_t *dst = c.epi + b * C::kYTile;
+        for (int k = 0; k < 2; ++k) {
+            if (g0 + 64 * k >= a.N) continue;
+            tma_load_2d(dst + k * C::BM * 128, c.tmC, g0 + 64 * k, r0, bar);
+            tma_load_2d(dst + (2 + k) * C::BM * 128, c.tmC, a.n_half + g0 + 64 * k, r0, bar);
         }
     }
 
-    // g = bf16(yg + acc_g), u = bf16(yu + acc_u), h = bf16(silu(g) * u) for one
-    // chunk pair, both accumulator chunks transposed through the warp's two
-    // 32 x 32 buffers; the same rounded operations as the LoRA add followed by
-    // the unfused SwiGLU kernel.
-    static __device__ __forceinline__ void finish_lora_swiglu(const Ctx &c, const GemmArgs &a, int row0,
-                                                              int nb, int half, int p,
-                                                              const uint32_t (&vg)[32],
-                                                              const uint32_t (&vu)[32],
-                                                              const uint4 (&yg)[4], const uint4 (&yu)[4]) {
-        const int lane = threadIdx.x & 31, e = (int)(threadIdx.x >> 5) - C::kEpiWarp0;
-        const uint32_t buf = smem_u32(c.epi) + (uint32_t)e * 8192u;
-        const int cg = lane & 3;
-        uint16_t *out = static_cast<uint16_t *>(a.out);
-        const int n = nb * (BN / 2) + chunk_col(p, half) + 8 * cg;
-        const uint32_t rowbuf = buf + (uint32_t)lane * 128u;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const uint32_t off = ((uint32_t)u ^ (uint32_t)(lane & 7)) << 4;
-            sts128(rowbuf + off, vg[4 * u], vg[4 * u + 1], vg[4 * u + 2], vg[4 * u + 3]);
-            sts128(rowbuf + 4096u + off, vu[4 * u], vu[4 * u + 1], vu[4 * u + 2], vu[4 * u + 3]);
+    static __device__ void h_tile_store(const Ctx &c, const GemmArgs &a, int t, int b) {
+        int mb, nb;
+        tile_coords(c, t, mb, nb);
+        const int r0 = y_row0(c, t), g0 = nb * (BN / 2);
+        if (r0 < a.M) {
+            const uint8_t *src = c.epi + b * C::kYTile;
+            for (int k = 0; k < 2; ++k)
+                if (g0 + 64 * k < a.N) tma_store_2d(c.tmD, src + k * C::BM * 128, g0 + 64 * k, r0);
         }
-        __syncwarp();
+        bulk_commit();
+    }
+
+    // This thread's row rl: g = bf16(yg + acc_g), u = bf16(yu + acc_u),
+    // h = bf16(silu(g) * u) for the 32 gate columns of part p (and the matching
+    // up columns), in place of the gate values in buffer b.  The same rounded
+    // operations as the LoRA add followed by the unfused SwiGLU kernel.
+    static __device__ __forceinline__ void lora_swiglu_smem(const Ctx &c, int b, int rl, int p,
+                                                            const uint32_t (&vg)[32],
+                                                            const uint32_t (&vu)[32]) {
+        const int col = 32 * p;                      // gate column within the tile's 128
+        const uint32_t base = smem_u32(c.epi) + (uint32_t)(b * C::kYTile) + (uint32_t)rl * 128u;
+        const uint32_t gbox = base + (uint32_t)((col >> 6) * C::BM * 128);
+        const uint32_t ubox = gbox + (uint32_t)(2 * C::BM * 128);
+        const int u0 = (col & 63) >> 3;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int rr = (lane >> 2) + 8 * i;
-            const uint32_t rb = buf + (uint32_t)rr * 128u;
-            const uint32_t o0 = ((uint32_t)(2 * cg) ^ (uint32_t)(rr & 7)) << 4;
-            const uint32_t o1 = ((uint32_t)(2 * cg + 1) ^ (uint32_t)(rr & 7)) << 4;
-            const uint4 g0 = lds128(rb + o0), g1 = lds128(rb + o1);
-            const uint4 u0 = lds128(rb + 4096u + o0), u1 = lds128(rb + 4096u + o1);
-            const uint32_t ag[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-            const uint32_t au[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-            const uint32_t gw[4] = {yg[i].x, yg[i].y, yg[i].z, yg[i].w};
-            const uint32_t uw[4] = {yu[i].x, yu[i].y, yu[i].z, yu[i].w};
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t off = (uint32_t)((u0 + q) ^ (rl & 7)) << 4;
+            const uint4 gw4 = lds128(gbox + off), uw4 = lds128(ubox + off);
+            const uint32_t gw[4] = {gw4.x, gw4.y, gw4.z, gw4.w}, uw[4] = {uw4.x, uw4.y, uw4.z, uw4.w};
             float h[8];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float g_lo = bf16_round(__fadd_rn(bf16_lo(gw[k]), __uint_as_float(ag[2 * k])));
-                const float g_hi = bf16_round(__fadd_rn(bf16_hi(gw[k]), __uint_as_float(ag[2 * k + 1])));
-                const float u_lo = bf16_round(__fadd_rn(bf16_lo(uw[k]), __uint_as_float(au[2 * k])));
-                const float u_hi = bf16_round(__fadd_rn(bf16_hi(uw[k]), __uint_as_float(au[2 * k + 1])));
+                const float g_lo = bf16_round(__fadd_rn(bf16_lo(gw[k]), __uint_as_float(vg[8 * q + 2 * k])));
+                const float g_hi = bf16_round(__fadd_rn(bf16_hi(gw[k]), __uint_as_float(vg[8 * q + 2 * k + 1])));
+                const float u_lo = bf16_round(__fadd_rn(bf16_lo(uw[k]), __uint_as_float(vu[8 * q + 2 * k])));
+                const float u_hi = bf16_round(__fadd_rn(bf16_hi(uw[k]), __uint_as_float(vu[8 * q + 2 * k + 1])));
                 h[2 * k] = silu_mul_fast(g_lo, u_lo);
                 h[2 * k + 1] = silu_mul_fast(g_hi, u_hi);
             }
-            const int r = row0 + rr;
-            if (r < a.M && n < a.N)
-                *reinterpret_cast<uint4 *>(out + (int64_t)r * a.ldo + n) =
-                    make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]),
-                               pack_bf16x2(h[4], h[5]), pack_bf16x2(h[6], h[7]));
+            sts128(gbox + off, pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]),
+                   pack_bf16x2(h[6], h[7]));
         }
-        __syncwarp();   // the buffers are rewritten by the next chunk pair
     }
 
     static __device__ __forceinline__ void release_acc(const Ctx &c, uint32_t acc, int lane) {
@@ -858,7 +854,7 @@ struct Gemm {
     static __device__ void epilogue(const Ctx &c, const GemmArgs &a) {
         int yiter = 0, yloads = 0;
         epilogue_tiles(c, a, yiter, yloads);
-        if constexpr (EPI == kEpiAddBF16) {
+        if constexpr (EPI == kEpiAddBF16 || C::kLoraSwi) {
             const int e = (int)(threadIdx.x >> 5) - C::kEpiWarp0, lane = threadIdx.x & 31;
             if (e == 0 && lane == 0) {
                 // every TMA store has finished before the CTA's shared memory goes
@@ -903,25 +899,40 @@ struct Gemm {
                 // the tile's exact int32 accumulators are complete
                 finish_row(a, row, row_ok, nb, half, tot);
             } else if constexpr (C::kLoraSwi) {
-                constexpr int kPairs = C::kChunks32 / 2;
-                uint4 yg[kPairs][4], yu[kPairs][4];
-#pragma unroll
-                for (int p = 0; p < kPairs; ++p) load_gu_chunk(a, row - lane, nb, half, p, yg[p], yu[p]);
+                // base g|u tiles by TMA one tile ahead, h computed in place over the
+                // gate columns, stored by TMA after a bounded epilogue rendezvous
+                const int b = yiter & 1;
+                if (e == 0 && lane == 0) {
+                    if (yiter == 0) {
+                        gu_tile_load(c, a, t, b);
+                        ++yloads;
+                    }
+                    const int tn = t + c.nslots;
+                    if (tn < c.num_tiles) {
+                        bulk_wait_read_all();
+                        gu_tile_load(c, a, tn, b ^ 1);
+                        ++yloads;
+                    }
+                }
                 if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
                 tc_fence_after();
+                if (!mbar_wait(&c.bar->ybar[b], (uint32_t)(yiter >> 1) & 1u, c.w, kSiteEpiAccFull)) return;
                 const uint32_t tbase = c.tmem + acc * BN + lane_off;
-#pragma unroll
-                for (int p = 0; p < kPairs; ++p) {
-                    uint32_t vg[32], vu[32];
-                    tmem_ld32(tbase + chunk_col(p, half), vg);
-                    tmem_ld32(tbase + chunk_col(p + kPairs, half), vu);
-                    tmem_ld_wait();
-                    if (p == kPairs - 1) {
-                        release_acc(c, acc, lane);
-                        if (++acc == (uint32_t)C::kAccBufs) { acc = 0; aph ^= 1u; }
-                    }
-                    finish_lora_swiglu(c, a, row - lane, nb, half, p, vg, vu, yg[p], yu[p]);
+                uint32_t vg[32], vu[32];
+                tmem_ld32(tbase + chunk_col(0, half), vg);
+                tmem_ld32(tbase + chunk_col(1, half), vu);
+                tmem_ld_wait();
+                release_acc(c, acc, lane);
+                if (++acc == (uint32_t)C::kAccBufs) { acc = 0; aph ^= 1u; }
+                lora_swiglu_smem(c, b, quad * 32 + lane, half, vg, vu);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c.bar->epi_done);
+                if (e == 0 && lane == 0) {
+                    if (!mbar_wait(&c.bar->epi_done, (uint32_t)yiter & 1u, c.w, kSiteEpiAccFull)) return;
+                    h_tile_store(c, a, t, b);
                 }
+                ++yiter;
             } else if constexpr (EPI == kEpiAddBF16) {
                 // y += acc: the tile's y arrives by TMA (loaded one tile ahead into
                 // the other buffer), each thread adds its accumulator row in place,
@@ -983,6 +994,7 @@ template <int OP, int EPI, int BN, bool PAIR>
 __global__ void __launch_bounds__(Cfg<OP, EPI, BN, PAIR>::kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
+            const __grid_constant__ CUtensorMap tmD,
             const GemmArgs args) {
     using C = Cfg<OP, EPI, BN, PAIR>;
     using G = Gemm<OP, EPI, BN, PAIR>;
@@ -1020,7 +1032,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         if (C::kLoraSwi) tma_prefetch_desc(&tmB2);
-        if (EPI == kEpiAddBF16) tma_prefetch_desc(&tmC);
+        if (EPI == kEpiAddBF16 || C::kLoraSwi) tma_prefetch_desc(&tmC);
+        if (C::kLoraSwi) tma_prefetch_desc(&tmD);
     }
     if (warp == 1) {
         if (PAIR) {
@@ -1044,6 +1057,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     c.raw = smem + C::NSTAGE * C::kStage;
     c.epi = smem + C::NSTAGE * C::kStage + C::NRAW * C::kRawStage;   // 1024-aligned
     c.tmC = &tmC;
+    c.tmD = &tmD;
     c.bar = bar;
     const uint32_t own_tmem = bar->tmem_slot;
     if (PAIR) {
@@ -1133,9 +1147,19 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
     rc = internal_make_tmap(&tb, dt, B.base, B.inner, B.rows, B.pitch, box_k,
                             C::kSwiGLU ? BN / 2 : C::kBRows, sw);
     if (rc) return rc;
-    CUtensorMap tb2 = tb, tc = tb;
+    CUtensorMap tb2 = tb, tc = tb, td = tb;
     if (EPI == kEpiAddBF16) {   // y tiles: 64-column boxes of BM rows, 128-byte swizzle
         rc = internal_make_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, args.out, (uint64_t)args.N,
+                                (uint64_t)args.M, (uint64_t)args.ldo * 2, 64, C::BM,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc) return rc;
+    }
+    if (C::kLoraSwi) {          // base g|u tiles in, h tiles out, the same boxes
+        rc = internal_make_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, args.aux, 2 * (uint64_t)args.n_half,
+                                (uint64_t)args.M, (uint64_t)args.ld_aux * 2, 64, C::BM,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc) return rc;
+        rc = internal_make_tmap(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, args.out, (uint64_t)args.N,
                                 (uint64_t)args.M, (uint64_t)args.ldo * 2, 64, C::BM,
                                 CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc) return rc;
@@ -1173,10 +1197,10 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
         }
         const int pairs = tiles < max_pairs ? tiles : max_pairs;
         cfg.gridDim = dim3(2 * pairs, 1, 1);
-        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, tc, args);
+        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, tc, td, args);
     } else {
         const int grid = tiles < num_sms ? tiles : num_sms;
-        kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(ta, tb, tb2, tc, args);
+        kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(ta, tb, tb2, tc, td, args);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return internal_cuda_error(e, "gemm launch");
