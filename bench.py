@@ -392,6 +392,20 @@ def main():
         "wall_s_timed_region": wall,
     }
 
+    # ---- LoRA launches (runtime adapters): bf16 tensor-core work, near the ridge
+    lora_keys = [k for k in kt if k[0] == "lora"]
+    if lora_keys:
+        l_fl, l_by = layer.lora_work()
+        l_t = sum(statistics.mean(kt[k]) for k in lora_keys)
+        line["lora"] = {"ms_per_step": 1e3 * l_t, "launches_per_step": len(lora_keys),
+                        "tflops": l_fl / l_t / 1e12, "tflops_frac": l_fl / l_t / 1e12 / bf16_peak,
+                        "gbs": l_by / l_t / 1e9, "gbs_frac": l_by / l_t / 1e9 / hbm_gbs,
+                        "flops_per_step": l_fl, "min_bytes_per_step": l_by,
+                        "note": "2 M r (K + N) flops per adapter; bytes: x once per shrink launch, "
+                                "t written and read, y read and written (gate/up: base halves "
+                                "read, h written); against the bf16 burst peak and the copy "
+                                "bandwidth"}
+
     # ---- the quantizer streaming: alone on 16 records of the widest activation
     line["quantizer"]["stream"] = quantizer_stream(cfg, acts_np, dev, stream, flush, hbm_gbs, clef, torch)
 

@@ -172,6 +172,31 @@ int clef_lora_add(const void *x, int64_t ldx, const void *A, const void *B,
                   void *t_scratch, void *y, int64_t ldy, void *stream);
 
 /*
+ * clef_lora_shrink / clef_lora_expand_add -- the two stages of clef_lora_add
+ * as separate calls [LORA], for adapters that share an input: with their A
+ * factors stacked (each zero-padded to a multiple of 64 rows) one shrink
+ * call reads x once for all of them, and each adapter's expand call reads its
+ * own column block of t (t + offset, the shared pitch ldt).  clef_lora_add is
+ * exactly clef_lora_shrink into t_scratch (ldt = r_pad) followed by
+ * clef_lora_expand_add from it.
+ * clef_lora_shrink: t[m][j] = bf16(sum_k x[m][k] * A[j][k]) for j < r_pad
+ *   (rows j >= r of A read as zeros, so those columns of t are 0).
+ *   x: bf16 [M][K], pitch ldx; A: bf16 [r][K] dense; t: bf16 [M][r_pad],
+ *   pitch ldt (only columns 0 .. r_pad - 1 written).
+ * clef_lora_expand_add: y[m][n] = bf16((float)y[m][n] + sum_{j<r} t[m][j] * B[n][j])
+ *   in place.  t: bf16, columns 0 .. r_pad - 1 read (pitch ldt; columns
+ *   r .. r_pad - 1 are multiplied by zeros); B: bf16 [N][r] dense; y: bf16
+ *   [M][N], pitch ldy.
+ * Requirements: K % 8 == 0, N % 8 == 0, r % 8 == 0, 0 < r <= 4096,
+ *   ldx >= K, ldt >= r_pad, ldy >= N, all pitches multiples of 8, every
+ *   pointer (t + offset included) 16-byte aligned.
+ */
+int clef_lora_shrink(const void *x, int64_t ldx, const void *A, int64_t M, int64_t K, int64_t r,
+                     void *t, int64_t ldt, void *stream);
+int clef_lora_expand_add(const void *t, int64_t ldt, const void *B, int64_t M, int64_t N, int64_t r,
+                         void *y, int64_t ldy, void *stream);
+
+/*
  * clef_lora_gateup_swiglu -- runtime LoRA on the gate and up projections
  * [LORA], followed by the MLP product [USAGE], in one pass over the base
  * gate/up values: with t_g = bf16(x A_gate^T) and t_u = bf16(x A_up^T) as in

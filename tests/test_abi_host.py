@@ -94,6 +94,46 @@ def test_lora_rejects_bad_arguments(bad):
     assert clef.library().clef_lora_add(x, ldx, A, B, M, K, N, r, t, y, ldy, S) == 1
 
 
+@pytest.mark.parametrize("bad", ["rank", "rank_big", "K", "ldx", "ldt", "ldt8", "null_x", "align_t"])
+def test_lora_shrink_rejects_bad_arguments(bad):
+    x, ldx, A, M, K, r, t, ldt = FAKE, 256, FAKE, 4, 256, 48, FAKE, 64
+    if bad == "rank":
+        r = 0
+    elif bad == "rank_big":
+        r = 4104
+    elif bad == "K":
+        K = 12
+    elif bad == "ldx":
+        ldx = 128
+    elif bad == "ldt":
+        ldt = 56       # below round_up(48, 64)
+    elif bad == "ldt8":
+        ldt = 68
+    elif bad == "null_x":
+        x = NUL
+    elif bad == "align_t":
+        t = ODD
+    assert clef.library().clef_lora_shrink(x, ldx, A, M, K, r, t, ldt, S) == 1
+
+
+@pytest.mark.parametrize("bad", ["rank", "N", "ldt", "ldy", "null_B", "align_y"])
+def test_lora_expand_add_rejects_bad_arguments(bad):
+    t, ldt, B, M, N, r, y, ldy = FAKE, 64, FAKE, 4, 64, 48, FAKE, 64
+    if bad == "rank":
+        r = 12
+    elif bad == "N":
+        N = 60
+    elif bad == "ldt":
+        ldt = 48       # below round_up(48, 64)
+    elif bad == "ldy":
+        ldy = 32
+    elif bad == "null_B":
+        B = NUL
+    elif bad == "align_y":
+        y = ODD
+    assert clef.library().clef_lora_expand_add(t, ldt, B, M, N, r, y, ldy, S) == 1
+
+
 def test_valid_arguments_without_gpu_report_device_error():
     """With valid arguments the call reaches the device checks; on a machine
     without a usable sm_103 GPU that is an error code, never a crash."""

@@ -346,6 +346,62 @@ def test_lora_add(orc, M, K, N, r):
     assert np.all(d2 <= tol2), f"y: worst excess {(d2 - tol2).max():.3g}"
 
 
+def stacked_adapters(name, K, ranks, Ns):
+    """Adapters on one input: their (A, B) pairs and the A factors stacked,
+    each zero-padded to a multiple of 64 rows."""
+    pairs = [S.lora_pair(0, f"{name}/{i}", r, K, N) for i, (r, N) in enumerate(zip(ranks, Ns))]
+    pads = [clef.lora_pad(r) for r in ranks]
+    A_cat = np.zeros((sum(pads), K), np.uint16)
+    o = 0
+    for (A, _), p in zip(pairs, pads):
+        A_cat[o:o + A.shape[0]] = A
+        o += p
+    return pairs, pads, A_cat
+
+
+@pytest.mark.parametrize("M,K", [(300, 1024), (1, 128), (130, 2048)])
+def test_lora_shrink_expand_equal_lora_add(M, K):
+    """One shrink over three adapters' stacked A factors, then one expand per
+    adapter from its column block of t (pitch = the stacked width), gives
+    each adapter's lora_add bytes."""
+    ranks, Ns = (256, 48, 128), (512, 264, 128)
+    x = bf16_dev(S.activation(0, f"t/lst/{M}/x", M, K))
+    pairs, pads, A_cat = stacked_adapters(f"t/lst/{M}", K, ranks, Ns)
+    t = clef.lora_shrink(x, bf16_dev(A_cat))
+    o = 0
+    for i, ((A, B), p) in enumerate(zip(pairs, pads)):
+        y0 = S.normal_bf16(0, f"t/lst/{M}/y{i}", (M, B.shape[0]))
+        y_sh, y_ref = bf16_dev(y0), bf16_dev(y0)
+        clef.lora_expand_add(t[:, o:o + p], bf16_dev(B), y_sh)
+        clef.lora_add(x, bf16_dev(A), bf16_dev(B), y_ref)
+        assert torch.equal(y_sh.view(torch.int16), y_ref.view(torch.int16)), f"adapter {i}"
+        o += p
+
+
+def test_lora_shrink_tile_shape_does_not_change_t(orc):
+    """24,032 rows: a rank-64 and a rank-192 factor stacked (256 columns) run as
+    256-wide CTA-pair tiles, the rank-64 factor alone as 64-wide single-CTA
+    tiles, and 100 of the rows alone as one 256-wide single-CTA tile; every
+    element of t is the same fp32 sum of the same products in the same k
+    order in each, so the bytes agree.  Checked against the oracle too."""
+    M, K = 24032, 128
+    pairs, pads, A_cat = stacked_adapters("t/lsw", K, (64, 192), (64, 64))
+    x_h = S.activation(0, "t/lsw/x", M, K)
+    x = bf16_dev(x_h)
+    t_cat = clef.lora_shrink(x, bf16_dev(A_cat))
+    t_one = clef.lora_shrink(x, bf16_dev(pairs[0][0]))
+    assert torch.equal(t_cat[:, :64].view(torch.int16), t_one.view(torch.int16))
+    t_few = clef.lora_shrink(x[5000:5100], bf16_dev(A_cat))
+    assert torch.equal(t_cat[5000:5100].view(torch.int16), t_few.view(torch.int16))
+    A1 = pairs[1][0]
+    rows = np.r_[0:200, M - 300:M]
+    t_ref = orc.lora_t(x_h[rows], A1)
+    t = bf16_host(t_cat[:, 64:256])[rows]
+    tol = bf16_ulp(S.bf16_bits_to_f64(t_ref)) + 2 * lora_bound(x_h[rows], A1, K)
+    d = np.abs(S.bf16_bits_to_f64(t) - S.bf16_bits_to_f64(t_ref))
+    assert np.all(d <= tol), f"t: worst excess {(d - tol).max():.3g}"
+
+
 def test_lora_rank48_equals_zero_padded_64(orc):
     """A rank-48 pair and the same pair zero-padded to 64 give identical bytes."""
     M, K, N = 64, 1024, 256

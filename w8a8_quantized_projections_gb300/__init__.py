@@ -21,7 +21,8 @@ from . import build as _build
 
 __all__ = [
     "ClefError", "library", "library_path", "quant_act", "quant_act_static", "w8a8_linear", "w8a8_gateup_swiglu",
-    "fp8_linear", "fp8_gateup_swiglu", "lora_add", "lora_add_noalloc", "lora_gateup_swiglu", "swiglu_bf16",
+    "fp8_linear", "fp8_gateup_swiglu", "lora_add", "lora_add_noalloc", "lora_shrink", "lora_expand_add",
+    "lora_gateup_swiglu", "swiglu_bf16",
     "w8a8_gemm_s32",
     "poll_status", "set_wait_limit_ns", "set_quant_staging", "ACT_MODES",
 ]
@@ -63,6 +64,8 @@ def library():
                 "clef_fp8_gateup_swiglu": [vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp],
                 "clef_lora_add": [vp, i64, vp, vp, i64, i64, i64, i64, vp, vp, i64, vp],
                 "clef_lora_add_noalloc": [vp, i64, vp, vp, i64, i64, i64, i64, vp, i64, vp],
+                "clef_lora_shrink": [vp, i64, vp, i64, i64, i64, vp, i64, vp],
+                "clef_lora_expand_add": [vp, i64, vp, i64, i64, i64, vp, i64, vp],
                 "clef_swiglu_bf16": [vp, i64, i64, i64, vp, i64, vp],
                 "clef_lora_gateup_swiglu": [vp, i64, vp, vp, vp, vp, i64, i64, i64, i64, vp, vp, i64,
                                             vp, i64, vp],
@@ -226,6 +229,42 @@ def lora_add(x, A, B, y, t_scratch=None, stream=None):
     _dense(t_scratch, "t_scratch")
     _call("clef_lora_add", _ptr(x), _rows(x, "x"), _ptr(A), _ptr(B), M, K, N, r, _ptr(t_scratch),
           _ptr(y), _rows(y, "y"), _stream(x, stream))
+    return y
+
+
+def lora_shrink(x, A, t=None, stream=None):
+    """t[:, :lora_pad(r)] = bf16(x A^T), rows of A past r read as zeros.
+    A may hold several adapters' factors stacked (each padded to 64 rows);
+    t may be a column block of a wider buffer.  Returns t."""
+    for a, n in ((x, "x"), (A, "A")):
+        _cuda(a, n, (torch.bfloat16,))
+    _dense(A, "A")
+    M, K = x.shape
+    r = A.shape[0]
+    if A.shape[1] != K:
+        raise ValueError("LoRA shapes disagree")
+    if t is None:
+        t = torch.empty((M, lora_pad(r)), dtype=torch.bfloat16, device=x.device)
+    _cuda(t, "t", (torch.bfloat16,))
+    if t.shape[0] != M or t.shape[1] < lora_pad(r):
+        raise ValueError("t must have M rows and at least round_up(r, 64) columns")
+    _call("clef_lora_shrink", _ptr(x), _rows(x, "x"), _ptr(A), M, K, r, _ptr(t), _rows(t, "t"),
+          _stream(x, stream))
+    return t
+
+
+def lora_expand_add(t, B, y, stream=None):
+    """In place: y = bf16(y + t[:, :r] B^T) with r = B.shape[1] (t's columns
+    r .. lora_pad(r) - 1 must be finite; they meet zeros).  Returns y."""
+    for a, n in ((t, "t"), (B, "B"), (y, "y")):
+        _cuda(a, n, (torch.bfloat16,))
+    _dense(B, "B")
+    M = y.shape[0]
+    N, r = B.shape
+    if t.shape[0] != M or t.shape[1] < lora_pad(r) or y.shape[1] != N:
+        raise ValueError("LoRA shapes disagree")
+    _call("clef_lora_expand_add", _ptr(t), _rows(t, "t"), _ptr(B), M, N, r, _ptr(y), _rows(y, "y"),
+          _stream(y, stream))
     return y
 
 

@@ -133,6 +133,35 @@ GemmArgs base_args(const DeviceState *d, int64_t M, int64_t N, int64_t K) {
 
 constexpr int64_t kMaxDim = (int64_t)1 << 30;
 
+// LoRA stage 1 (arguments already checked): t = bf16(x A^T), [M][r_pad] at
+// pitch ldt; rows of A past r read as zeros.  N-fastest tiles: the column
+// tiles of one row block run side by side and share its x rows in L2, so x
+// (the large operand) streams from HBM once.
+int lora_shrink_launch(DeviceState *d, const void *x, int64_t ldx, const void *A, int64_t M, int64_t K,
+                       int64_t r, void *t, int64_t ldt, cudaStream_t st) {
+    const int64_t r_pad = (r + 63) / 64 * 64;
+    GemmArgs a1 = base_args(d, M, r_pad, K);
+    a1.out = t;
+    a1.ldo = ldt;
+    a1.n_fastest = 1;
+    return launch_gemm(kOpBF16, kEpiStoreBF16, lora_shrink_width(M, r_pad, d->num_sms, 0),
+                       Operand{x, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2},
+                       Operand{A, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2}, a1, d->num_sms, st);
+}
+
+// LoRA stage 2 (arguments already checked): y = bf16(y + t B^T) over K =
+// r_pad; columns of B past r read as zeros, so t's columns r .. r_pad - 1
+// add nothing.
+int lora_expand_launch(DeviceState *d, const void *t, int64_t ldt, const void *B, int64_t M, int64_t N,
+                       int64_t r, void *y, int64_t ldy, cudaStream_t st) {
+    const int64_t r_pad = (r + 63) / 64 * 64;
+    GemmArgs a2 = base_args(d, M, N, r_pad);
+    a2.out = y;
+    a2.ldo = ldy;
+    return launch_gemm(kOpBF16, kEpiAddBF16, 256, Operand{t, (uint64_t)r_pad, (uint64_t)M, (uint64_t)ldt * 2},
+                       Operand{B, (uint64_t)r, (uint64_t)N, (uint64_t)r * 2}, a2, d->num_sms, st);
+}
+
 // Shared checks of the W8A8 GEMM entry points.  b_rows is the row count of
 // the weight operand; out_elem the output element size.
 // Returns CLEF_OK with *empty = true for a valid M = 0 call (whose row-indexed
@@ -326,22 +355,43 @@ int clef_lora_add(const void *x, int64_t ldx, const void *A, const void *B, int6
     int rc = device_state(&d);
     if (rc) return rc;
     const int64_t r_pad = (r + 63) / 64 * 64;
-    const int bn = r_pad == 64 ? 64 : (r_pad == 128 ? 128 : 256);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // stage 1: t = bf16(x A^T), [M][r_pad]; rows of A past r read as zeros
-    GemmArgs a1 = base_args(d, M, r_pad, K);
-    a1.out = t_scratch;
-    a1.ldo = r_pad;
-    rc = launch_gemm(kOpBF16, kEpiStoreBF16, bn, Operand{x, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2},
-                     Operand{A, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2}, a1, d->num_sms, st);
+    if ((rc = lora_shrink_launch(d, x, ldx, A, M, K, r, t_scratch, r_pad, st))) return rc;
+    return lora_expand_launch(d, t_scratch, r_pad, B, M, N, r, y, ldy, st);
+}
+
+int clef_lora_shrink(const void *x, int64_t ldx, const void *A, int64_t M, int64_t K, int64_t r,
+                     void *t, int64_t ldt, void *stream) {
+    if (M < 0 || M > kMaxDim) return arg_fail("M out of range");
+    if (K <= 0 || K > kMaxDim || K % 8 != 0) return arg_fail("K must be positive and a multiple of 8");
+    if (r <= 0 || r > 4096 || r % 8 != 0) return arg_fail("rank must be in (0, 4096] and a multiple of 8");
+    if (ldx < K || ldx % 8 != 0) return arg_fail("ldx must be >= K and a multiple of 8");
+    if (ldt < (r + 63) / 64 * 64 || ldt % 8 != 0)
+        return arg_fail("ldt must be >= round_up(r, 64) and a multiple of 8");
+    if (M == 0) return CLEF_OK;
+    if (!x || !A || !t) return arg_fail("null pointer");
+    if (!aligned16(x) || !aligned16(A) || !aligned16(t)) return arg_fail("pointers must be 16-byte aligned");
+    DeviceState *d = nullptr;
+    int rc = device_state(&d);
     if (rc) return rc;
-    // stage 2: y = bf16(y + t B^T); columns of B past r read as zeros
-    GemmArgs a2 = base_args(d, M, N, r_pad);
-    a2.out = y;
-    a2.ldo = ldy;
-    return launch_gemm(kOpBF16, kEpiAddBF16, 256,
-                       Operand{t_scratch, (uint64_t)r_pad, (uint64_t)M, (uint64_t)r_pad * 2},
-                       Operand{B, (uint64_t)r, (uint64_t)N, (uint64_t)r * 2}, a2, d->num_sms, st);
+    return lora_shrink_launch(d, x, ldx, A, M, K, r, t, ldt, static_cast<cudaStream_t>(stream));
+}
+
+int clef_lora_expand_add(const void *t, int64_t ldt, const void *B, int64_t M, int64_t N, int64_t r,
+                         void *y, int64_t ldy, void *stream) {
+    if (M < 0 || M > kMaxDim) return arg_fail("M out of range");
+    if (N <= 0 || N > kMaxDim || N % 8 != 0) return arg_fail("N must be positive and a multiple of 8");
+    if (r <= 0 || r > 4096 || r % 8 != 0) return arg_fail("rank must be in (0, 4096] and a multiple of 8");
+    if (ldt < (r + 63) / 64 * 64 || ldt % 8 != 0)
+        return arg_fail("ldt must be >= round_up(r, 64) and a multiple of 8");
+    if (ldy < N || ldy % 8 != 0) return arg_fail("ldy must be >= N and a multiple of 8");
+    if (M == 0) return CLEF_OK;
+    if (!t || !B || !y) return arg_fail("null pointer");
+    if (!aligned16(t) || !aligned16(B) || !aligned16(y)) return arg_fail("pointers must be 16-byte aligned");
+    DeviceState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc) return rc;
+    return lora_expand_launch(d, t, ldt, B, M, N, r, y, ldy, static_cast<cudaStream_t>(stream));
 }
 
 int clef_lora_gateup_swiglu(const void *x, int64_t ldx, const void *A_gate, const void *B_gate,
@@ -365,16 +415,19 @@ int clef_lora_gateup_swiglu(const void *x, int64_t ldx, const void *A_gate, cons
     int rc = device_state(&d);
     if (rc) return rc;
     const int64_t r_pad = (r + 63) / 64 * 64;
-    const int bn = r_pad == 64 ? 64 : (r_pad == 128 ? 128 : 256);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // stage 1: t = [bf16(x A_gate^T) | bf16(x A_up^T)], [M][2 r_pad]
-    for (int half = 0; half < 2; ++half) {
-        GemmArgs a1 = base_args(d, M, r_pad, K);
-        a1.out = static_cast<uint16_t *>(t_scratch) + half * r_pad;
+    // stage 1: t = [bf16(x A_gate^T) | bf16(x A_up^T)], [M][2 r_pad], as one
+    // GEMM whose B rows r_pad .. 2 r_pad - 1 are A_up's (x streams once)
+    {
+        GemmArgs a1 = base_args(d, M, 2 * r_pad, K);
+        a1.out = t_scratch;
         a1.ldo = 2 * r_pad;
-        rc = launch_gemm(kOpBF16, kEpiStoreBF16, bn, Operand{x, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2},
-                         Operand{half ? A_up : A_gate, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2}, a1,
-                         d->num_sms, st);
+        a1.n_fastest = 1;
+        a1.b2_row0 = (int)r_pad;
+        const Operand Au{A_up, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2};
+        rc = launch_gemm(kOpBF16, kEpiStoreBF16, lora_shrink_width(M, 2 * r_pad, d->num_sms, r_pad),
+                         Operand{x, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2},
+                         Operand{A_gate, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2}, a1, d->num_sms, st, &Au);
         if (rc) return rc;
     }
     // stage 2: one GEMM over K = 2 r_pad; gate rows see B_gate in the first

@@ -64,6 +64,12 @@ struct GemmArgs {
     const void *aux;
     int64_t ld_aux;
     int k_shift;
+    // tile order: 0 = M fastest (running CTAs share weight tiles), 1 = N
+    // fastest (running CTAs share activation row blocks: LoRA x A^T)
+    int n_fastest;
+    // kEpiStoreBF16 with two stacked B factors: rows from b2_row0 on come from
+    // the second operand (its row b2_row0 less); 0 = one B operand
+    int b2_row0;
 };
 
 // A row-major 2-D operand: rows of `inner` elements, `pitch` bytes apart.
@@ -80,6 +86,11 @@ int launch_gemm(int op, int epi, int bn, const Operand &A, const Operand &B, con
 
 // Whether a launch with this width and row count uses CTA pairs.
 bool gemm_uses_pair(int bn, int M, int num_sms);
+
+// Tile width (64, 128 or 256) for t = x A^T with N = the padded rank (256
+// uses CTA pairs when M > 128).  split > 0: the column where a second
+// stacked factor starts, which no tile may straddle.
+int lora_shrink_width(int64_t M, int64_t N, int num_sms, int64_t split);
 
 cudaError_t launch_swiglu_bf16(const uint16_t *y_gu, int64_t M, int64_t N, int64_t ldg,
                                uint16_t *h, int64_t ldh, cudaStream_t st);

@@ -364,13 +364,21 @@ struct Gemm {
         uint32_t rank;       // rank in the CTA pair (0 in single mode)
         int slot, nslots;    // tile-loop start and stride
         int num_m, num_n, num_tiles, nkb;
+        int n_fastest;       // tile order: 0 = M fastest, 1 = N fastest
         int force_timeout;   // test knob: the MMA issuer waits on a barrier nothing signals
         WaitCtx w;
     };
 
+    // M-fastest: the CTAs running at the same time share B (weight) tiles;
+    // N-fastest: they share A row blocks (x A^T, where x is the large operand).
     static __device__ __forceinline__ void tile_coords(const Ctx &c, int t, int &mb, int &nb) {
-        mb = t % c.num_m;
-        nb = t / c.num_m;
+        if (c.n_fastest) {
+            nb = t % c.num_n;
+            mb = t / c.num_n;
+        } else {
+            mb = t % c.num_m;
+            nb = t / c.num_m;
+        }
     }
 
     // Waits on barriers that receive arrivals from the peer CTA or from the
@@ -394,6 +402,15 @@ struct Gemm {
         // reads the up factor from its own map, shifted along K
         auto bmap = [&](int h) { return (C::kLoraSwi && h) ? tmB2 : tmB0; };
         auto bk = [&](int h, int k0) { return (C::kLoraSwi && h) ? k0 - a.k_shift : k0; };
+        // two stacked factors (b2_row0 > 0): B rows from b2_row0 on are rows
+        // row - b2_row0 of the second map (no stage straddles b2_row0)
+        auto bsplit = [&](const CUtensorMap *&m, int row) {
+            if (!C::kSwiGLU && a.b2_row0 > 0 && row >= a.b2_row0) {
+                m = tmB2;
+                return row - a.b2_row0;
+            }
+            return row;
+        };
         const CUtensorMap *tmB = tmB0;
         static_assert(C::NRAW <= 8 && C::NSTAGE <= 8, "fill bookkeeping");
         uint32_t s = 0, ph = 0;
@@ -427,8 +444,9 @@ struct Gemm {
                         const uint32_t lfull = leader_addr(&c.bar->full[s]);
                         if (c.rank == 0) mbar_arrive_expect_tx(&c.bar->full[s], 2 * C::kStage);
                         tma_load_2d_pair(sa, tmA, k0, row_a, lfull);
-                        tma_load_2d_pair(sb, bmap((int)c.rank), bk((int)c.rank, k0), b_row(c, a, nb, (int)c.rank),
-                                         lfull);
+                        const CUtensorMap *mb_ = bmap((int)c.rank);
+                        const int br = bsplit(mb_, b_row(c, a, nb, (int)c.rank));
+                        tma_load_2d_pair(sb, mb_, bk((int)c.rank, k0), br, lfull);
                     } else {
                         uint64_t *full = &c.bar->full[s];
                         mbar_arrive_expect_tx(full, C::kStage);
@@ -437,7 +455,9 @@ struct Gemm {
                             tma_load_2d(sb, bmap(0), bk(0, k0), b_row(c, a, nb, 0), full);
                             tma_load_2d(sb + (BN / 2) * 128, bmap(1), bk(1, k0), b_row(c, a, nb, 1), full);
                         } else {
-                            tma_load_2d(sb, tmB, k0, b_row(c, a, nb, 0), full);
+                            const CUtensorMap *mb_ = tmB;
+                            const int br = bsplit(mb_, b_row(c, a, nb, 0));
+                            tma_load_2d(sb, mb_, k0, br, full);
                         }
                     }
                 }
@@ -1078,6 +1098,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     c.num_n = (args.N + C::kOutColsPerTile - 1) / C::kOutColsPerTile;
     c.num_tiles = c.num_m * c.num_n;
     c.nkb = C::kI8 ? (args.K + 63) / 64 : (args.K + C::BK - 1) / C::BK;
+    c.n_fastest = args.n_fastest;
     c.force_timeout = args.force_timeout;
     c.w.limit_ns = args.wait_limit_ns;
     c.w.abort = &bar->abort;
@@ -1168,6 +1189,11 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
         if (!B2) return internal_cuda_error(cudaErrorInvalidValue, "LoRA gate/up needs the up factor");
         rc = internal_make_tmap(&tb2, dt, B2->base, B2->inner, B2->rows, B2->pitch, box_k, BN / 2, sw);
         if (rc) return rc;
+    } else if (args.b2_row0 > 0) {   // a second factor stacked below the first
+        if (!B2 || C::kSwiGLU || args.b2_row0 % C::kBRows != 0)
+            return internal_cuda_error(cudaErrorInvalidValue, "stacked B operands");
+        rc = internal_make_tmap(&tb2, dt, B2->base, B2->inner, B2->rows, B2->pitch, box_k, C::kBRows, sw);
+        if (rc) return rc;
     }
     auto kern = gemm_kernel<OP, EPI, BN, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -1211,6 +1237,18 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
 
 bool gemm_uses_pair(int bn, int M, int num_sms) { return bn == 256 && M > 128 && num_sms >= 2; }
 
+int lora_shrink_width(int64_t M, int64_t N, int num_sms, int64_t split) {
+    // Wide CTA-pair tiles whenever they apply, although narrower tiles fill
+    // the last wave better: on 24,032 x 5120 -> 256, 256-wide pair tiles took
+    // 91 us against 94 us for 128-wide and 130 us for 64-wide single tiles,
+    // which stage the same x rows in two or four SMs and read more operand
+    // bytes per product.  Small ranks keep tiles no wider than the rank.
+    if (N > 128 && gemm_uses_pair(256, (int)M, num_sms) && (split == 0 || split % 128 == 0)) return 256;
+    int bn = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
+    while (split > 0 && bn > 64 && split % bn != 0) bn /= 2;   // no tile straddles the split
+    return bn;
+}
+
 int launch_gemm(int op, int epi, int bn, const Operand &A, const Operand &B, const GemmArgs &args,
                 int num_sms, cudaStream_t st, const Operand *B2) {
     const bool pair = gemm_uses_pair(bn, args.M, num_sms);
@@ -1226,9 +1264,11 @@ int launch_gemm(int op, int epi, int bn, const Operand &A, const Operand &B, con
         if (epi == kEpiSwiGLU) CLEF_GEMM(kOpF8, kEpiSwiGLU, 256);
     } else if (op == kOpBF16) {
         if (epi == kEpiStoreBF16) {
-            if (bn == 64) return launch_one<kOpBF16, kEpiStoreBF16, 64, false>(A, B, args, num_sms, st);
-            if (bn == 128) return launch_one<kOpBF16, kEpiStoreBF16, 128, false>(A, B, args, num_sms, st);
-            if (bn == 256) CLEF_GEMM(kOpBF16, kEpiStoreBF16, 256);
+            if (bn == 64) return launch_one<kOpBF16, kEpiStoreBF16, 64, false>(A, B, args, num_sms, st, B2);
+            if (bn == 128) return launch_one<kOpBF16, kEpiStoreBF16, 128, false>(A, B, args, num_sms, st, B2);
+            if (bn == 256)
+                return pair ? launch_one<kOpBF16, kEpiStoreBF16, 256, true>(A, B, args, num_sms, st, B2)
+                            : launch_one<kOpBF16, kEpiStoreBF16, 256, false>(A, B, args, num_sms, st, B2);
         } else if (epi == kEpiAddBF16 && bn == 256) {
             CLEF_GEMM(kOpBF16, kEpiAddBF16, 256);
         } else if (epi == kEpiLoraSwiGLU && bn == 256) {

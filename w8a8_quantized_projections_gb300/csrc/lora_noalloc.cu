@@ -108,7 +108,7 @@ extern "C" int clef_lora_add_noalloc(const void *x, int64_t ldx, const void *A, 
     uint16_t *t = nullptr;
     if ((rc = scratch_address(&t))) return rc;
 
-    const int bn = r_pad == 64 ? 64 : (r_pad == 128 ? 128 : 256);
+    const int bn = lora_shrink_width(M, r_pad, num_sms, 0);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     GemmArgs a1 = {};
     a1.M = (int)M;
@@ -116,6 +116,7 @@ extern "C" int clef_lora_add_noalloc(const void *x, int64_t ldx, const void *A, 
     a1.K = (int)K;
     a1.out = t;
     a1.ldo = r_pad;
+    a1.n_fastest = 1;
     a1.status = status;
     a1.wait_limit_ns = 1000000000ull;
     rc = launch_gemm(kOpBF16, kEpiStoreBF16, bn, Operand{x, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2},

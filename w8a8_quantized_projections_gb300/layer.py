@@ -22,7 +22,11 @@ projection one GEMM call (gate/up with the fused SwiGLU epilogue).  With
 runtime LoRA pairs, every adapted projection adds ``bf16(x A^T) B^T`` after
 its GEMM; gate/up is then run as a packed linear (bf16 gate and up), and one
 call adds the gate and up adapters to their halves and forms h (the same
-rounded operations as two LoRA adds followed by the unfused SwiGLU).
+rounded operations as two LoRA adds followed by the unfused SwiGLU).  The
+adapters of a packed group share their input, so their A factors are stacked
+at set-up (each padded to 64 rows) and one shrink call computes every
+adapter's t from one pass over x; each adapter's expand call then reads its
+own column block of t (the same bytes as a separate LoRA add per adapter).
 """
 from __future__ import annotations
 
@@ -30,8 +34,8 @@ from typing import Dict, Optional, Tuple
 
 import torch
 
-from . import (fp8_gateup_swiglu, fp8_linear, lora_add, lora_gateup_swiglu, lora_pad, quant_act,
-               w8a8_gateup_swiglu, w8a8_linear)
+from . import (fp8_gateup_swiglu, fp8_linear, lora_add, lora_expand_add, lora_gateup_swiglu, lora_pad,
+               lora_shrink, quant_act, w8a8_gateup_swiglu, w8a8_linear)
 
 
 class QuantizedLayer:
@@ -98,10 +102,31 @@ class QuantizedLayer:
             if p.chained:
                 self.q[p.act] = (torch.empty((M, p.K), dtype=code, device=device),
                                  torch.empty((M,), dtype=torch.float32, device=device))
-        # one dense LoRA scratch per width in use: [M][r_pad], and [M][2 r_pad]
-        # for the gate/up pair
+        # LoRA scratch: per packed group with adapters, the stacked A factors
+        # and a [M][sum r_pad] t whose column blocks belong to its adapters;
+        # one dense [M][r_pad] (or [M][2 r_pad] for the gate/up pair) per width
+        # for the others
         self.t = {}
+        self.lora_groups = {}   # group index -> (stacked A, t, [(name, col0, r_pad)])
+        for gi, g in enumerate(self.groups):
+            members = [p for p in g if p.name in self.lora] if len(g) > 1 else []
+            if not members:
+                continue
+            K = g[0].K
+            pads = [lora_pad(self.lora[p.name][0].shape[0]) for p in members]
+            A_cat = torch.zeros((sum(pads), K), dtype=torch.bfloat16, device=device)
+            blocks, c0 = [], 0
+            for p, r_pad in zip(members, pads):
+                A = self.lora[p.name][0]
+                A_cat[c0:c0 + A.shape[0]] = A
+                blocks.append((p.name, c0, r_pad))
+                c0 += r_pad
+            t = torch.empty((M, c0), dtype=torch.bfloat16, device=device)
+            self.lora_groups[gi] = (A_cat, t, blocks)
+        grouped = {name for _, _, blocks in self.lora_groups.values() for name, _, _ in blocks}
         for key, (A, _) in self.lora.items():
+            if key in grouped:
+                continue
             width = lora_pad(A.shape[0]) * (2 if key.endswith("/gate") or key.endswith("/up") else 1)
             if width not in self.t:
                 self.t[width] = torch.empty((M, width), dtype=torch.bfloat16, device=device)
@@ -114,12 +139,45 @@ class QuantizedLayer:
             out.append((_unit_name(g), rows, g[0].K, 2 * self.M * rows * g[0].K))
         return out
 
+    def lora_work(self) -> Tuple[int, int]:
+        """Per step, the LoRA launches' (flops, minimum HBM bytes): 2 M r (K + N)
+        flops per adapter; x read once per shrink launch, t written and read
+        back, y read and written (gate/up: both base halves read, h written)."""
+        M, fl, by = self.M, 0, 0
+        for gi, g in enumerate(self.groups):
+            if gi in self.lora_groups:
+                _, t, blocks = self.lora_groups[gi]
+                by += M * g[0].K * 2 + 2 * M * t.shape[1] * 2
+                for name, _, _ in blocks:
+                    N, r = self.lora[name][1].shape
+                    fl += 2 * M * r * (g[0].K + N)
+                    by += 2 * M * N * 2
+                continue
+            for p in g:
+                if p.kind == "gateup" and p.name + "/gate" in self.lora:
+                    for half in ("/gate", "/up"):
+                        A, B = self.lora[p.name + half]
+                        fl += 2 * M * A.shape[0] * (p.K + B.shape[0])
+                    r_pad = lora_pad(self.lora[p.name + "/gate"][0].shape[0])
+                    by += M * p.K * 2 + 2 * M * 2 * r_pad * 2 + M * 2 * p.N * 2 + M * p.N * 2
+                elif p.name in self.lora:
+                    A, B = self.lora[p.name]
+                    fl += 2 * M * A.shape[0] * (p.K + B.shape[0])
+                    by += M * p.K * 2 + 2 * M * lora_pad(A.shape[0]) * 2 + 2 * M * B.shape[0] * 2
+        return fl, by
+
     def launches_per_step(self) -> int:
         n = len(self.cfg.activations()) + len(self.groups)
         for p in self.cfg.projections:
             n += 1 if p.chained else 0
-            if self.lora:
-                n += 3 if p.kind == "gateup" else 2   # gate/up: two x A^T, one fused add + SwiGLU
+        if self.lora:
+            for gi, g in enumerate(self.groups):
+                if gi in self.lora_groups:      # one shared x A^T, one expand per adapter
+                    n += 1 + len(self.lora_groups[gi][2])
+                elif g[0].kind == "gateup":     # stacked x A^T, one fused add + SwiGLU
+                    n += 2
+                else:
+                    n += sum(2 for p in g if p.name in self.lora)
         return n
 
     def step(self, acts: Dict[str, torch.Tensor], events=None,
@@ -149,11 +207,13 @@ class QuantizedLayer:
                 qx, sx = self.q[g[0].act]
                 with ev("gemm", _unit_name(g)):
                     lin(qx, sx, qw, sw, b, y=self.unit_out[gi])
-                for p in g:
-                    if self.lora and p.name in self.lora:
-                        A, B = self.lora[p.name]
-                        with ev("lora", p.name):
-                            lora_add(acts[p.act], A, B, self.out[p.name], t_scratch=self._t(A))
+                if gi in self.lora_groups:
+                    A_cat, t, blocks = self.lora_groups[gi]
+                    with ev("lora", _unit_name(g) + ":xA"):
+                        lora_shrink(acts[g[0].act], A_cat, t=t)
+                    for name, c0, r_pad in blocks:
+                        with ev("lora", name):
+                            lora_expand_add(t[:, c0:c0 + r_pad], self.lora[name][1], self.out[name])
                 continue
             p = g[0]
             qw, sw, b = self.unit_w[gi]
