@@ -134,6 +134,20 @@ def test_lora_expand_add_rejects_bad_arguments(bad):
     assert clef.library().clef_lora_expand_add(t, ldt, B, M, N, r, y, ldy, S) == 1
 
 
+@pytest.mark.parametrize("bad", ["align", "small"])
+def test_bind_workspace_rejects_bad_arguments(bad):
+    ws, n = FAKE, 1 << 26
+    if bad == "align":
+        ws = ODD
+    else:
+        n = 1024           # below the counter block
+    assert clef.library().clef_bind_workspace(S, ws, n) == 1
+
+
+def test_workspace_bytes_rejects_null():
+    assert clef.library().clef_gemm_workspace_bytes(NUL) == 1
+
+
 def test_valid_arguments_without_gpu_report_device_error():
     """With valid arguments the call reaches the device checks; on a machine
     without a usable sm_103 GPU that is an error code, never a crash."""

@@ -1,0 +1,113 @@
+"""INT8 stream-K: with a workspace bound to the stream, GEMMs whose last wave
+of whole tiles would leave CTA pairs idle deal the tiles' 1024-deep K chunks
+evenly to the pairs, and the pieces of a tile meet as exact int32 partial sums.
+Every output must equal the unsplit launch's bytes (and the oracle's)."""
+import numpy as np
+import pytest
+import torch
+
+import w8a8_quantized_projections_gb300 as clef
+from gpu_util import dev, host, par_rows
+
+pytestmark = pytest.mark.gpu
+
+COUNTER_BYTES = 4096 * 2 * 8 * 4
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+
+
+def codes(seed, rows, K):
+    rng = np.random.default_rng(seed)
+    return rng.integers(-127, 128, (rows, K)).astype(np.int8)
+
+
+def bound_workspace(stream=None):
+    ws = torch.zeros(clef.gemm_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    clef.bind_workspace(ws, stream)
+    return ws
+
+
+# (M, N, K): 120 tiles on 76 pairs; 48 tiles (one thin wave); K with a
+# one-k-block last chunk; two chunks per tile; a full wave (no split)
+SHAPES = [(1502, 5120, 17408), (300, 6144, 5120), (600, 2048, 17472), (257, 512, 1088),
+          (1024, 4864, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_stream_k_s32_equals_unsplit_and_oracle(orc, M, N, K):
+    qx, qw = codes(M + N, M, K), codes(K + 1, N, K)
+    qx_d, qw_d = dev(qx), dev(qw)
+    plain = clef.w8a8_gemm_s32(qx_d, qw_d)
+    ws = bound_workspace()
+    try:
+        for _ in range(3):   # repeated launches reuse the zeroed counters
+            split = clef.w8a8_gemm_s32(qx_d, qw_d)
+            assert torch.equal(split, plain)
+        torch.cuda.synchronize()
+        assert int(ws[:COUNTER_BYTES].count_nonzero()) == 0, "counters must be zero between launches"
+    finally:
+        clef.bind_workspace(None)
+    rows = np.unique(np.r_[0:3, M // 2, M - 3:M])
+    ref = par_rows(lambda a, b: orc.int8_gemm_acc(qx[rows][a:b], qw), len(rows))
+    assert np.array_equal(host(plain)[rows], ref)
+
+
+def test_stream_k_scale_bias_equals_unsplit(orc):
+    """The scale/bias epilogue on the 1,502-token down projection shape."""
+    M, N, K = 1502, 5120, 17408
+    qx, qw = codes(3, M, K), codes(4, N, K)
+    rng = np.random.default_rng(5)
+    sx = torch.tensor(rng.random(M, dtype=np.float32) * 1e-3, device="cuda")
+    sw = torch.tensor(rng.random(N, dtype=np.float32) * 1e-3, device="cuda")
+    b = torch.tensor(rng.standard_normal(N, dtype=np.float32), device="cuda").to(torch.bfloat16)
+    qx_d, qw_d = dev(qx), dev(qw)
+    plain = clef.w8a8_linear(qx_d, sx, qw_d, sw, b)
+    ws = bound_workspace()
+    try:
+        split = clef.w8a8_linear(qx_d, sx, qw_d, sw, b)
+    finally:
+        clef.bind_workspace(None)
+    assert torch.equal(split.view(torch.int16), plain.view(torch.int16))
+    del ws
+
+
+def test_stream_k_two_streams_own_workspaces():
+    """Launches on two streams that overlap, each stream with its own
+    workspace, give the unsplit bytes on both."""
+    M, N, K = 1502, 5120, 17408
+    qx_d, qw_d = dev(codes(6, M, K)), dev(codes(7, N, K))
+    plain = clef.w8a8_gemm_s32(qx_d, qw_d)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    ws1, ws2 = bound_workspace(s1), bound_workspace(s2)
+    try:
+        outs = []
+        torch.cuda.synchronize()
+        for s in (s1, s2, s1, s2):
+            with torch.cuda.stream(s):
+                outs.append(clef.w8a8_gemm_s32(qx_d, qw_d))
+        torch.cuda.synchronize()
+        for o in outs:
+            assert torch.equal(o, plain)
+    finally:
+        clef.bind_workspace(None, s1)
+        clef.bind_workspace(None, s2)
+    del ws1, ws2
+
+
+def test_unbound_stream_never_splits_and_unbind_works():
+    """A workspace bound to another stream is not used; after unbinding,
+    launches run unsplit (their counters stay untouched)."""
+    M, N, K = 300, 6144, 5120
+    qx_d, qw_d = dev(codes(8, M, K)), dev(codes(9, N, K))
+    other = torch.cuda.Stream()
+    ws = bound_workspace(other)
+    ws[:COUNTER_BYTES].fill_(0)
+    ref = clef.w8a8_gemm_s32(qx_d, qw_d)
+    clef.bind_workspace(None, other)
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero()) == 0, "a workspace bound to another stream was written"
+    assert torch.equal(clef.w8a8_gemm_s32(qx_d, qw_d), ref)

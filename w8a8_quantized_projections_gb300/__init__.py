@@ -24,7 +24,8 @@ __all__ = [
     "fp8_linear", "fp8_gateup_swiglu", "lora_add", "lora_add_noalloc", "lora_shrink", "lora_expand_add",
     "lora_gateup_swiglu", "swiglu_bf16",
     "w8a8_gemm_s32",
-    "poll_status", "set_wait_limit_ns", "set_quant_staging", "ACT_MODES",
+    "poll_status", "set_wait_limit_ns", "set_quant_staging", "ACT_MODES", "gemm_workspace_bytes",
+    "bind_workspace",
 ]
 
 ACT_MODES = {"int8_h128": 0, "fp8": 1, "fp8_h128": 2}
@@ -65,6 +66,8 @@ def library():
                 "clef_lora_add": [vp, i64, vp, vp, i64, i64, i64, i64, vp, vp, i64, vp],
                 "clef_lora_add_noalloc": [vp, i64, vp, vp, i64, i64, i64, i64, vp, i64, vp],
                 "clef_lora_shrink": [vp, i64, vp, i64, i64, i64, vp, i64, vp],
+                "clef_gemm_workspace_bytes": [vp],
+                "clef_bind_workspace": [vp, vp, i64],
                 "clef_lora_expand_add": [vp, i64, vp, i64, i64, i64, vp, i64, vp],
                 "clef_swiglu_bf16": [vp, i64, i64, i64, vp, i64, vp],
                 "clef_lora_gateup_swiglu": [vp, i64, vp, vp, vp, vp, i64, i64, i64, i64, vp, vp, i64,
@@ -208,6 +211,33 @@ def w8a8_gemm_s32(qx, qw, acc=None, stream=None):
     _call("clef_w8a8_gemm_s32", _ptr(qx), _ptr(qw), M, N, K, _ptr(acc), _rows(acc, "acc"),
           _stream(qx, stream))
     return acc
+
+
+_BOUND = {}
+
+
+def gemm_workspace_bytes() -> int:
+    """Bytes of the stream-K workspace on the current device."""
+    n = C.c_int64(0)
+    _call("clef_gemm_workspace_bytes", C.c_void_p(C.addressof(n)))
+    return n.value
+
+
+def bind_workspace(ws, stream=None):
+    """Bind a zero-filled uint8 CUDA buffer of gemm_workspace_bytes() to
+    `stream` (default: the current stream) so that INT8 GEMMs launched on it
+    may split tiles across SMs; ws = None unbinds.  The buffer is kept alive
+    while bound."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    key = (torch.cuda.current_device(), s.cuda_stream)
+    if ws is None:
+        _call("clef_bind_workspace", C.c_void_p(s.cuda_stream), C.c_void_p(None), 0)
+        _BOUND.pop(key, None)
+        return
+    _cuda(ws, "ws", (torch.uint8,))
+    _dense(ws, "ws")
+    _call("clef_bind_workspace", C.c_void_p(s.cuda_stream), _ptr(ws), ws.numel())
+    _BOUND[key] = ws
 
 
 def lora_pad(r: int) -> int:

@@ -25,12 +25,24 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
     bool ready = false;
     bool supported = false;
+    int index = 0;
     int num_sms = 0;
     unsigned int *status = nullptr;  // device address of g_status on this device
 };
 
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
+
+// Caller-owned stream-K workspaces bound to (device, stream); guarded by g_mu.
+struct WsBinding {
+    int dev;
+    void *stream;
+    void *ptr;
+    int64_t bytes;
+};
+constexpr size_t kMaxBindings = 256;
+WsBinding g_ws[kMaxBindings];
+size_t g_ws_count = 0;
 std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
 std::atomic<int> g_force_timeout{0};
 std::atomic<int> g_quant_staging{1};
@@ -60,6 +72,7 @@ int device_state(DeviceState **out) {
     if (dev < 0 || dev >= kMaxDevices) return arg_fail("device index");
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState &d = g_dev[dev];
+    d.index = dev;
     if (!d.ready) {
         int major = 0, minor = 0;
         if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
@@ -158,7 +171,7 @@ int lora_expand_launch(DeviceState *d, const void *t, int64_t ldt, const void *B
     GemmArgs a2 = base_args(d, M, N, r_pad);
     a2.out = y;
     a2.ldo = ldy;
-    return launch_gemm(kOpBF16, kEpiAddBF16, 256, Operand{t, (uint64_t)r_pad, (uint64_t)M, (uint64_t)ldt * 2},
+    return launch_gemm(kOpBF16, kEpiAddBF16, 128, Operand{t, (uint64_t)r_pad, (uint64_t)M, (uint64_t)ldt * 2},
                        Operand{B, (uint64_t)r, (uint64_t)N, (uint64_t)r * 2}, a2, d->num_sms, st);
 }
 
@@ -204,6 +217,16 @@ int run_w8a8(int op, int epi, const void *qx, const float *sx, const void *qw, c
     a.bias = static_cast<const uint16_t *>(bias);
     a.out = out;
     a.ldo = ldo;
+    if (op == kOpI8) {   // a workspace bound to this stream lets tiles be split across SMs
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (size_t i = 0; i < g_ws_count; ++i)
+            if (g_ws[i].dev == d->index && g_ws[i].stream == stream) {
+                a.sk_cnt = static_cast<int *>(g_ws[i].ptr);
+                a.sk_ws = reinterpret_cast<int4 *>(static_cast<char *>(g_ws[i].ptr) + kSkCounterBytes);
+                a.sk_ws_bytes = g_ws[i].bytes - kSkCounterBytes;
+                break;
+            }
+    }
     return launch_gemm(op, epi, 256, A, B, a, d->num_sms, static_cast<cudaStream_t>(stream));
 }
 
@@ -463,6 +486,36 @@ int clef_swiglu_bf16(const void *y_gu, int64_t M, int64_t N, int64_t ldg, void *
     cudaError_t e = launch_swiglu_bf16(static_cast<const uint16_t *>(y_gu), M, N, ldg,
                                        static_cast<uint16_t *>(h), ldh, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CLEF_OK : cuda_fail(e, "swiglu launch");
+}
+
+int clef_gemm_workspace_bytes(int64_t *bytes) {
+    if (!bytes) return arg_fail("null pointer");
+    DeviceState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc) return rc;
+    *bytes = kSkCounterBytes + (int64_t)(d->num_sms / 2) * kSkBytesPerPair;
+    return CLEF_OK;
+}
+
+int clef_bind_workspace(void *stream, void *ws, int64_t bytes) {
+    if (ws && !aligned16(ws)) return arg_fail("workspace must be 16-byte aligned");
+    if (ws && bytes < kSkCounterBytes) return arg_fail("workspace smaller than its counter block");
+    DeviceState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc) return rc;
+    std::lock_guard<std::mutex> lk(g_mu);
+    size_t i = 0;
+    while (i < g_ws_count && !(g_ws[i].dev == d->index && g_ws[i].stream == stream)) ++i;
+    if (!ws) {   // unbind
+        if (i < g_ws_count) g_ws[i] = g_ws[--g_ws_count];
+        return CLEF_OK;
+    }
+    if (i == g_ws_count) {
+        if (g_ws_count == kMaxBindings) return arg_fail("too many bound workspaces (256)");
+        ++g_ws_count;
+    }
+    g_ws[i] = WsBinding{d->index, stream, ws, bytes};
+    return CLEF_OK;
 }
 
 int clef_poll_status(void) {

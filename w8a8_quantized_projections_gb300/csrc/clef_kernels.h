@@ -70,7 +70,21 @@ struct GemmArgs {
     // kEpiStoreBF16 with two stacked B factors: rows from b2_row0 on come from
     // the second operand (its row b2_row0 less); 0 = one B operand
     int b2_row0;
+    // INT8 stream-K (sk = 1): the tiles' 1024-K chunks are shared evenly by
+    // the CTA pairs; pieces of a tile meet in the workspace: sk_cnt holds
+    // kSkMaxTiles x 2 x 8 arrival counters (zero between launches), sk_ws the
+    // int32 partial sums.  sk_ws_bytes: the partial region's size.
+    int sk;
+    int *sk_cnt;
+    int4 *sk_ws;
+    int64_t sk_ws_bytes;
 };
+
+// Stream-K workspace: counters for up to kSkMaxTiles tiles, then per CTA pair
+// two pieces x two CTAs x eight epilogue warps x 16 KB of int32 sums.
+constexpr int kSkMaxTiles = 4096;
+constexpr int64_t kSkCounterBytes = (int64_t)kSkMaxTiles * 2 * 8 * 4;
+constexpr int64_t kSkBytesPerPair = 2 * 2 * 8 * 16384;
 
 // A row-major 2-D operand: rows of `inner` elements, `pitch` bytes apart.
 struct Operand {

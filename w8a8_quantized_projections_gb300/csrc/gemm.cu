@@ -87,9 +87,12 @@ struct Cfg {
     // Read-modify-write epilogue (y += acc): a 32 x 32 fp32 transpose buffer
     // per epilogue warp, so that y is read and written in row segments.
     static constexpr bool kLoraSwi = (EPI == kEpiLoraSwiGLU);
-    // y += acc: two y tiles (BM x BN bf16) that TMA loads and stores, double-buffered
+    // y += acc: a ring of kYBufs y tiles (BM x BN bf16) that TMA loads
+    // kYBufs - 1 tiles ahead and stores; 128-wide tiles keep 4 (three loads
+    // in flight, 96 KB, against one 64 KB load for the 256-wide pair tiles)
     static constexpr int kYTile = BM * BN * 2;
-    static constexpr int kEpiStage = (EPI == kEpiAddBF16 || kLoraSwi) ? 2 * kYTile : 0;
+    static constexpr int kYBufs = (EPI == kEpiAddBF16 && BN == 128) ? 4 : 2;
+    static constexpr int kEpiStage = (EPI == kEpiAddBF16 || kLoraSwi) ? kYBufs * kYTile : 0;
     static constexpr int NSTAGE_RAWFREE = (kSmemBudget - NRAW * kRawStage - kEpiStage) / kStage;
     static constexpr int NSTAGE = kI8 ? (PAIR ? 4 : 2) : (NSTAGE_RAWFREE > 8 ? 8 : NSTAGE_RAWFREE);
     static constexpr int kChunkKBlocks = kI8 ? 16 : (1 << 30);  // 1024 K per exact chunk
@@ -102,6 +105,9 @@ struct Cfg {
     static constexpr int kColsPerThread = BN / kParts;     // columns one epilogue thread owns
     static constexpr int kChunks32 = kColsPerThread / 32;
     static constexpr bool kSwiGLU = (EPI == kEpiSwiGLU || EPI == kEpiLoraSwiGLU);  // gate|up tile
+    // INT8 stream-K is compiled into the pair kernels of the scale/bias and
+    // int32 epilogues (with the SwiGLU epilogue the combine step spills)
+    static constexpr bool kStreamK = kI8 && PAIR && !kSwiGLU;
     static constexpr int kOutColsPerTile = kSwiGLU ? BN / 2 : BN;
     // full[s]: TMA (native) or the local converter warps (INT8); in pair mode
     // the leader's barrier also counts the peer's forwarded readiness.
@@ -133,7 +139,7 @@ struct Barriers {
     uint64_t acc_full[2], acc_empty[2];
     uint64_t drain;
     uint64_t never;      // nothing arrives here: the forced-timeout test waits on it
-    uint64_t ybar[2];    // y += acc: the y tile in buffer b has landed
+    uint64_t ybar[4];    // y += acc: the y tile in buffer b has landed
     uint64_t epi_done;   // y += acc: every epilogue warp has written the tile's y
     uint32_t tmem_slot;
     int abort;
@@ -365,6 +371,7 @@ struct Gemm {
         int slot, nslots;    // tile-loop start and stride
         int num_m, num_n, num_tiles, nkb;
         int n_fastest;       // tile order: 0 = M fastest, 1 = N fastest
+        int sk;              // INT8 stream-K: the slots share the tiles' 1024-K chunks evenly
         int force_timeout;   // test knob: the MMA issuer waits on a barrier nothing signals
         WaitCtx w;
     };
@@ -379,6 +386,57 @@ struct Gemm {
             mb = t % c.num_m;
             nb = t / c.num_m;
         }
+    }
+
+    // A CTA's work is a list of segments: a tile and a range of its k-blocks.
+    // Classic schedule: whole tiles slot, slot + nslots, ...  Stream-K: the
+    // num_tiles * cpt chunks in tile order, slot p owning chunks [b(p),
+    // b(p + 1)) with b(p) = floor(p * num_tiles * cpt / nslots), so a slot's
+    // run may begin and end inside tiles.  part: -1 for a whole tile, 0 for a
+    // piece that is the slot's first segment, 1 for a later piece (a slot has
+    // at most two pieces: its first and its last segment).
+    struct Seg {
+        int tile, kb0, kb1, part;
+    };
+    struct SegIt {
+        int cur, end, first;
+    };
+    static __device__ __forceinline__ int chunks_per_tile(const Ctx &c) {
+        return (c.nkb + C::kChunkKBlocks - 1) / C::kChunkKBlocks;
+    }
+    static __device__ __forceinline__ int sk_bound(const Ctx &c, int p) {
+        return (int)((int64_t)p * c.num_tiles * chunks_per_tile(c) / c.nslots);
+    }
+    static __device__ __forceinline__ int sk_owner(const Ctx &c, int u) {
+        int p = (int)((int64_t)u * c.nslots / ((int64_t)c.num_tiles * chunks_per_tile(c)));
+        while (p + 1 < c.nslots && sk_bound(c, p + 1) <= u) ++p;
+        while (p > 0 && sk_bound(c, p) > u) --p;
+        return p;
+    }
+    static __device__ __forceinline__ SegIt seg_begin(const Ctx &c) {
+        if (!c.sk) return SegIt{c.slot, c.num_tiles, 1};
+        return SegIt{sk_bound(c, c.slot), sk_bound(c, c.slot + 1), 1};
+    }
+    static __device__ __forceinline__ bool seg_next(const Ctx &c, SegIt &it, Seg &sg) {
+        if (it.cur >= it.end) return false;
+        if (!c.sk) {
+            sg.tile = it.cur;
+            sg.kb0 = 0;
+            sg.kb1 = c.nkb;
+            sg.part = -1;
+            it.cur += c.nslots;
+            return true;
+        }
+        const int cpt = chunks_per_tile(c);
+        const int tile = it.cur / cpt, ch0 = it.cur - tile * cpt;
+        const int ch1 = min(cpt, ch0 + (it.end - it.cur));
+        sg.tile = tile;
+        sg.kb0 = ch0 * C::kChunkKBlocks;
+        sg.kb1 = min(c.nkb, ch1 * C::kChunkKBlocks);
+        sg.part = (ch0 == 0 && ch1 == cpt) ? -1 : (it.first ? 0 : 1);
+        it.cur += ch1 - ch0;
+        it.first = 0;
+        return true;
     }
 
     // Waits on barriers that receive arrivals from the peer CTA or from the
@@ -415,11 +473,13 @@ struct Gemm {
         static_assert(C::NRAW <= 8 && C::NSTAGE <= 8, "fill bookkeeping");
         uint32_t s = 0, ph = 0;
         const int nstage = C::kI8 ? C::NRAW : C::NSTAGE;
-        for (int t = c.slot; t < c.num_tiles; t += c.nslots) {
+        SegIt it = seg_begin(c);
+        Seg sg;
+        while (seg_next(c, it, sg)) {
             int mb, nb;
-            tile_coords(c, t, mb, nb);
+            tile_coords(c, sg.tile, mb, nb);
             const int row_a = mb * C::kTileRows + (int)c.rank * C::BM;
-            for (int kb = 0; kb < c.nkb; ++kb) {
+            for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                 if (C::kI8) {
                     if (!mbar_wait(&c.bar->raw_empty[s], ph ^ 1u, c.w, kSiteTmaEmpty)) return;
                     uint64_t *full = &c.bar->raw_full[s];
@@ -501,9 +561,18 @@ struct Gemm {
         const uint32_t dst1 = (uint32_t)(row0 * 128 + (((2 * piece + 1) ^ phase) << 4));
         const uint32_t raw_base = smem_u32(c.raw), stage_base = smem_u32(c.stage);
         const int lane = threadIdx.x & 31;
-        // this CTA's k-blocks in order: tiles slot, slot + nslots, ... times nkb
-        const int tiles = c.slot < c.num_tiles ? (c.num_tiles - 1 - c.slot) / c.nslots + 1 : 0;
-        const int total = tiles * c.nkb;
+        // this CTA's k-blocks in order, over all its segments: whole tiles, or
+        // (stream-K) its chunks, each 16 k-blocks but a tile's last, which has
+        // nkb - 16 (cpt - 1); chunk u is a tile's last when (u + 1) % cpt == 0
+        int total;
+        if (c.sk) {
+            const int cpt = chunks_per_tile(c), u0 = sk_bound(c, c.slot), u1 = sk_bound(c, c.slot + 1);
+            const int lasts = u1 / cpt - u0 / cpt;
+            total = (u1 - u0) * C::kChunkKBlocks - lasts * (cpt * C::kChunkKBlocks - c.nkb);
+        } else {
+            const int tiles = c.slot < c.num_tiles ? (c.num_tiles - 1 - c.slot) / c.nslots + 1 : 0;
+            total = tiles * c.nkb;
+        }
         uint32_t rs = (uint32_t)group, rph = 0, cs = (uint32_t)group, cph = 0;
         for (int kidx = group; kidx < total; kidx += kG) {
             if (!mbar_wait(&c.bar->raw_full[rs], rph, c.w, kSiteConvRaw)) return;
@@ -553,8 +622,10 @@ struct Gemm {
     // after this arrive lands, so a relaxed arrive suffices.
     static __device__ void forwarder(const Ctx &c) {
         uint32_t s = 0, ph = 0;
-        for (int t = c.slot; t < c.num_tiles; t += c.nslots) {
-            for (int kb = 0; kb < c.nkb; ++kb) {
+        SegIt it = seg_begin(c);
+        Seg sg;
+        while (seg_next(c, it, sg)) {
+            for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                 if (!mbar_wait(&c.bar->full[s], ph, c.w, kSiteMmaFull)) return;
                 arrive_cluster_relaxed(leader_addr(&c.bar->full[s]));
                 if (++s == (uint32_t)C::NSTAGE) { s = 0; ph ^= 1u; }
@@ -571,9 +642,11 @@ struct Gemm {
             mbar_wait(&c.bar->never, 0, c.w, kSiteMmaFull);  // runs out; sets the abort flag
             return;
         }
-        for (int t = c.slot; t < c.num_tiles; t += c.nslots) {
-            for (int kb0 = 0; kb0 < c.nkb; kb0 += C::kChunkKBlocks) {
-                const int kb1 = min(c.nkb, kb0 + C::kChunkKBlocks);
+        SegIt it = seg_begin(c);
+        Seg sg;
+        while (seg_next(c, it, sg)) {
+            for (int kb0 = sg.kb0; kb0 < sg.kb1; kb0 += C::kChunkKBlocks) {
+                const int kb1 = min(sg.kb1, kb0 + C::kChunkKBlocks);
                 if (!wait_pair(&c.bar->acc_empty[acc], aph ^ 1u, c, kSiteMmaAccEmpty)) return;
                 tc_fence_after();
                 const uint32_t d = c.tmem + acc * BN;
@@ -871,6 +944,53 @@ struct Gemm {
         }
     }
 
+    // Stream-K: a piece of a tile.  Each epilogue warp owns the int32 sums of
+    // 32 rows x kColsPerThread columns: it stores them in its block of the
+    // workspace, and the warp that arrives last on the block's counter adds
+    // the other pieces' blocks to its own sums and finishes the rows.  The
+    // sums are exact integers, so the result is the same whatever the split.
+    // Returns whether this warp finishes the rows.
+    static __device__ __forceinline__ int sk_block(const Ctx &c, int q, int tile, int e) {
+        const int first = sk_bound(c, q) >= tile * chunks_per_tile(c) ? 0 : 1;
+        return ((q * 2 + first) * 2 + (int)c.rank) * C::kEpiWarps + e;
+    }
+    static __device__ bool sk_combine(const Ctx &c, const GemmArgs &a, const Seg &sg, int e, int lane,
+                                      int32_t (&tot)[C::kColsPerThread]) {
+        constexpr int kV = C::kColsPerThread / 4;   // int4 per lane per block
+        static_assert(32 * kV * 16 == 16384, "workspace block");
+        {
+            int4 *mine = a.sk_ws + (int64_t)sk_block(c, c.slot, sg.tile, e) * (32 * kV) + lane;
+#pragma unroll
+            for (int j = 0; j < kV; ++j)
+                mine[j * 32] = make_int4(tot[4 * j], tot[4 * j + 1], tot[4 * j + 2], tot[4 * j + 3]);
+        }
+        __threadfence();
+        __syncwarp();
+        const int cpt = chunks_per_tile(c), u_first = sg.tile * cpt;
+        const int q0 = sk_owner(c, u_first), q1 = sk_owner(c, u_first + cpt - 1);
+        int *cnt = a.sk_cnt + (sg.tile * 2 + (int)c.rank) * 8 + e;
+        int old = 0;
+        if (lane == 0) old = atomicAdd(cnt, 1);
+        old = __shfl_sync(0xFFFFFFFFu, old, 0);
+        if (old != q1 - q0) return false;
+        __threadfence();
+#pragma unroll 1
+        for (int q = q0; q <= q1; ++q) {
+            if (q == c.slot) continue;
+            const int4 *o = a.sk_ws + (int64_t)sk_block(c, q, sg.tile, e) * (32 * kV) + lane;
+#pragma unroll
+            for (int j = 0; j < kV; ++j) {
+                const int4 v = __ldcg(o + j * 32);
+                tot[4 * j] += v.x;
+                tot[4 * j + 1] += v.y;
+                tot[4 * j + 2] += v.z;
+                tot[4 * j + 3] += v.w;
+            }
+        }
+        if (lane == 0) atomicExch(cnt, 0);   // zero again for the next launch
+        return true;
+    }
+
     static __device__ void epilogue(const Ctx &c, const GemmArgs &a) {
         int yiter = 0, yloads = 0;
         epilogue_tiles(c, a, yiter, yloads);
@@ -881,7 +1001,8 @@ struct Gemm {
                 // away, and a y load still in flight (after an abort) has landed
                 bulk_wait_all();
                 for (int k = yiter; k < yloads; ++k)
-                    mbar_wait_drain(&c.bar->ybar[k & 1], (uint32_t)(k >> 1) & 1u, 200000000ull, a.status);
+                    mbar_wait_drain(&c.bar->ybar[k % C::kYBufs], (uint32_t)(k / C::kYBufs) & 1u, 200000000ull,
+                                    a.status);
             }
         }
     }
@@ -892,7 +1013,10 @@ struct Gemm {
         const int e = warp - C::kEpiWarp0, quad = warp & 3, half = e >> 2;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         uint32_t acc = 0, aph = 0;
-        for (int t = c.slot; t < c.num_tiles; t += c.nslots) {
+        SegIt it = seg_begin(c);
+        Seg sg;
+        while (seg_next(c, it, sg)) {
+            const int t = sg.tile;
             int mb, nb;
             tile_coords(c, t, mb, nb);
             const int row = mb * C::kTileRows + (int)c.rank * C::BM + quad * 32 + lane;
@@ -901,7 +1025,7 @@ struct Gemm {
                 int32_t tot[C::kColsPerThread];
 #pragma unroll
                 for (int i = 0; i < C::kColsPerThread; ++i) tot[i] = 0;
-                for (int kb0 = 0; kb0 < c.nkb; kb0 += C::kChunkKBlocks) {
+                for (int kb0 = sg.kb0; kb0 < sg.kb1; kb0 += C::kChunkKBlocks) {
                     if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
                     tc_fence_after();
                     const uint32_t tbase = c.tmem + acc * BN + lane_off;
@@ -916,27 +1040,30 @@ struct Gemm {
                     release_acc(c, acc, lane);
                     if (++acc == (uint32_t)C::kAccBufs) { acc = 0; aph ^= 1u; }
                 }
-                // the tile's exact int32 accumulators are complete
-                finish_row(a, row, row_ok, nb, half, tot);
+                // the tile's exact int32 accumulators are complete (stream-K:
+                // once the last piece to arrive has added the others)
+                if (sg.part < 0 || sk_combine(c, a, sg, e, lane, tot))
+                    finish_row(a, row, row_ok, nb, half, tot);
             } else if constexpr (C::kLoraSwi) {
                 // base g|u tiles by TMA one tile ahead, h computed in place over the
                 // gate columns, stored by TMA after a bounded epilogue rendezvous
-                const int b = yiter & 1;
+                const int b = yiter % C::kYBufs;
                 if (e == 0 && lane == 0) {
-                    if (yiter == 0) {
-                        gu_tile_load(c, a, t, b);
-                        ++yloads;
-                    }
-                    const int tn = t + c.nslots;
+                    if (yiter == 0)
+                        for (int i = 0; i < C::kYBufs - 1 && t + i * c.nslots < c.num_tiles; ++i) {
+                            gu_tile_load(c, a, t + i * c.nslots, i);
+                            ++yloads;
+                        }
+                    const int tn = t + (C::kYBufs - 1) * c.nslots;
                     if (tn < c.num_tiles) {
-                        bulk_wait_read_all();
-                        gu_tile_load(c, a, tn, b ^ 1);
+                        bulk_wait_read_all();   // tile yiter - 1's store, this buffer's last tenant, has read it
+                        gu_tile_load(c, a, tn, (yiter + C::kYBufs - 1) % C::kYBufs);
                         ++yloads;
                     }
                 }
                 if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
                 tc_fence_after();
-                if (!mbar_wait(&c.bar->ybar[b], (uint32_t)(yiter >> 1) & 1u, c.w, kSiteEpiAccFull)) return;
+                if (!mbar_wait(&c.bar->ybar[b], (uint32_t)(yiter / C::kYBufs) & 1u, c.w, kSiteEpiAccFull)) return;
                 const uint32_t tbase = c.tmem + acc * BN + lane_off;
                 uint32_t vg[32], vu[32];
                 tmem_ld32(tbase + chunk_col(0, half), vg);
@@ -957,22 +1084,23 @@ struct Gemm {
                 // y += acc: the tile's y arrives by TMA (loaded one tile ahead into
                 // the other buffer), each thread adds its accumulator row in place,
                 // and the tile leaves by TMA once every epilogue thread is done
-                const int b = yiter & 1;
+                const int b = yiter % C::kYBufs;
                 if (e == 0 && lane == 0) {
-                    if (yiter == 0) {
-                        y_tile_load(c, a, t, b);
-                        ++yloads;
-                    }
-                    const int tn = t + c.nslots;
+                    if (yiter == 0)
+                        for (int i = 0; i < C::kYBufs - 1 && t + i * c.nslots < c.num_tiles; ++i) {
+                            y_tile_load(c, a, t + i * c.nslots, i);
+                            ++yloads;
+                        }
+                    const int tn = t + (C::kYBufs - 1) * c.nslots;
                     if (tn < c.num_tiles) {
-                        bulk_wait_read_all();   // the other buffer's last store has read it
-                        y_tile_load(c, a, tn, b ^ 1);
+                        bulk_wait_read_all();   // tile yiter - 1's store, this buffer's last tenant, has read it
+                        y_tile_load(c, a, tn, (yiter + C::kYBufs - 1) % C::kYBufs);
                         ++yloads;
                     }
                 }
                 if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
                 tc_fence_after();
-                if (!mbar_wait(&c.bar->ybar[b], (uint32_t)(yiter >> 1) & 1u, c.w, kSiteEpiAccFull)) return;
+                if (!mbar_wait(&c.bar->ybar[b], (uint32_t)(yiter / C::kYBufs) & 1u, c.w, kSiteEpiAccFull)) return;
                 const uint32_t tbase = c.tmem + acc * BN + lane_off;
 #pragma unroll
                 for (int j = 0; j < C::kChunks32; ++j) {
@@ -1041,8 +1169,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             mbar_init(&bar->acc_empty[s], C::kAccEmptyArrivals);
         }
         mbar_init(&bar->drain, 1);
-        mbar_init(&bar->ybar[0], 1);
-        mbar_init(&bar->ybar[1], 1);
+        for (int i = 0; i < C::kYBufs; ++i) mbar_init(&bar->ybar[i], 1);
         mbar_init(&bar->epi_done, C::kEpiWarps);
         mbar_init(&bar->never, 1);
         bar->abort = 0;
@@ -1099,6 +1226,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     c.num_tiles = c.num_m * c.num_n;
     c.nkb = C::kI8 ? (args.K + 63) / 64 : (args.K + C::BK - 1) / C::BK;
     c.n_fastest = args.n_fastest;
+    c.sk = C::kStreamK ? args.sk : 0;
     c.force_timeout = args.force_timeout;
     c.w.limit_ns = args.wait_limit_ns;
     c.w.abort = &bar->abort;
@@ -1221,9 +1349,26 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
             e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
             max_pairs = (e == cudaSuccess && n > 0) ? n : num_sms / 2;
         }
-        const int pairs = tiles < max_pairs ? tiles : max_pairs;
+        int pairs = tiles < max_pairs ? tiles : max_pairs;
+        GemmArgs la = args;
+        la.sk = 0;
+        if (C::kStreamK && args.sk_ws && args.sk_cnt) {
+            // stream-K where the last wave of whole tiles would leave more than
+            // 8% of the pairs' time idle (the GEMM time follows the count of
+            // waves: 1502 x 5120 x 17408 and 1502 x 6400 x 17408 both take
+            // 206 us) and the workspace holds every pair's pieces
+            const int nkb = (args.K + 63) / 64, cpt = (nkb + C::kChunkKBlocks - 1) / C::kChunkKBlocks;
+            const int64_t waves = (tiles + max_pairs - 1) / max_pairs;
+            const double fill = (double)tiles / (double)(waves * max_pairs);
+            if (fill < 0.92 && cpt >= 2 && tiles <= kSkMaxTiles &&
+                args.sk_ws_bytes >= (int64_t)max_pairs * kSkBytesPerPair) {
+                la.sk = 1;
+                const int64_t units = (int64_t)tiles * cpt;
+                pairs = units < max_pairs ? (int)units : max_pairs;
+            }
+        }
         cfg.gridDim = dim3(2 * pairs, 1, 1);
-        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, tc, td, args);
+        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, tc, td, la);
     } else {
         const int grid = tiles < num_sms ? tiles : num_sms;
         kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(ta, tb, tb2, tc, td, args);
@@ -1271,6 +1416,8 @@ int launch_gemm(int op, int epi, int bn, const Operand &A, const Operand &B, con
                             : launch_one<kOpBF16, kEpiStoreBF16, 256, false>(A, B, args, num_sms, st, B2);
         } else if (epi == kEpiAddBF16 && bn == 256) {
             CLEF_GEMM(kOpBF16, kEpiAddBF16, 256);
+        } else if (epi == kEpiAddBF16 && bn == 128) {
+            return launch_one<kOpBF16, kEpiAddBF16, 128, false>(A, B, args, num_sms, st);
         } else if (epi == kEpiLoraSwiGLU && bn == 256) {
             const bool pr = gemm_uses_pair(bn, args.M, num_sms);
             return pr ? launch_one<kOpBF16, kEpiLoraSwiGLU, 256, true>(A, B, args, num_sms, st, B2)

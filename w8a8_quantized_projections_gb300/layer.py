@@ -34,8 +34,9 @@ from typing import Dict, Optional, Tuple
 
 import torch
 
-from . import (fp8_gateup_swiglu, fp8_linear, lora_add, lora_expand_add, lora_gateup_swiglu, lora_pad,
-               lora_shrink, quant_act, w8a8_gateup_swiglu, w8a8_linear)
+from . import (bind_workspace, fp8_gateup_swiglu, fp8_linear, gemm_workspace_bytes, lora_add,
+               lora_expand_add, lora_gateup_swiglu, lora_pad, lora_shrink, quant_act, w8a8_gateup_swiglu,
+               w8a8_linear)
 
 
 class QuantizedLayer:
@@ -72,6 +73,11 @@ class QuantizedLayer:
                 self.w[p.name] = (qw[r0:r1], sw[r0:r1], None if b is None else b[r0:r1])
                 r0 = r1
         torch.cuda.synchronize()
+        # INT8: a stream-K workspace, bound to whichever stream runs a step
+        # (tiles of a GEMM whose last wave would be mostly idle are split
+        # across SMs; the outputs are the same bytes)
+        self.ws = None if self.fp8 else torch.zeros(gemm_workspace_bytes(), dtype=torch.uint8,
+                                                     device=device)
         code = torch.uint8 if self.fp8 else torch.int8
         self.q = {}
         for name, K in cfg.activations():
@@ -191,6 +197,8 @@ class QuantizedLayer:
         step's last projection writes its output (e.g. the read-back of the
         previous step's output on another stream)."""
         ev = _Rec(events)
+        if self.ws is not None:
+            bind_workspace(self.ws)
         lin = fp8_linear if self.fp8 else w8a8_linear
         gu = fp8_gateup_swiglu if self.fp8 else w8a8_gateup_swiglu
         for name, _ in self.cfg.activations():
