@@ -1,7 +1,8 @@
 """INT8 stream-K: with a workspace bound to the stream, GEMMs whose last wave
-of whole tiles would leave CTA pairs idle deal the tiles' 1024-deep K chunks
-evenly to the pairs, and the pieces of a tile meet as exact int32 partial sums.
-Every output must equal the unsplit launch's bytes (and the oracle's)."""
+of whole tiles would leave CTA pairs idle keep their whole waves and deal the
+remaining tiles' k-blocks to the pairs in even runs; the pieces of a tile meet
+as exact int32 partial sums.  Every output must equal the unsplit launch's
+bytes (and the oracle's)."""
 import numpy as np
 import pytest
 import torch
@@ -31,10 +32,12 @@ def bound_workspace(stream=None):
     return ws
 
 
-# (M, N, K): 120 tiles on 76 pairs; 48 tiles (one thin wave); K with a
-# one-k-block last chunk; two chunks per tile; a full wave (no split)
-SHAPES = [(1502, 5120, 17408), (300, 6144, 5120), (600, 2048, 17472), (257, 512, 1088),
-          (1024, 4864, 1024)]
+# (M, N, K) on 76 CTA pairs: 120 tiles (one whole wave, 44 tiles split); K
+# of 273 k-blocks (runs end off the 16-k-block chunk grid); 88 tiles with 12
+# split into two 16-k-block runs each; 180 tiles (two whole waves, 28 split);
+# 48 tiles (under one wave: not split); 76 tiles (a full wave: not split)
+SHAPES = [(1502, 5120, 17408), (1502, 5120, 17472), (1024, 5632, 2048), (2270, 5120, 6144),
+          (300, 6144, 5120), (1024, 4864, 1024)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
@@ -111,3 +114,25 @@ def test_unbound_stream_never_splits_and_unbind_works():
     torch.cuda.synchronize()
     assert int(ws.count_nonzero()) == 0, "a workspace bound to another stream was written"
     assert torch.equal(clef.w8a8_gemm_s32(qx_d, qw_d), ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(1024, 2560, 4096), (300, 2048, 4096)])
+def test_stream_k_swiglu_equals_unsplit(M, N, K):
+    """The fused gate/up SwiGLU launches never split (their kernel has no
+    split path); a bound workspace leaves their bytes and the counters as
+    they were: 80 tiles of 256 rows x 128 h columns and 32 tiles."""
+    rng = np.random.default_rng(M)
+    qx_d = dev(codes(10, M, K))
+    qw_d = dev(codes(11, 2 * N, K))
+    sx = torch.tensor(rng.random(M, dtype=np.float32) * 1e-3, device="cuda")
+    sw = torch.tensor(rng.random(2 * N, dtype=np.float32) * 1e-3, device="cuda")
+    b = torch.tensor(rng.standard_normal(2 * N, dtype=np.float32), device="cuda").to(torch.bfloat16)
+    plain = clef.w8a8_gateup_swiglu(qx_d, sx, qw_d, sw, b)
+    ws = bound_workspace()
+    try:
+        split = clef.w8a8_gateup_swiglu(qx_d, sx, qw_d, sw, b)
+        torch.cuda.synchronize()
+        assert int(ws[:COUNTER_BYTES].count_nonzero()) == 0
+    finally:
+        clef.bind_workspace(None)
+    assert torch.equal(split.view(torch.int16), plain.view(torch.int16))

@@ -70,11 +70,13 @@ struct GemmArgs {
     // kEpiStoreBF16 with two stacked B factors: rows from b2_row0 on come from
     // the second operand (its row b2_row0 less); 0 = one B operand
     int b2_row0;
-    // INT8 stream-K (sk = 1): the tiles' 1024-K chunks are shared evenly by
-    // the CTA pairs; pieces of a tile meet in the workspace: sk_cnt holds
-    // kSkMaxTiles x 2 x 8 arrival counters (zero between launches), sk_ws the
-    // int32 partial sums.  sk_ws_bytes: the partial region's size.
+    // INT8 stream-K (sk > 0): tiles from sk_tail0 on are dealt to the first
+    // sk CTA pairs as even runs of k-blocks; pieces of a tile meet in the
+    // workspace: sk_cnt holds kSkMaxTiles x 2 x 8 arrival counters (zero
+    // between launches), sk_ws the int32 partial sums.  sk_ws_bytes: the
+    // partial region's size.  The launcher sets sk and sk_tail0.
     int sk;
+    int sk_tail0;
     int *sk_cnt;
     int4 *sk_ws;
     int64_t sk_ws_bytes;

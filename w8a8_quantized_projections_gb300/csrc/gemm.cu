@@ -40,6 +40,7 @@
 // "clef-flash-FP8" model card, Quantization table (FP8 W8A8 dynamic);
 // TensorFold pull request 1364 (LoRA products on bf16 tensor cores,
 // y = bf16(y + bf16(x A^T) B^T)).
+#include <algorithm>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -105,8 +106,10 @@ struct Cfg {
     static constexpr int kColsPerThread = BN / kParts;     // columns one epilogue thread owns
     static constexpr int kChunks32 = kColsPerThread / 32;
     static constexpr bool kSwiGLU = (EPI == kEpiSwiGLU || EPI == kEpiLoraSwiGLU);  // gate|up tile
-    // INT8 stream-K is compiled into the pair kernels of the scale/bias and
-    // int32 epilogues (with the SwiGLU epilogue the combine step spills)
+    // INT8 stream-K is compiled into the pair kernels (exact int32 pieces)
+    // but not the SwiGLU one: the gate/up launches of the workloads fill at
+    // least 94% of their last wave, and with the split path compiled in the
+    // unsplit gate/up kernel ran 1.2% slower (352.7 against 344.5 us)
     static constexpr bool kStreamK = kI8 && PAIR && !kSwiGLU;
     static constexpr int kOutColsPerTile = kSwiGLU ? BN / 2 : BN;
     // full[s]: TMA (native) or the local converter warps (INT8); in pair mode
@@ -143,6 +146,9 @@ struct Barriers {
     uint64_t epi_done;   // y += acc: every epilogue warp has written the tile's y
     uint32_t tmem_slot;
     int abort;
+    // INT8 stream-K (kept here rather than in registers): the count of slots
+    // sharing the last tiles' k-blocks (0 = off) and the first of those tiles
+    int sk, sk_tail0;
 };
 static_assert(sizeof(Barriers) <= 512, "barrier block");
 
@@ -371,7 +377,6 @@ struct Gemm {
         int slot, nslots;    // tile-loop start and stride
         int num_m, num_n, num_tiles, nkb;
         int n_fastest;       // tile order: 0 = M fastest, 1 = N fastest
-        int sk;              // INT8 stream-K: the slots share the tiles' 1024-K chunks evenly
         int force_timeout;   // test knob: the MMA issuer waits on a barrier nothing signals
         WaitCtx w;
     };
@@ -390,53 +395,68 @@ struct Gemm {
 
     // A CTA's work is a list of segments: a tile and a range of its k-blocks.
     // Classic schedule: whole tiles slot, slot + nslots, ...  Stream-K: the
-    // num_tiles * cpt chunks in tile order, slot p owning chunks [b(p),
-    // b(p + 1)) with b(p) = floor(p * num_tiles * cpt / nslots), so a slot's
-    // run may begin and end inside tiles.  part: -1 for a whole tile, 0 for a
-    // piece that is the slot's first segment, 1 for a later piece (a slot has
-    // at most two pieces: its first and its last segment).
+    // same for the tiles before sk_tail0 (the whole waves), then the k-blocks
+    // of the remaining tiles, in (tile, k-block) order, dealt to the first sk
+    // slots in even contiguous runs: slot p < sk owns k-block indices [b(p),
+    // b(p + 1)) with b(p) = floor(p * (num_tiles - sk_tail0) * nkb / sk).
+    // part: -1 for a whole tile, 0 for the slot's first piece of a split
+    // tile, 1 for its second (a run is shorter than a tile, so it touches at
+    // most two).
     struct Seg {
         int tile, kb0, kb1, part;
     };
-    struct SegIt {
-        int cur, end, first;
-    };
-    static __device__ __forceinline__ int chunks_per_tile(const Ctx &c) {
-        return (c.nkb + C::kChunkKBlocks - 1) / C::kChunkKBlocks;
-    }
+    static __device__ __forceinline__ int sk_of(const Ctx &c) { return C::kStreamK ? c.bar->sk : 0; }
+    static __device__ __forceinline__ int sk_tail0(const Ctx &c) { return C::kStreamK ? c.bar->sk_tail0 : 0; }
+    // (32-bit arithmetic suffices: fewer than 256 slots share fewer than 256
+    // tiles of at most 1024 k-blocks)
     static __device__ __forceinline__ int sk_bound(const Ctx &c, int p) {
-        return (int)((int64_t)p * c.num_tiles * chunks_per_tile(c) / c.nslots);
+        return (int)((uint32_t)p * (uint32_t)((c.num_tiles - sk_tail0(c)) * c.nkb) / (uint32_t)sk_of(c));
     }
-    static __device__ __forceinline__ int sk_owner(const Ctx &c, int u) {
-        int p = (int)((int64_t)u * c.nslots / ((int64_t)c.num_tiles * chunks_per_tile(c)));
-        while (p + 1 < c.nslots && sk_bound(c, p + 1) <= u) ++p;
-        while (p > 0 && sk_bound(c, p) > u) --p;
+    static __device__ __forceinline__ int sk_owner(const Ctx &c, int v) {
+        int p = (int)((uint32_t)v * (uint32_t)sk_of(c) / (uint32_t)((c.num_tiles - sk_tail0(c)) * c.nkb));
+        while (p + 1 < sk_of(c) && sk_bound(c, p + 1) <= v) ++p;
+        while (p > 0 && sk_bound(c, p) > v) --p;
         return p;
     }
-    static __device__ __forceinline__ SegIt seg_begin(const Ctx &c) {
-        if (!c.sk) return SegIt{c.slot, c.num_tiles, 1};
-        return SegIt{sk_bound(c, c.slot), sk_bound(c, c.slot + 1), 1};
+    // The slot's segments: `whole` whole tiles, then (stream-K) the pieces
+    // of its run, `total` in all.  Loops run i = 0 .. total - 1 over seg_at.
+    struct Segs {
+        int whole, total;
+    };
+    static __device__ __forceinline__ Segs seg_plan(const Ctx &c) {
+        const int whole_end = sk_of(c) ? sk_tail0(c) : c.num_tiles;
+        Segs p;
+        p.whole = c.slot < whole_end ? (whole_end - 1 - c.slot) / c.nslots + 1 : 0;
+        p.total = p.whole;
+        if (sk_of(c) && c.slot < sk_of(c)) {
+            const int v0 = sk_bound(c, c.slot), v1 = sk_bound(c, c.slot + 1);
+            if (v1 > v0) p.total += (v1 - 1) / c.nkb - v0 / c.nkb + 1;
+        }
+        return p;
     }
-    static __device__ __forceinline__ bool seg_next(const Ctx &c, SegIt &it, Seg &sg) {
-        if (it.cur >= it.end) return false;
-        if (!c.sk) {
-            sg.tile = it.cur;
+    static __device__ __forceinline__ Seg seg_at(const Ctx &c, const Segs &p, int i) {
+        Seg sg;
+        if (i < p.whole) {
+            sg.tile = c.slot + i * c.nslots;
             sg.kb0 = 0;
             sg.kb1 = c.nkb;
             sg.part = -1;
-            it.cur += c.nslots;
-            return true;
+            return sg;
         }
-        const int cpt = chunks_per_tile(c);
-        const int tile = it.cur / cpt, ch0 = it.cur - tile * cpt;
-        const int ch1 = min(cpt, ch0 + (it.end - it.cur));
-        sg.tile = tile;
-        sg.kb0 = ch0 * C::kChunkKBlocks;
-        sg.kb1 = min(c.nkb, ch1 * C::kChunkKBlocks);
-        sg.part = (ch0 == 0 && ch1 == cpt) ? -1 : (it.first ? 0 : 1);
-        it.cur += ch1 - ch0;
-        it.first = 0;
-        return true;
+        const int v0 = sk_bound(c, c.slot), v1 = sk_bound(c, c.slot + 1);
+        const int rel0 = v0 / c.nkb;
+        if (i == p.whole) {
+            sg.tile = sk_tail0(c) + rel0;
+            sg.kb0 = v0 - rel0 * c.nkb;
+            sg.kb1 = min(c.nkb, sg.kb0 + (v1 - v0));
+            sg.part = (sg.kb0 == 0 && sg.kb1 == c.nkb) ? -1 : 0;
+        } else {
+            sg.tile = sk_tail0(c) + rel0 + 1;
+            sg.kb0 = 0;
+            sg.kb1 = v1 - (rel0 + 1) * c.nkb;
+            sg.part = 1;
+        }
+        return sg;
     }
 
     // Waits on barriers that receive arrivals from the peer CTA or from the
@@ -473,9 +493,9 @@ struct Gemm {
         static_assert(C::NRAW <= 8 && C::NSTAGE <= 8, "fill bookkeeping");
         uint32_t s = 0, ph = 0;
         const int nstage = C::kI8 ? C::NRAW : C::NSTAGE;
-        SegIt it = seg_begin(c);
-        Seg sg;
-        while (seg_next(c, it, sg)) {
+        const Segs sp = seg_plan(c);
+        for (int si = 0; si < sp.total; ++si) {
+            const Seg sg = seg_at(c, sp, si);
             int mb, nb;
             tile_coords(c, sg.tile, mb, nb);
             const int row_a = mb * C::kTileRows + (int)c.rank * C::BM;
@@ -561,18 +581,11 @@ struct Gemm {
         const uint32_t dst1 = (uint32_t)(row0 * 128 + (((2 * piece + 1) ^ phase) << 4));
         const uint32_t raw_base = smem_u32(c.raw), stage_base = smem_u32(c.stage);
         const int lane = threadIdx.x & 31;
-        // this CTA's k-blocks in order, over all its segments: whole tiles, or
-        // (stream-K) its chunks, each 16 k-blocks but a tile's last, which has
-        // nkb - 16 (cpt - 1); chunk u is a tile's last when (u + 1) % cpt == 0
-        int total;
-        if (c.sk) {
-            const int cpt = chunks_per_tile(c), u0 = sk_bound(c, c.slot), u1 = sk_bound(c, c.slot + 1);
-            const int lasts = u1 / cpt - u0 / cpt;
-            total = (u1 - u0) * C::kChunkKBlocks - lasts * (cpt * C::kChunkKBlocks - c.nkb);
-        } else {
-            const int tiles = c.slot < c.num_tiles ? (c.num_tiles - 1 - c.slot) / c.nslots + 1 : 0;
-            total = tiles * c.nkb;
-        }
+        // this CTA's k-blocks in order, over all its segments: its whole tiles,
+        // then (stream-K) its run of the remaining tiles' k-blocks
+        const int whole_end = sk_of(c) ? sk_tail0(c) : c.num_tiles;
+        int total = (c.slot < whole_end ? (whole_end - 1 - c.slot) / c.nslots + 1 : 0) * c.nkb;
+        if (sk_of(c) && c.slot < sk_of(c)) total += sk_bound(c, c.slot + 1) - sk_bound(c, c.slot);
         uint32_t rs = (uint32_t)group, rph = 0, cs = (uint32_t)group, cph = 0;
         for (int kidx = group; kidx < total; kidx += kG) {
             if (!mbar_wait(&c.bar->raw_full[rs], rph, c.w, kSiteConvRaw)) return;
@@ -622,9 +635,9 @@ struct Gemm {
     // after this arrive lands, so a relaxed arrive suffices.
     static __device__ void forwarder(const Ctx &c) {
         uint32_t s = 0, ph = 0;
-        SegIt it = seg_begin(c);
-        Seg sg;
-        while (seg_next(c, it, sg)) {
+        const Segs sp = seg_plan(c);
+        for (int si = 0; si < sp.total; ++si) {
+            const Seg sg = seg_at(c, sp, si);
             for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                 if (!mbar_wait(&c.bar->full[s], ph, c.w, kSiteMmaFull)) return;
                 arrive_cluster_relaxed(leader_addr(&c.bar->full[s]));
@@ -642,9 +655,9 @@ struct Gemm {
             mbar_wait(&c.bar->never, 0, c.w, kSiteMmaFull);  // runs out; sets the abort flag
             return;
         }
-        SegIt it = seg_begin(c);
-        Seg sg;
-        while (seg_next(c, it, sg)) {
+        const Segs sp = seg_plan(c);
+        for (int si = 0; si < sp.total; ++si) {
+            const Seg sg = seg_at(c, sp, si);
             for (int kb0 = sg.kb0; kb0 < sg.kb1; kb0 += C::kChunkKBlocks) {
                 const int kb1 = min(sg.kb1, kb0 + C::kChunkKBlocks);
                 if (!wait_pair(&c.bar->acc_empty[acc], aph ^ 1u, c, kSiteMmaAccEmpty)) return;
@@ -951,7 +964,7 @@ struct Gemm {
     // sums are exact integers, so the result is the same whatever the split.
     // Returns whether this warp finishes the rows.
     static __device__ __forceinline__ int sk_block(const Ctx &c, int q, int tile, int e) {
-        const int first = sk_bound(c, q) >= tile * chunks_per_tile(c) ? 0 : 1;
+        const int first = sk_bound(c, q) >= (tile - sk_tail0(c)) * c.nkb ? 0 : 1;
         return ((q * 2 + first) * 2 + (int)c.rank) * C::kEpiWarps + e;
     }
     static __device__ bool sk_combine(const Ctx &c, const GemmArgs &a, const Seg &sg, int e, int lane,
@@ -966,8 +979,8 @@ struct Gemm {
         }
         __threadfence();
         __syncwarp();
-        const int cpt = chunks_per_tile(c), u_first = sg.tile * cpt;
-        const int q0 = sk_owner(c, u_first), q1 = sk_owner(c, u_first + cpt - 1);
+        const int v_first = (sg.tile - sk_tail0(c)) * c.nkb;
+        const int q0 = sk_owner(c, v_first), q1 = sk_owner(c, v_first + c.nkb - 1);
         int *cnt = a.sk_cnt + (sg.tile * 2 + (int)c.rank) * 8 + e;
         int old = 0;
         if (lane == 0) old = atomicAdd(cnt, 1);
@@ -1013,9 +1026,9 @@ struct Gemm {
         const int e = warp - C::kEpiWarp0, quad = warp & 3, half = e >> 2;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         uint32_t acc = 0, aph = 0;
-        SegIt it = seg_begin(c);
-        Seg sg;
-        while (seg_next(c, it, sg)) {
+        const Segs sp = seg_plan(c);
+        for (int si = 0; si < sp.total; ++si) {
+            const Seg sg = seg_at(c, sp, si);
             const int t = sg.tile;
             int mb, nb;
             tile_coords(c, t, mb, nb);
@@ -1173,6 +1186,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         mbar_init(&bar->epi_done, C::kEpiWarps);
         mbar_init(&bar->never, 1);
         bar->abort = 0;
+        bar->sk = C::kStreamK ? args.sk : 0;
+        bar->sk_tail0 = args.sk_tail0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -1226,7 +1241,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     c.num_tiles = c.num_m * c.num_n;
     c.nkb = C::kI8 ? (args.K + 63) / 64 : (args.K + C::BK - 1) / C::BK;
     c.n_fastest = args.n_fastest;
-    c.sk = C::kStreamK ? args.sk : 0;
+
     c.force_timeout = args.force_timeout;
     c.w.limit_ns = args.wait_limit_ns;
     c.w.abort = &bar->abort;
@@ -1352,19 +1367,28 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
         int pairs = tiles < max_pairs ? tiles : max_pairs;
         GemmArgs la = args;
         la.sk = 0;
+        la.sk_tail0 = 0;
         if (C::kStreamK && args.sk_ws && args.sk_cnt) {
-            // stream-K where the last wave of whole tiles would leave more than
-            // 8% of the pairs' time idle (the GEMM time follows the count of
-            // waves: 1502 x 5120 x 17408 and 1502 x 6400 x 17408 both take
-            // 206 us) and the workspace holds every pair's pieces
-            const int nkb = (args.K + 63) / 64, cpt = (nkb + C::kChunkKBlocks - 1) / C::kChunkKBlocks;
+            // Stream-K where the last wave of whole tiles would leave more
+            // than 8% of the pairs' time idle (the GEMM time follows the count
+            // of waves: 1502 x 5120 x 17408 and 1502 x 6400 x 17408 both take
+            // 206 us unsplit).  The whole waves stay whole tiles (running pairs
+            // then share weight tiles in L2, as unsplit); the R tiles left are
+            // dealt as k-block runs of at least 16 k-blocks to up to every
+            // pair, and the workspace must hold every pair's two pieces.  A
+            // launch of less than one wave stays unsplit (300 x 6144 x 5120:
+            // 53.5 us unsplit, 55.6 us with every tile split).
+            const int nkb = (args.K + 63) / 64;
             const int64_t waves = (tiles + max_pairs - 1) / max_pairs;
             const double fill = (double)tiles / (double)(waves * max_pairs);
-            if (fill < 0.92 && cpt >= 2 && tiles <= kSkMaxTiles &&
+            const int tail0 = tiles >= max_pairs ? (tiles / max_pairs) * max_pairs : 0;
+            const int64_t rest = (int64_t)(tiles - tail0) * nkb;
+            const int p2 = (int)std::min<int64_t>(max_pairs, rest / C::kChunkKBlocks);
+            if (fill < 0.92 && tail0 > 0 && p2 > tiles - tail0 && tiles <= kSkMaxTiles &&
                 args.sk_ws_bytes >= (int64_t)max_pairs * kSkBytesPerPair) {
-                la.sk = 1;
-                const int64_t units = (int64_t)tiles * cpt;
-                pairs = units < max_pairs ? (int)units : max_pairs;
+                la.sk = p2;
+                la.sk_tail0 = tail0;
+                pairs = tail0 > 0 ? max_pairs : p2;
             }
         }
         cfg.gridDim = dim3(2 * pairs, 1, 1);

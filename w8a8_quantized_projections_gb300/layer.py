@@ -78,6 +78,7 @@ class QuantizedLayer:
         # across SMs; the outputs are the same bytes)
         self.ws = None if self.fp8 else torch.zeros(gemm_workspace_bytes(), dtype=torch.uint8,
                                                      device=device)
+        self._ws_stream = None   # the stream the workspace was last bound to
         code = torch.uint8 if self.fp8 else torch.int8
         self.q = {}
         for name, K in cfg.activations():
@@ -198,7 +199,12 @@ class QuantizedLayer:
         previous step's output on another stream)."""
         ev = _Rec(events)
         if self.ws is not None:
-            bind_workspace(self.ws)
+            # bind once per stream (the binding is host bookkeeping, but a
+            # Python call per step would delay the step's first launch)
+            s = torch.cuda.current_stream()
+            if self._ws_stream != s.cuda_stream:
+                bind_workspace(self.ws, s)
+                self._ws_stream = s.cuda_stream
         lin = fp8_linear if self.fp8 else w8a8_linear
         gu = fp8_gateup_swiglu if self.fp8 else w8a8_gateup_swiglu
         for name, _ in self.cfg.activations():
