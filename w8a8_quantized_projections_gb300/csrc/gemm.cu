@@ -89,10 +89,13 @@ struct Cfg {
     // per epilogue warp, so that y is read and written in row segments.
     static constexpr bool kLoraSwi = (EPI == kEpiLoraSwiGLU);
     // y += acc: a ring of kYBufs y tiles (BM x BN bf16) that TMA loads
-    // kYBufs - 1 tiles ahead and stores; 128-wide tiles keep 4 (three loads
-    // in flight, 96 KB, against one 64 KB load for the 256-wide pair tiles)
+    // kYBufs - 1 tiles ahead and stores.  128-wide tiles keep 3, which leaves
+    // room for 4 operand stages: the t and B operands come from L2 and their
+    // latency bounds this short-K GEMM as much as y's (24,032 x 4096 rank-256
+    // expand: 2 y buffers + 5 stages 102.7 us, 4 + 3 103.3 us, 3 + 4 96.5 us;
+    // 256-wide pair tiles with 2 + 3: 114.7 us)
     static constexpr int kYTile = BM * BN * 2;
-    static constexpr int kYBufs = (EPI == kEpiAddBF16 && BN == 128) ? 4 : 2;
+    static constexpr int kYBufs = (EPI == kEpiAddBF16 && BN == 128) ? 3 : 2;
     static constexpr int kEpiStage = (EPI == kEpiAddBF16 || kLoraSwi) ? kYBufs * kYTile : 0;
     static constexpr int NSTAGE_RAWFREE = (kSmemBudget - NRAW * kRawStage - kEpiStage) / kStage;
     static constexpr int NSTAGE = kI8 ? (PAIR ? 4 : 2) : (NSTAGE_RAWFREE > 8 ? 8 : NSTAGE_RAWFREE);

@@ -130,7 +130,7 @@ extern "C" int clef_lora_add_noalloc(const void *x, int64_t ldx, const void *A, 
     a2.ldo = ldy;
     a2.status = status;
     a2.wait_limit_ns = 1000000000ull;
-    return launch_gemm(kOpBF16, kEpiAddBF16, 256,
+    return launch_gemm(kOpBF16, kEpiAddBF16, 128,
                        Operand{t, (uint64_t)r_pad, (uint64_t)M, (uint64_t)r_pad * 2},
                        Operand{B, (uint64_t)r, (uint64_t)N, (uint64_t)r * 2}, a2, num_sms, st);
 }
