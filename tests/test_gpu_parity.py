@@ -51,7 +51,8 @@ def staging(request):
 
 
 @pytest.mark.parametrize("M,K", [(298, 2048), (1, 128), (5, 384), (130, 5120), (1502, 17408),
-                                 (2270, 6144), (3, 40960), (12000, 5120), (2, 128 * 131), (4, 65536)])
+                                 (2270, 6144), (3, 40960), (12000, 5120), (2, 128 * 131), (4, 65536),
+                                 (700, 8192), (33, 12288), (5, 128 * 71)])
 def test_quant_int8_h128_bitexact(orc, staging, M, K):
     x = special_rows(S.activation(0, f"t/q8/{M}x{K}", M, K))
     q, s = clef.quant_act(bf16_dev(x), "int8_h128")

@@ -10,14 +10,15 @@
 // CTA per row with direct 16-byte loads.
 //
 // In both, each thread owns one 32-element chunk of the row (two chunks for
-// rows longer than 32768 in the fallback): four 16-byte pieces of bf16,
-// widened to fp32 in registers.  A 128-block of the row spans four neighbouring lanes,
-// so the Walsh-Hadamard butterfly runs its strides 1..16 inside a thread and
-// strides 32 and 64 as lane exchanges (xor 1, xor 2), in the fixed order
+// rows longer than 32768 in the fallback; the staged kernel gives rows of
+// 8,192 to 12,288 elements 64 per thread): 16-byte pieces of bf16, widened
+// to fp32 in registers.  A 128-block of the row spans four (two) neighbouring
+// lanes, so the Walsh-Hadamard butterfly runs its strides 1..16 (1..32) inside
+// a thread and the rest as lane exchanges (xor 1, xor 2), in the fixed order
 // 1, 2, 4, ..., 64 with explicitly rounded fp32 add/sub (no contraction),
 // then one multiply by fp32(1/sqrt(128)).  The row's absmax is a warp-shuffle
-// max plus one shared-memory step; codes are written as two 16-byte stores
-// per chunk.  Reads 2 B and writes 1 B per element, plus a 4 B scale per row.
+// max plus one shared-memory step; codes are written as 16-byte stores.
+// Reads 2 B and writes 1 B per element, plus a 4 B scale per row.
 //
 // What it computes follows the "CLEF Calibrated INT8 ConvRot" model card
 // (note under the latency table: activations are rotated and quantized to
@@ -121,6 +122,52 @@ __device__ __forceinline__ void wht128_lanes(float (&v)[32], int lane) {
     }
 }
 
+// The same rotation on E = 2 NP consecutive values (E = 32 or 64) held as NP
+// natural pairs p[i] = (v[2i], v[2i+1]) (the load's bf16 order); a 128-block
+// spans 128 / E neighbouring lanes.  Stride 1 pairs the two halves of each
+// pair, strides 2 .. E/2 pair p[i] with p[i + h/2] lane-wise, and the strides
+// E .. 64 exchange whole pairs with lanes xor 1, xor 2.  Each output is the
+// same fp32 add or subtract of the same two values in the same stage order as
+// wht128_lanes.
+template <int NP>
+__device__ __forceinline__ void wht128_pairs(uint64_t (&p)[NP], int lane) {
+    static_assert(NP == 16 || NP == 32, "32 or 64 values per thread");
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {   // stride 1
+        float a, b;
+        unf2(p[i], a, b);
+        p[i] = f2(__fadd_rn(a, b), __fsub_rn(a, b));
+    }
+#pragma unroll
+    for (int hp = 1; hp < NP; hp <<= 1) {   // strides 2 .. E/2
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+            if ((k & hp) == 0) {
+                const uint64_t a = p[k], b = p[k + hp];
+                p[k] = add2(a, b);
+                p[k + hp] = sub2(a, b);
+            }
+        }
+    }
+#pragma unroll
+    for (int s = 1; 2 * NP * s <= 64; s <<= 1) {   // strides E .. 64 across lanes
+        const float sg = (lane & s) ? -1.0f : 1.0f;
+        const uint64_t sgn = f2(sg, sg);
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+            float a, b;
+            unf2(p[k], a, b);
+            const float oa = __shfl_xor_sync(kFull, a, s);
+            const float ob = __shfl_xor_sync(kFull, b, s);
+            p[k] = fma2(sgn, p[k], f2(oa, ob));
+        }
+    }
+    const float c = hadamard_c();
+    const uint64_t c2 = f2(c, c);
+#pragma unroll
+    for (int k = 0; k < NP; ++k) p[k] = mul2(p[k], c2);
+}
+
 __device__ __forceinline__ void load_chunk(const uint16_t *p, float (&v)[32]) {
     const uint4 *p4 = reinterpret_cast<const uint4 *>(p);
 #pragma unroll
@@ -178,6 +225,41 @@ __device__ __forceinline__ void store_codes(const float (&v)[32], float r, bool 
                 w[i] = 0u;
             } else {
                 const float *u = &v[4 * i];
+                w[i] = e4m3x2(__fmul_rn(u[0], r), __fmul_rn(u[1], r)) |
+                       (e4m3x2(__fmul_rn(u[2], r), __fmul_rn(u[3], r)) << 16);
+            }
+        }
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(dst8);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Codes of 32 values held as natural pairs (as store_codes).
+template <bool kInt8, bool kClamp = false>
+__device__ __forceinline__ void store_codes_pairs(const uint64_t *p, float r, bool zero_row,
+                                                  uint8_t *dst8) {
+    uint32_t w[8];
+    if (kInt8) {
+        const uint64_t r2 = f2(r, r);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float u[4];
+            unf2(mul2(p[2 * i], r2), u[0], u[1]);
+            unf2(mul2(p[2 * i + 1], r2), u[2], u[3]);
+            w[i] = pack_s8x4(__float2int_rn(u[0]), __float2int_rn(u[1]), __float2int_rn(u[2]),
+                             __float2int_rn(u[3]));
+            if (kClamp) w[i] = __vmaxs4(w[i], 0x81818181u);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (zero_row) {
+                w[i] = 0u;
+            } else {
+                float u[4];
+                unf2(p[2 * i], u[0], u[1]);
+                unf2(p[2 * i + 1], u[2], u[3]);
                 w[i] = e4m3x2(__fmul_rn(u[0], r), __fmul_rn(u[1], r)) |
                        (e4m3x2(__fmul_rn(u[2], r), __fmul_rn(u[3], r)) << 16);
             }
@@ -277,7 +359,7 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m
 // One block barrier per row: it publishes the warps' absmax (double-buffered
 // by row parity) and certifies that every thread has read the slot, after
 // which thread 0 refills it with the row nslot iterations ahead.
-template <int MODE, int MAXT, int MINB>
+template <int MODE, int E, int MAXT, int MINB>
 __global__ void __launch_bounds__(MAXT, MINB)
 quant_staged_kernel(const __grid_constant__ CUtensorMap tmx, int M, int K, int nslot,
                     uint32_t slot_stride, int nbox, int box_rows, uint8_t *__restrict__ q,
@@ -294,7 +376,7 @@ quant_staged_kernel(const __grid_constant__ CUtensorMap tmx, int M, int K, int n
     uint8_t *ring = dyn + (((base + 1023u) & ~1023u) - base);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nw = (int)(blockDim.x >> 5);
-    const int nchunk = K >> 5;
+    const int nchunk = K / E;
     const uint32_t row_bytes = (uint32_t)K * 2u;
 
     if (tid == 0) {
@@ -322,41 +404,48 @@ quant_staged_kernel(const __grid_constant__ CUtensorMap tmx, int M, int K, int n
         }
     }
 
+    // E = 32: thread t reads half t & 1 of line t >> 1 (four 16-byte units);
+    // E = 64: the whole line t (eight units).  Either way a quarter-warp's
+    // eight reads of one step hit eight different bank groups.
+    constexpr int kU = E / 8;   // 16-byte units per thread
     const bool active = tid < nchunk;
-    const uint32_t line = (uint32_t)(tid >> 1);
-    uint32_t off[4];
+    const uint32_t line = (uint32_t)(E == 64 ? tid : tid >> 1);
+    uint32_t off[kU];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) off[j] = line * 128u + (((uint32_t)((tid & 1) * 4 + j) ^ (line & 7u)) << 4);
+    for (int j = 0; j < kU; ++j)
+        off[j] = line * 128u + (((uint32_t)((E == 64 ? 0 : (tid & 1) * 4) + j) ^ (line & 7u)) << 4);
 
     int it = 0;
     for (int m = (int)blockIdx.x; m < M; m += (int)gridDim.x, ++it) {
         const int slot = it % nslot;
         mbar_wait(&full[slot], (uint32_t)(it / nslot) & 1u, w, kSiteQuantFull);
-        float v[32];
+        uint64_t p[E / 2];   // the thread's E values as natural pairs (v[2i], v[2i+1])
         if (active) {
             const uint32_t src = smem_u32(ring) + (uint32_t)slot * slot_stride;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < kU; ++j) {
                 uint32_t a0, a1, a2, a3;
                 asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                              : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(src + off[j]));
                 const uint32_t ws[4] = {a0, a1, a2, a3};
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    v[8 * j + 2 * k] = __uint_as_float(ws[k] << 16);
-                    v[8 * j + 2 * k + 1] = __uint_as_float(ws[k] & 0xFFFF0000u);
-                }
+                for (int k = 0; k < 4; ++k)
+                    p[4 * j + k] = f2(__uint_as_float(ws[k] << 16), __uint_as_float(ws[k] & 0xFFFF0000u));
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+            for (int j = 0; j < E / 2; ++j) p[j] = 0ull;
         }
-        // whole 128-blocks are active or inactive together (nchunk % 4 == 0
-        // in the rotated modes), and every lane of the warp exists
-        if (kRotate) wht128_lanes(v, lane);
+        // whole 128-blocks are active or inactive together (K % 128 == 0 in
+        // the rotated modes), and every lane of the warp exists
+        if (kRotate) wht128_pairs<E / 2>(p, lane);
         float amax = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+        for (int j = 0; j < E / 2; ++j) {
+            float a, b;
+            unf2(p[j], a, b);
+            amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
+        }
 #pragma unroll
         for (int sh = 16; sh > 0; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, sh));
         if (lane == 0) red[it & 1][warp] = amax;
@@ -369,8 +458,19 @@ quant_staged_kernel(const __grid_constant__ CUtensorMap tmx, int M, int K, int n
                 issue(slot, mn);
             }
         }
-        amax = red[it & 1][0];
-        for (int k = 1; k < nw; ++k) amax = fmaxf(amax, red[it & 1][k]);
+        // the nw partial maxima: lane l reads partial l and five shuffles
+        // combine them (24,032 rows: K = 17408, 17 warps, 269.3 -> 261.6 us;
+        // 6144, 6 warps, 90.4 -> 88.1; 5120, 5 warps, 78.8 -> 77.8), or, for
+        // 64 values per thread or two warps at most, each thread reads all
+        // (K = 12288 with 64 per thread: 172.0 against 176.1 us)
+        if (E == 32 && nw > 2) {
+            amax = lane < nw ? red[it & 1][lane] : 0.0f;
+#pragma unroll
+            for (int sh = 16; sh > 0; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, sh));
+        } else {
+            amax = red[it & 1][0];
+            for (int k = 1; k < nw; ++k) amax = fmaxf(amax, red[it & 1][k]);
+        }
 
         const float qmax = kInt8 ? 127.0f : 448.0f;
         const bool stat = static_r > 0.0f;   // static scale: the row's amax is not used
@@ -378,8 +478,12 @@ quant_staged_kernel(const __grid_constant__ CUtensorMap tmx, int M, int K, int n
         const float r = stat ? static_r : (zero_row ? 0.0f : __fdiv_rn(qmax, amax));
         if (tid == 0) scale[m] = stat ? static_s : (zero_row ? 0.0f : __fdiv_rn(amax, qmax));
         if (active) {
-            if (stat) store_codes<kInt8, kInt8>(v, r, false, q + (int64_t)m * K + 32 * tid);
-            else store_codes<kInt8>(v, r, zero_row, q + (int64_t)m * K + 32 * tid);
+            uint8_t *dst = q + (int64_t)m * K + E * tid;
+#pragma unroll
+            for (int g = 0; g < E / 32; ++g) {
+                if (stat) store_codes_pairs<kInt8, kInt8>(p + 16 * g, r, false, dst + 32 * g);
+                else store_codes_pairs<kInt8>(p + 16 * g, r, zero_row, dst + 32 * g);
+            }
         }
     }
     if (abort_flag && tid == 0) {
@@ -407,7 +511,9 @@ struct StagedPlan {
     uint32_t slot_stride, smem;
 };
 
-bool staged_plan(int64_t K, StagedPlan &p) {
+// E: elements per thread (32, or 64 for long rows: fewer warps meet at each
+// row's barrier and one lane exchange of the rotation stays in registers)
+bool staged_plan(int64_t K, int E, StagedPlan &p) {
     if (K % 64 != 0 || K / 32 > 1024) return false;
     const int lines = (int)(K / 64);
     int nbox = (lines + 255) / 256;
@@ -416,11 +522,12 @@ bool staged_plan(int64_t K, StagedPlan &p) {
     if (nbox > 8) return false;
     p.nbox = nbox;
     p.box_rows = lines / nbox;
-    p.threads = (int)((K / 32 + 31) / 32 * 32);
+    p.threads = (int)((K / E + 31) / 32 * 32);
     p.slot_stride = (uint32_t)((K * 2 + 1023) / 1024 * 1024);
-    // about 1,152 threads per SM (registers for 56 per thread), 220 KB of ring
+    // about 1,152 threads per SM with 32 values each (registers for 56 per
+    // thread) or 640 with 64 (about 100), and 220 KB of ring
     const uint32_t budget = 220u * 1024u;
-    int want = 1152 / p.threads;
+    int want = (E == 64 ? 640 : 1152) / p.threads;
     want = want < 1 ? 1 : (want > 8 ? 8 : want);
     for (int P = want; P >= 1; --P) {
         const uint32_t per = budget / (uint32_t)P;
@@ -435,7 +542,7 @@ bool staged_plan(int64_t K, StagedPlan &p) {
     return false;
 }
 
-template <int MODE, int MAXT, int MINB>
+template <int MODE, int E, int MAXT, int MINB>
 cudaError_t launch_staged(const StagedPlan &p, const uint16_t *x, int64_t M, int64_t K,
                           int64_t ldx, uint8_t *q, float *scale, const QuantEnv &env,
                           cudaStream_t st) {
@@ -446,10 +553,11 @@ cudaError_t launch_staged(const StagedPlan &p, const uint16_t *x, int64_t M, int
     if (internal_make_tmap_nd(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, dims, strides, box,
                               CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    auto kern = quant_staged_kernel<MODE, MAXT, MINB>;
+    auto kern = quant_staged_kernel<MODE, E, MAXT, MINB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
     if (e != cudaSuccess) return e;
-    // resident CTAs per SM, cached per row length (K / 64 <= 512 here)
+    // resident CTAs per SM, cached per row length (K / 64 <= 512 here; one
+    // table per instantiation)
     static int resident_by_lines[513] = {0};
     int resident = resident_by_lines[K / 64];
     if (resident == 0) {
@@ -473,9 +581,16 @@ cudaError_t launch_mode(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, ui
     StagedPlan p;
     // a few rows per SM or fewer: the per-row kernel starts sooner
     const bool want = env.staging == 2 || (env.staging == 1 && M >= 8 * (int64_t)env.num_sms);
-    if (want && staged_plan(K, p)) {
-        if (p.threads <= 576) return launch_staged<MODE, 576, 2>(p, x, M, K, ldx, q, scale, env, st);
-        return launch_staged<MODE, 1024, 1>(p, x, M, K, ldx, q, scale, env, st);
+    if (want) {
+        // rows of 8,192 to 12,288 elements: 64 values per thread (24,032 rows:
+        // K = 8192 116.7 -> 106.5 us, 12288 174.1 -> 172.0 us; at K = 17408,
+        // with two CTAs of 9 warps per SM, 268.3 -> 282.6 us, so 32 there)
+        if (K >= 8192 && K <= 12288 && staged_plan(K, 64, p))
+            return launch_staged<MODE, 64, 320, 2>(p, x, M, K, ldx, q, scale, env, st);
+        if (staged_plan(K, 32, p)) {
+            if (p.threads <= 576) return launch_staged<MODE, 32, 576, 2>(p, x, M, K, ldx, q, scale, env, st);
+            return launch_staged<MODE, 32, 1024, 1>(p, x, M, K, ldx, q, scale, env, st);
+        }
     }
     const int64_t nchunk = K / 32;
     if (nchunk <= 576) {
