@@ -34,6 +34,7 @@ import clef_synth as S  # noqa: E402
 
 METRIC = "W8A8 linear TOPS & % of GB300 dense INT8/FP8 peak; quantizer GB/s vs HBM"
 L2_FLUSH_BYTES = 256 << 20
+CPU_SAMPLE_S = 10.0   # target length of the timed oracle sample
 
 
 def parse():
@@ -433,16 +434,20 @@ def main():
     if not args.no_e2e:
         line["e2e"] = e2e(args, layer, acts, acts_np, cfg, dev, stream, world, torch)
 
-    # ---- CPU oracle on a bounded sample (rank 0, N = 1)
+    # ---- CPU oracle on a bounded sample (rank 0, N = 1): a probe of two rows
+    # per host thread sizes a sample of about CPU_SAMPLE_S seconds
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = cpu_threads()
-        rows = sample_rows(cfg, 12 * threads)
         qw = oracle_weights(cfg, weights_np, threads)
+        probe = sample_rows(cfg, 2 * threads)
+        dt0, _ = oracle_sample(cfg, acts_np, weights_np, qw, lora_np, probe, threads)
+        n = int(min(cfg.M, max(len(probe), len(probe) * CPU_SAMPLE_S / max(dt0, 1e-3))))
+        rows = sample_rows(cfg, n)
         dt, ops = oracle_sample(cfg, acts_np, weights_np, qw, lora_np, rows, threads)
         line["cpu_baseline"] = {"value": ops / dt / 1e12, "unit": "TOPS", "cores": threads,
                                 "kind": "oracle",
                                 "sample": f"{len(rows)} of {cfg.M} token rows through every projection "
-                                          f"of {cfg.name} ({dt:.1f} s)"}
+                                          f"of {cfg.name} ({dt:.1f} s on {threads} threads)"}
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
