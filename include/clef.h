@@ -267,23 +267,26 @@ int clef_lora_add_noalloc(const void *x, int64_t ldx, const void *A, const void 
  * clef_gemm_workspace_bytes / clef_bind_workspace -- optional scratch that
  * lets the INT8 GEMMs (clef_w8a8_linear, clef_w8a8_gemm_s32; M > 128) split
  * tiles across SMs when the last wave of whole 256 x 256 tiles would leave
- * more than 8% of the CTA pairs idle ("stream-K": the tiles' 1024-deep K
- * chunks are dealt evenly to the pairs, and the pieces of a tile meet as
- * exact int32 partial sums, so the bytes of every output equal those of an
- * unsplit launch).  The GEMM time follows the number of tile waves (1502 x
- * 5120 x 17408 and 1502 x 6400 x 17408 take the same time unsplit), so a
- * shape with a nearly empty last wave gains up to the idle fraction.
+ * more than 8% of the CTA pairs idle ("stream-K": the whole waves run as
+ * whole tiles, the remaining tiles' K is dealt to all pairs in even runs of
+ * at least 1024, and the pieces of a tile meet as exact int32 partial sums,
+ * so the bytes of every output equal those of an unsplit launch).  The GEMM
+ * time follows the number of tile waves (1502 x 5120 x 17408 and 1502 x 6400
+ * x 17408 take the same time unsplit), so a shape with a partly empty last
+ * wave gains up to the idle fraction.  Launches of less than one wave, the
+ * gate/up SwiGLU call and the FP8 calls (whose fp32 sums would change with
+ * the split) never split.
  * clef_gemm_workspace_bytes: the size needed on the current device (about
  * 38 MB on a 152-SM GB300), written to *bytes.
  * clef_bind_workspace: binds a caller-owned device buffer of that size to
  * `stream` on the current device (ws = NULL unbinds); INT8 GEMM calls on that
  * stream may then use it, calls on unbound streams never split.  The buffer
- * must be zero-filled when bound; every launch leaves it zeroed again (after
- * a CLEF_ERR_TIMEOUT, refill it with zeros before further use).  Launches
- * that use one buffer must not run concurrently: bind a separate buffer to
- * each stream whose work may overlap.  Binding is host bookkeeping only (no
- * CUDA call), so it may be done while the stream is being captured into a
- * graph; the graph then keeps the buffer's address.
+ * must be zero-filled when bound; every launch leaves its counter block
+ * zeroed again (after a CLEF_ERR_TIMEOUT, refill the buffer with zeros before
+ * further use).  Launches that use one buffer must not run concurrently: bind
+ * a separate buffer to each stream whose work may overlap.  Binding is host
+ * bookkeeping (no stream operation), so it may be done while the stream is
+ * being captured into a graph; the graph then keeps the buffer's address.
  * Requirements: ws 16-byte aligned and bytes >= the counter block (the
  * workspace is used for splitting only when bytes >= the size returned);
  * at most 256 bindings.
