@@ -410,8 +410,8 @@ struct Gemm {
     };
     static __device__ __forceinline__ int sk_of(const Ctx &c) { return C::kStreamK ? c.bar->sk : 0; }
     static __device__ __forceinline__ int sk_tail0(const Ctx &c) { return C::kStreamK ? c.bar->sk_tail0 : 0; }
-    // (32-bit arithmetic suffices: fewer than 256 slots share fewer than 256
-    // tiles of at most 1024 k-blocks)
+    // (32-bit arithmetic: the launcher splits only when slots x remaining
+    // k-blocks stays below 2^32)
     static __device__ __forceinline__ int sk_bound(const Ctx &c, int p) {
         return (int)((uint32_t)p * (uint32_t)((c.num_tiles - sk_tail0(c)) * c.nkb) / (uint32_t)sk_of(c));
     }
@@ -1387,7 +1387,10 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
             const int tail0 = tiles >= max_pairs ? (tiles / max_pairs) * max_pairs : 0;
             const int64_t rest = (int64_t)(tiles - tail0) * nkb;
             const int p2 = (int)std::min<int64_t>(max_pairs, rest / C::kChunkKBlocks);
-            if (fill < 0.92 && tail0 > 0 && p2 > tiles - tail0 && tiles <= kSkMaxTiles &&
+            // (the device splits runs with 32-bit products of a slot index and
+            // the remaining k-block count)
+            const bool fits32 = rest * (int64_t)max_pairs < ((int64_t)1 << 32);
+            if (fill < 0.92 && tail0 > 0 && p2 > tiles - tail0 && tiles <= kSkMaxTiles && fits32 &&
                 args.sk_ws_bytes >= (int64_t)max_pairs * kSkBytesPerPair) {
                 la.sk = p2;
                 la.sk_tail0 = tail0;
