@@ -128,6 +128,7 @@ extern "C" int clef_lora_add_noalloc(const void *x, int64_t ldx, const void *A, 
     a2.K = (int)r_pad;
     a2.out = y;
     a2.ldo = ldy;
+    a2.n_fastest = 1;
     a2.status = status;
     a2.wait_limit_ns = 1000000000ull;
     return launch_gemm(kOpBF16, kEpiAddBF16, 128,
