@@ -10,8 +10,10 @@ fused SwiGLU epilogue, then down 17408 -> 5120).
 Printed (rank 0, one JSON line): whole-step W8A8 GEMM throughput in TOPS
 (2*M*N*K per projection, counted once), the end-to-end figure through the
 C ABI with host buffers, the roofline of the dominant kernel from CUDA events
-recorded on its stream, the quantizer's GB/s, clocks sampled during the timed
-region, and the CPU oracle timed on a bounded sample on the host cores.
+recorded on its stream (in a separate pass of up to 100 steps with an event
+pair around every launch; the timed steps carry only the step's own pair),
+the quantizer's GB/s, clocks sampled during the timed region, and the CPU
+oracle timed on a bounded sample on the host cores.
 ``--impl reference`` times that oracle as the reference arm instead.
 """
 from __future__ import annotations
@@ -35,6 +37,7 @@ import clef_synth as S  # noqa: E402
 METRIC = "W8A8 linear TOPS & % of GB300 dense INT8/FP8 peak; quantizer GB/s vs HBM"
 L2_FLUSH_BYTES = 256 << 20
 CPU_SAMPLE_S = 10.0   # target length of the timed oracle sample
+INSTRUMENTED_STEPS = 100   # steps of the per-kernel timing pass
 
 
 def parse():
@@ -326,7 +329,7 @@ def main():
         s0 = torch.cuda.Event(enable_timing=True)
         s1 = torch.cuda.Event(enable_timing=True)
         s0.record(stream)
-        layer.step(acts, events=events)
+        layer.step(acts)
         s1.record(stream)
         step_ev.append((s0, s1))
     torch.cuda.synchronize(dev)
@@ -337,6 +340,13 @@ def main():
     status = clef.poll_status()
     if status:
         raise RuntimeError(f"device status word reported {status}")
+    # per-kernel times from a separate pass with an event pair around every
+    # launch (the events themselves cost about 2 us each, so the timed steps
+    # above carry only the step's own pair)
+    for _ in range(min(args.steps, INSTRUMENTED_STEPS)):
+        flush.zero_()
+        layer.step(acts, events=events)
+    torch.cuda.synchronize(dev)
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     t_sum = max_over_ranks(sum(step_ms) / 1e3, world, dist, dev)
     ops_step = cfg.gemm_ops()
