@@ -14,8 +14,15 @@
 //           single mode (about 128 B per clock per SM covers TMA writes, thread
 //           accesses and tensor-core operand reads together).
 //
-// Warp roles (one CTA per SM, persistent over tiles in M-fastest order so that
-// concurrently running CTAs share weight tiles in L2):
+// Schedule: one CTA (or pair) per SM, persistent over tiles slot, slot +
+// nslots, ... in M-fastest order, so that concurrently running CTAs share
+// weight tiles in L2 (N-fastest for the LoRA launches, whose large operand is
+// the activation or y).  INT8 stream-K (a caller-bound workspace, pair mode,
+// not SwiGLU): when the last wave of tiles would leave pairs idle, the whole
+// waves run as above and the remaining tiles' k-blocks are dealt to the pairs
+// in even runs; the pieces of a tile meet as exact int32 partial sums.
+//
+// Warp roles:
 //   warp 0     TMA producer (one elected lane)
 //   warp 1     TMEM allocator and MMA issuer (one elected lane; in pair mode the
 //              leader's only)
@@ -30,9 +37,10 @@
 // fp16, every product (<= 16129) is exact in fp32, and a sum of at most 1024
 // such products stays below 2^24, so every partial sum the tensor core forms
 // is an exactly representable integer.  The K loop is therefore cut into
-// chunks of 1024; each chunk's fp32 accumulator is converted to int32 by the
-// epilogue warps (exact) and added to int32 totals held in registers.  The
-// result is the exact int32 accumulator, whatever the summation order.
+// chunks of at most 1024; each chunk's fp32 accumulator is converted to int32
+// by the epilogue warps (exact) and added to int32 totals held in registers.
+// The result is the exact int32 accumulator, whatever the summation order or
+// split.
 //
 // Sources: "CLEF Calibrated INT8 ConvRot" model card, Benefits (kernels fuse
 // calibrated scales, biases and MLP SwiGLU); "Loading CLEF INT8" usage
