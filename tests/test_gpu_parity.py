@@ -457,6 +457,78 @@ def test_row_invariance_int8_fp8_lora():
     assert torch.equal(whole.view(torch.int16), part.view(torch.int16)), "lora"
 
 
+def _same_rows(whole, part, what):
+    assert torch.equal(whole.view(torch.int16) if whole.dtype == torch.bfloat16 else whole,
+                       part.view(torch.int16) if part.dtype == torch.bfloat16 else part), what
+
+
+def test_row_invariance_other_kernels():
+    """The rest of the path: the quantizer (all modes), the fused gate/up SwiGLU
+    (INT8, FP8), the LoRA gate/up + SwiGLU call and the stacked LoRA shrink and
+    expand, 600 rows at once against pieces of 1..255 rows."""
+    M, N, K, r = 600, 256, 1024, 64
+    x = bf16_dev(S.activation(0, "t/inv2/x", M, K))
+    for mode in ("int8_h128", "fp8", "fp8_h128"):
+        q, sc = clef.quant_act(x, mode)
+        qp, sp = torch.empty_like(q), torch.empty_like(sc)
+        for a, c in pieces(M):
+            clef.quant_act(x[a:c], mode, q=qp[a:c], scale=sp[a:c])
+        assert torch.equal(q, qp) and torch.equal(sc, sp), mode
+    w = bf16_dev(S.weight(0, "t/inv2/w", 2 * N, K))
+    b = bf16_dev(S.bias(0, "t/inv2/b", 2 * N))
+    for mode, gu in (("int8_h128", clef.w8a8_gateup_swiglu), ("fp8", clef.fp8_gateup_swiglu)):
+        qx, sx = clef.quant_act(x, mode)
+        qw, sw = clef.quant_act(w, mode)
+        whole = gu(qx, sx, qw, sw, b)
+        part = torch.empty_like(whole)
+        for a, c in pieces(M):
+            gu(qx[a:c], sx[a:c], qw, sw, b, h=part[a:c])
+        _same_rows(whole, part, mode + " gate/up")
+    Ag, Bg = (bf16_dev(v) for v in S.lora_pair(0, "t/inv2/g", r, K, N))
+    Au, Bu = (bf16_dev(v) for v in S.lora_pair(0, "t/inv2/u", r, K, N))
+    ygu = bf16_dev(S.normal_bf16(0, "t/inv2/ygu", (M, 2 * N)))
+    whole = clef.lora_gateup_swiglu(x, Ag, Bg, Au, Bu, ygu)
+    part = torch.empty_like(whole)
+    for a, c in pieces(M):
+        clef.lora_gateup_swiglu(x[a:c], Ag, Bg, Au, Bu, ygu[a:c], h=part[a:c])
+    _same_rows(whole, part, "lora gate/up")
+    A_cat = torch.cat([Ag, Au], dim=0)
+    t_whole = clef.lora_shrink(x, A_cat)
+    t_part = torch.empty_like(t_whole)
+    for a, c in pieces(M):
+        clef.lora_shrink(x[a:c], A_cat, t=t_part[a:c])
+    _same_rows(t_whole, t_part, "lora shrink")
+    y0 = bf16_dev(S.normal_bf16(0, "t/inv2/y", (M, N)))
+    y_whole, y_part = y0.clone(), y0.clone()
+    clef.lora_expand_add(t_whole[:, r:], Bu, y_whole)
+    for a, c in pieces(M):
+        clef.lora_expand_add(t_whole[a:c, r:], Bu, y_part[a:c])
+    _same_rows(y_whole, y_part, "lora expand")
+
+
+def test_row_invariance_with_stream_k():
+    """1,502 rows of the down projection at once split their last 44 tiles
+    across all SMs (stream-K); pieces of 1..255 rows never split; the bytes
+    agree row for row."""
+    M, N, K = 1502, 5120, 17408
+    rng = np.random.default_rng(21)
+    qx = dev(rng.integers(-127, 128, (M, K)).astype(np.int8))
+    qw = dev(rng.integers(-127, 128, (N, K)).astype(np.int8))
+    sx = torch.tensor(rng.random(M, dtype=np.float32) * 1e-3, device="cuda")
+    sw = torch.tensor(rng.random(N, dtype=np.float32) * 1e-3, device="cuda")
+    b = torch.tensor(rng.standard_normal(N, dtype=np.float32), device="cuda").to(torch.bfloat16)
+    ws = torch.zeros(clef.gemm_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    clef.bind_workspace(ws)
+    try:
+        whole = clef.w8a8_linear(qx, sx, qw, sw, b)
+        part = torch.empty_like(whole)
+        for a, c in pieces(M):
+            clef.w8a8_linear(qx[a:c], sx[a:c], qw, sw, b, y=part[a:c])
+    finally:
+        clef.bind_workspace(None)
+    _same_rows(whole, part, "int8 stream-K")
+
+
 def test_two_streams_and_repeats_are_deterministic():
     M, N, K = 1024, 2048, 4096
     x = bf16_dev(S.activation(0, "t/det/x", M, K))
