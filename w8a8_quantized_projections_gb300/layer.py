@@ -30,6 +30,7 @@ own column block of t (the same bytes as a separate LoRA add per adapter).
 """
 from __future__ import annotations
 
+from types import SimpleNamespace
 from typing import Dict, Optional, Tuple
 
 import torch
@@ -274,11 +275,20 @@ class QuantizedLayer:
             self.step(acts)
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
+        self._unbind()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             self.step(acts)
+            # the graph keeps the workspace's address; drop the host binding of
+            # the capture stream so no later user of that stream inherits it
+            self._unbind()
         self.graph = graph
         return graph
+
+    def _unbind(self):
+        if self.ws is not None and self._ws_stream is not None:
+            bind_workspace(None, SimpleNamespace(cuda_stream=self._ws_stream))
+            self._ws_stream = None
 
     def replay(self) -> Dict[str, torch.Tensor]:
         self.graph.replay()
