@@ -273,9 +273,10 @@ int clef_lora_add_noalloc(const void *x, int64_t ldx, const void *A, const void 
  * so the bytes of every output equal those of an unsplit launch).  The GEMM
  * time follows the number of tile waves (1502 x 5120 x 17408 and 1502 x 6400
  * x 17408 take the same time unsplit), so a shape with a partly empty last
- * wave gains up to the idle fraction.  Launches of less than one wave, the
- * gate/up SwiGLU call and the FP8 calls (whose fp32 sums would change with
- * the split) never split.
+ * wave gains up to the idle fraction.  A launch of less than one wave is
+ * split only when its tiles would keep under an eighth of the pairs busy
+ * (small M, long K); the gate/up SwiGLU call and the FP8 calls (whose fp32
+ * sums would change with the split) never split.
  * clef_gemm_workspace_bytes: the size needed on the current device (about
  * 38 MB on a 152-SM GB300), written to *bytes.
  * clef_bind_workspace: binds a caller-owned device buffer of that size to

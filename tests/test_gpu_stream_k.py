@@ -35,10 +35,12 @@ def bound_workspace(stream=None):
 # (M, N, K) on 76 CTA pairs: 120 tiles (one whole wave, 44 tiles split); K
 # of 273 k-blocks (runs end off the 16-k-block chunk grid); 88 tiles with 12
 # split into two 16-k-block runs each; 180 tiles (two whole waves, 28 split);
-# 120 tiles whose last column tile is partial (N = 5000); 48 tiles (under one
-# wave: not split); 76 tiles (a full wave: not split)
+# 120 tiles whose last column tile is partial (N = 5000); 8 and 4 tiles (under
+# an eighth of a wave: every tile split in runs of 8 or more k-blocks); 48 tiles
+# (under one wave: not split); 76 tiles (a full wave: not split)
 SHAPES = [(1502, 5120, 17408), (1502, 5120, 17472), (1024, 5632, 2048), (2270, 5120, 6144),
-          (1502, 5000, 5120), (300, 6144, 5120), (1024, 4864, 1024)]
+          (1502, 5000, 5120), (200, 2048, 8192), (130, 1024, 4096), (300, 6144, 5120),
+          (1024, 4864, 1024)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)

@@ -1388,17 +1388,24 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
             // dealt as k-block runs of at least 16 k-blocks to up to every
             // pair, and the workspace must hold every pair's two pieces.  A
             // launch of less than one wave stays unsplit (300 x 6144 x 5120:
-            // 53.5 us unsplit, 55.6 us with every tile split).
+            // 53.5 us unsplit, 55.6 us with every tile split; 298 x 2048 x 2048
+            // 28.4 against 31.2 us) unless it keeps under an eighth of the
+            // pairs busy (200 x 2048 x 8192, 8 tiles: 59.4 -> 45.2 us; 130 x
+            // 1024 x 4096, 4 tiles: 39.4 -> 35.1 us).
             const int nkb = (args.K + 63) / 64;
             const int64_t waves = (tiles + max_pairs - 1) / max_pairs;
             const double fill = (double)tiles / (double)(waves * max_pairs);
             const int tail0 = tiles >= max_pairs ? (tiles / max_pairs) * max_pairs : 0;
             const int64_t rest = (int64_t)(tiles - tail0) * nkb;
-            const int p2 = (int)std::min<int64_t>(max_pairs, rest / C::kChunkKBlocks);
+            // runs of at least 16 k-blocks, or 8 when a launch of under an
+            // eighth of a wave is split (small M, long K)
+            const int minrun = tail0 > 0 ? C::kChunkKBlocks : 8;
+            const int p2 = (int)std::min<int64_t>(max_pairs, rest / minrun);
             // (the device splits runs with 32-bit products of a slot index and
             // the remaining k-block count)
             const bool fits32 = rest * (int64_t)max_pairs < ((int64_t)1 << 32);
-            if (fill < 0.92 && tail0 > 0 && p2 > tiles - tail0 && tiles <= kSkMaxTiles && fits32 &&
+            if (fill < 0.92 && (tail0 > 0 || 8 * tiles <= max_pairs) && p2 > tiles - tail0 &&
+                tiles <= kSkMaxTiles && fits32 &&
                 args.sk_ws_bytes >= (int64_t)max_pairs * kSkBytesPerPair) {
                 la.sk = p2;
                 la.sk_tail0 = tail0;
