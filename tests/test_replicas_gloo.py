@@ -43,7 +43,9 @@ def _rank(rank, world, port, out):
 def test_two_replicas_on_gloo():
     world = 2
     port = _free_port()
-    with mp.Manager() as m:
+    # every process of the test is spawned (the Manager's too): a fork after
+    # the GPU tests of the same session have started threads could deadlock
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.start_processes(_rank, args=(world, port, out), nprocs=world, start_method="spawn")
         res = dict(out)
