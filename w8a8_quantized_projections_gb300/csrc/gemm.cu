@@ -1031,6 +1031,25 @@ struct Gemm {
         }
     }
 
+    // The ring of y tiles (one thread): at the CTA's first tile, load its first
+    // kYBufs - 1 tiles; then, each tile, load the one kYBufs - 1 ahead into the
+    // buffer whose last tenant (tile yiter - 1) has had its store read out.
+    template <typename Load>
+    static __device__ __forceinline__ void y_ring_prefetch(const Ctx &c, int t, int yiter, int &yloads,
+                                                           Load load) {
+        if (yiter == 0)
+            for (int i = 0; i < C::kYBufs - 1 && t + i * c.nslots < c.num_tiles; ++i) {
+                load(t + i * c.nslots, i);
+                ++yloads;
+            }
+        const int tn = t + (C::kYBufs - 1) * c.nslots;
+        if (tn < c.num_tiles) {
+            bulk_wait_read_all();
+            load(tn, (yiter + C::kYBufs - 1) % C::kYBufs);
+            ++yloads;
+        }
+    }
+
     // yiter: y tiles finished; yloads: y tile loads issued (y += acc only).
     static __device__ void epilogue_tiles(const Ctx &c, const GemmArgs &a, int &yiter, int &yloads) {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1069,22 +1088,12 @@ struct Gemm {
                 if (sg.part < 0 || sk_combine(c, a, sg, e, lane, tot))
                     finish_row(a, row, row_ok, nb, half, tot);
             } else if constexpr (C::kLoraSwi) {
-                // base g|u tiles by TMA one tile ahead, h computed in place over the
-                // gate columns, stored by TMA after a bounded epilogue rendezvous
+                // base g|u tiles by TMA through the ring (kYBufs - 1 tiles ahead),
+                // h computed in place over the gate columns, stored by TMA after a
+                // bounded epilogue rendezvous
                 const int b = yiter % C::kYBufs;
-                if (e == 0 && lane == 0) {
-                    if (yiter == 0)
-                        for (int i = 0; i < C::kYBufs - 1 && t + i * c.nslots < c.num_tiles; ++i) {
-                            gu_tile_load(c, a, t + i * c.nslots, i);
-                            ++yloads;
-                        }
-                    const int tn = t + (C::kYBufs - 1) * c.nslots;
-                    if (tn < c.num_tiles) {
-                        bulk_wait_read_all();   // tile yiter - 1's store, this buffer's last tenant, has read it
-                        gu_tile_load(c, a, tn, (yiter + C::kYBufs - 1) % C::kYBufs);
-                        ++yloads;
-                    }
-                }
+                if (e == 0 && lane == 0)
+                    y_ring_prefetch(c, t, yiter, yloads, [&](int tt, int bb) { gu_tile_load(c, a, tt, bb); });
                 if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
                 tc_fence_after();
                 if (!mbar_wait(&c.bar->ybar[b], (uint32_t)(yiter / C::kYBufs) & 1u, c.w, kSiteEpiAccFull)) return;
@@ -1105,23 +1114,12 @@ struct Gemm {
                 }
                 ++yiter;
             } else if constexpr (EPI == kEpiAddBF16) {
-                // y += acc: the tile's y arrives by TMA (loaded one tile ahead into
-                // the other buffer), each thread adds its accumulator row in place,
-                // and the tile leaves by TMA once every epilogue thread is done
+                // y += acc: the tile's y arrives by TMA through the ring (loaded
+                // kYBufs - 1 tiles ahead), each thread adds its accumulator row in
+                // place, and the tile leaves by TMA once every epilogue thread is done
                 const int b = yiter % C::kYBufs;
-                if (e == 0 && lane == 0) {
-                    if (yiter == 0)
-                        for (int i = 0; i < C::kYBufs - 1 && t + i * c.nslots < c.num_tiles; ++i) {
-                            y_tile_load(c, a, t + i * c.nslots, i);
-                            ++yloads;
-                        }
-                    const int tn = t + (C::kYBufs - 1) * c.nslots;
-                    if (tn < c.num_tiles) {
-                        bulk_wait_read_all();   // tile yiter - 1's store, this buffer's last tenant, has read it
-                        y_tile_load(c, a, tn, (yiter + C::kYBufs - 1) % C::kYBufs);
-                        ++yloads;
-                    }
-                }
+                if (e == 0 && lane == 0)
+                    y_ring_prefetch(c, t, yiter, yloads, [&](int tt, int bb) { y_tile_load(c, a, tt, bb); });
                 if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
                 tc_fence_after();
                 if (!mbar_wait(&c.bar->ybar[b], (uint32_t)(yiter / C::kYBufs) & 1u, c.w, kSiteEpiAccFull)) return;
