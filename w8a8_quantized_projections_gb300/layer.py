@@ -193,8 +193,9 @@ class QuantizedLayer:
         """acts: activation name -> bf16 [M][K].  Returns the output buffers.
 
         events: optional dict; when given, CUDA events are recorded on the
-        current stream around every launch, under keys ("quant", name) and
-        ("gemm", name), as (start, end) pairs appended to lists.
+        current stream around every launch, under keys ("quant", name),
+        ("gemm", name) and ("lora", name) (a packed group's shared x A^T under
+        ("lora", "q+k+v:xA")), as (start, end) pairs appended to lists.
         final_wait: optional CUDA event the current stream waits for before the
         step's last projection writes its output (e.g. the read-back of the
         previous step's output on another stream)."""
