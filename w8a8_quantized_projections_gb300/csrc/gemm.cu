@@ -145,6 +145,9 @@ struct Cfg {
     static_assert(NSTAGE >= 2, "pipeline depth");
     static_assert(!kI8 || (kConvWarps % kConvGroups == 0 && kConvGroups <= NSTAGE && kConvGroups <= NRAW),
                   "converter groups");
+    // stream-K counters and pieces are laid out for eight epilogue warps of
+    // 128 int32 columns each
+    static_assert(!kStreamK || (kEpiWarps == 8 && kColsPerThread == 128), "stream-K layout");
 };
 
 struct Barriers {
