@@ -54,14 +54,18 @@ def parse():
 
 def measured_traffic(cfg, proj):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, or None when that kernel's source changed since the capture."""
+    summary, or None when that kernel's source changed since the capture.
+    The record names the gemm.cu it was captured on, and may list later
+    gemm.cu sources whose changes lie outside the captured kernel's
+    instantiation (each with its reason in the summary)."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)
         src = os.path.join(ROOT, "w8a8_quantized_projections_gb300", "csrc", "gemm.cu")
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if h != rec["gemm_cu_sha256_prefix"] or not rec["workload"].startswith(cfg.name + " " + proj):
+        same = [rec["gemm_cu_sha256_prefix"]] + rec.get("same_kernel_sources", [])
+        if h not in same or not rec["workload"].startswith(cfg.name + " " + proj):
             return None
         return rec["dram_read_bytes"] + rec["dram_write_bytes"]
     except Exception:

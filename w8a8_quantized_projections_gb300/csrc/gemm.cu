@@ -1034,25 +1034,6 @@ struct Gemm {
         }
     }
 
-    // The ring of y tiles (one thread): at the CTA's first tile, load its first
-    // kYBufs - 1 tiles; then, each tile, load the one kYBufs - 1 ahead into the
-    // buffer whose last tenant (tile yiter - 1) has had its store read out.
-    template <typename Load>
-    static __device__ __forceinline__ void y_ring_prefetch(const Ctx &c, int t, int yiter, int &yloads,
-                                                           Load load) {
-        if (yiter == 0)
-            for (int i = 0; i < C::kYBufs - 1 && t + i * c.nslots < c.num_tiles; ++i) {
-                load(t + i * c.nslots, i);
-                ++yloads;
-            }
-        const int tn = t + (C::kYBufs - 1) * c.nslots;
-        if (tn < c.num_tiles) {
-            bulk_wait_read_all();
-            load(tn, (yiter + C::kYBufs - 1) % C::kYBufs);
-            ++yloads;
-        }
-    }
-
     // yiter: y tiles finished; yloads: y tile loads issued (y += acc only).
     static __device__ void epilogue_tiles(const Ctx &c, const GemmArgs &a, int &yiter, int &yloads) {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1095,8 +1076,22 @@ struct Gemm {
                 // h computed in place over the gate columns, stored by TMA after a
                 // bounded epilogue rendezvous
                 const int b = yiter % C::kYBufs;
-                if (e == 0 && lane == 0)
-                    y_ring_prefetch(c, t, yiter, yloads, [&](int tt, int bb) { gu_tile_load(c, a, tt, bb); });
+                if (e == 0 && lane == 0) {
+                    // the ring: at the CTA's first tile, load its first kYBufs - 1
+                    // tiles; then, each tile, load the one kYBufs - 1 ahead into the
+                    // buffer whose last tenant (tile yiter - 1) has had its store read out
+                    if (yiter == 0)
+                        for (int i = 0; i < C::kYBufs - 1 && t + i * c.nslots < c.num_tiles; ++i) {
+                            gu_tile_load(c, a, t + i * c.nslots, i);
+                            ++yloads;
+                        }
+                    const int tn = t + (C::kYBufs - 1) * c.nslots;
+                    if (tn < c.num_tiles) {
+                        bulk_wait_read_all();
+                        gu_tile_load(c, a, tn, (yiter + C::kYBufs - 1) % C::kYBufs);
+                        ++yloads;
+                    }
+                }
                 if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
                 tc_fence_after();
                 if (!mbar_wait(&c.bar->ybar[b], (uint32_t)(yiter / C::kYBufs) & 1u, c.w, kSiteEpiAccFull)) return;
@@ -1121,8 +1116,22 @@ struct Gemm {
                 // kYBufs - 1 tiles ahead), each thread adds its accumulator row in
                 // place, and the tile leaves by TMA once every epilogue thread is done
                 const int b = yiter % C::kYBufs;
-                if (e == 0 && lane == 0)
-                    y_ring_prefetch(c, t, yiter, yloads, [&](int tt, int bb) { y_tile_load(c, a, tt, bb); });
+                if (e == 0 && lane == 0) {
+                    // the ring: at the CTA's first tile, load its first kYBufs - 1
+                    // tiles; then, each tile, load the one kYBufs - 1 ahead into the
+                    // buffer whose last tenant (tile yiter - 1) has had its store read out
+                    if (yiter == 0)
+                        for (int i = 0; i < C::kYBufs - 1 && t + i * c.nslots < c.num_tiles; ++i) {
+                            y_tile_load(c, a, t + i * c.nslots, i);
+                            ++yloads;
+                        }
+                    const int tn = t + (C::kYBufs - 1) * c.nslots;
+                    if (tn < c.num_tiles) {
+                        bulk_wait_read_all();
+                        y_tile_load(c, a, tn, (yiter + C::kYBufs - 1) % C::kYBufs);
+                        ++yloads;
+                    }
+                }
                 if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
                 tc_fence_after();
                 if (!mbar_wait(&c.bar->ybar[b], (uint32_t)(yiter / C::kYBufs) & 1u, c.w, kSiteEpiAccFull)) return;
