@@ -46,7 +46,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="clef", choices=["clef", "reference"])
-    ap.add_argument("--config", type=int, default=1, help="workload index (0-4)")
+    ap.add_argument("--config", default="int8-mlp-27b-m1502",
+                    help="workload name (or its position 0-4 in the workload table)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -213,7 +214,7 @@ def sample_rows(cfg, n):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    cfg = S.CONFIGS[args.config]
+    cfg = S.workload(args.config)
     acts, weights, lora = S.layer_inputs(cfg, seed=0)
     threads = cpu_threads()
     per_step_rows = threads  # one row per host thread per step
@@ -297,7 +298,7 @@ def main():
     if world > 1:
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
-    cfg = S.CONFIGS[args.config]
+    cfg = S.workload(args.config)
     hbm_gbs, bf16_peak, bf16_sust, peak_src = peaks()
 
     # replicas: each rank works on its own batch (seeded by rank), weights shared by seed

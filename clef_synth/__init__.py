@@ -31,7 +31,7 @@ from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
-from .configs import CONFIGS, Config, Projection  # noqa: F401
+from .configs import CONFIGS, WORKLOADS, Config, Projection, workload  # noqa: F401
 
 _GOLDEN = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)

@@ -105,3 +105,14 @@ CONFIGS = {
     4: Config(4, "int8-layer-27b-m24032-lora256", 24032, "int8", _layer27b(24032),
               lora_rank=256),
 }
+
+WORKLOADS = {c.name: c for c in CONFIGS.values()}
+
+
+def workload(key) -> Config:
+    """The workload called ``key`` (its name), or at position ``key`` (0-4)."""
+    if isinstance(key, int) or (isinstance(key, str) and key.isdigit()):
+        return CONFIGS[int(key)]
+    if key not in WORKLOADS:
+        raise KeyError(f"unknown workload {key!r}; known: {', '.join(WORKLOADS)}")
+    return WORKLOADS[key]

@@ -46,17 +46,21 @@ def lora_y_bound(t_ref, B, y_ref, K, r_pad, x, A):
     return (2 * bf16_ulp(S.bf16_bits_to_f64(y_ref)) + terr @ Bv.T + 2 * gr * (np.abs(tv) @ Bv.T))
 
 
-@pytest.mark.parametrize("index,pack", [(0, True), (1, True), (2, True), (3, True), (4, True),
-                                        (3, False)])
-def test_workload_full_size(orc, index, pack):
-    cfg = S.CONFIGS[index]
+@pytest.mark.parametrize("name,pack", [("int8-linear-m298-2048x2048", True),
+                                       ("int8-mlp-27b-m1502", True),
+                                       ("int8-layer-27b-m2270", True),
+                                       ("fp8-layer-9b-m1502", True),
+                                       ("int8-layer-27b-m24032-lora256", True),
+                                       ("fp8-layer-9b-m1502", False)])
+def test_workload_full_size(orc, name, pack):
+    cfg = S.workload(name)
     fp8 = cfg.scheme == "fp8"
     acts_np, weights_np, lora_np = S.layer_inputs(cfg, seed=0)
     weights = {k: (bf16_dev(W), bf16_dev(b)) for k, (W, b) in weights_np.items()}
     lora = {k: (bf16_dev(A), bf16_dev(B)) for k, (A, B) in lora_np.items()}
     acts = {k: bf16_dev(x) for k, x in acts_np.items()}
     layer = QuantizedLayer(cfg, weights, lora or None, pack_shared_input=pack)
-    if pack and index in (2, 3, 4):
+    if pack and {"q", "k", "v"} <= {p.name for p in cfg.projections}:
         assert [len(g) for g in layer.groups][0] == 3, "q, k and v packed into one GEMM"
     out = layer.step(acts)
     torch.cuda.synchronize()

@@ -12,7 +12,7 @@ def _weights(cfg, bias=True):
 
 
 def test_q_k_v_pack_into_one_launch():
-    cfg = S.CONFIGS[2]
+    cfg = S.workload("int8-layer-27b-m2270")
     groups = layer._groups(cfg.projections, _weights(cfg))
     names = [[p.name for p in g] for g in groups]
     assert names == [["q", "k", "v"], ["o"], ["gateup"], ["down"]]
@@ -20,7 +20,7 @@ def test_q_k_v_pack_into_one_launch():
 
 
 def test_packing_needs_the_same_input_and_bias_presence():
-    cfg = S.CONFIGS[2]
+    cfg = S.workload("int8-layer-27b-m2270")
     w = _weights(cfg)
     w["k"] = (object(), None)     # k without bias: packed with neither q nor v
     names = [[p.name for p in g] for g in layer._groups(cfg.projections, w)]
@@ -39,6 +39,14 @@ def test_gateup_and_chained_down_are_never_packed():
 
 
 def test_gemm_ops_count_each_projection_once():
-    cfg = S.CONFIGS[1]
+    cfg = S.workload("int8-mlp-27b-m1502")
     # gate/up: 2 * M * (2 * 17408) * 5120; down: 2 * M * 5120 * 17408
     assert cfg.gemm_ops() == 2 * 1502 * 2 * 17408 * 5120 + 2 * 1502 * 5120 * 17408
+
+
+def test_workloads_resolve_by_name_and_position():
+    for i, cfg in S.CONFIGS.items():
+        assert S.workload(cfg.name) is cfg
+        assert S.workload(i) is cfg and S.workload(str(i)) is cfg
+    with pytest.raises(KeyError):
+        S.workload("no-such-workload")

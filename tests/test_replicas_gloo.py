@@ -27,7 +27,7 @@ def _rank(rank, world, port, out):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
-        cfg = S.CONFIGS[0]
+        cfg = S.workload("int8-linear-m298-2048x2048")
         acts, weights, _ = S.layer_inputs(cfg, seed=0)
         mine = bench.replica_activations(cfg, acts, rank)
         seconds = 1.0 + rank           # rank 1 is the slow one
@@ -60,7 +60,7 @@ def test_single_rank_is_unchanged():
     sys.path.insert(0, ROOT)
     import bench
     import clef_synth as S
-    cfg = S.CONFIGS[0]
+    cfg = S.workload("int8-linear-m298-2048x2048")
     acts, _, _ = S.layer_inputs(cfg, seed=0)
     assert bench.replica_activations(cfg, acts, 0) is acts
     assert bench.max_over_ranks(1.5, 1, None, "cpu") == 1.5
