@@ -37,7 +37,8 @@
  *    clamped to [-127, 127].  An all-zero row gets s = 0 and codes 0.
  *  - FP8: s = amax/448, r = 448/amax, codes = e4m3 (finite variant, max 448)
  *    round-to-nearest-even with saturation to +-448; the sign of a value that
- *    rounds to zero is kept (negative zero is code 0x80).
+ *    rounds to zero is kept (negative zero is code 0x80).  Inputs on this
+ *    path are finite; an infinity saturates and a NaN gives the NaN code 0x7F.
  *  - Epilogue: y = bf16(((float)acc * s[m]) * sw[n] + bias[n]).
  *  - SwiGLU: g and u are epilogue values before rounding, h = bf16(g / (1 +
  *    expf(-g)) * u); packed weights hold the gate rows first, then the up rows.
@@ -235,10 +236,13 @@ double orc_e4m3_decode(uint8_t c)
     return sgn ? -mag : mag;
 }
 
-/* Nearest e4m3 code to a finite fp32 value, ties to even mantissa,
- * magnitudes beyond 448 saturate to 448; the sign is always kept. */
+/* Nearest e4m3 code to an fp32 value, ties to even mantissa, magnitudes
+ * beyond 448 (infinities included) saturate to 448 with their sign; NaN gives
+ * the NaN code. */
 uint8_t orc_e4m3_encode(float f)
 {
+    if (isnan(f))
+        return 0x7F;                              /* the format's NaN, 0 1111 111 */
     uint8_t sgn = signbit(f) ? 0x80 : 0x00;
     double a = fabs((double)f);
     if (a >= 448.0)

@@ -14,7 +14,20 @@ def pytest_configure(config):
 
 
 @pytest.fixture(scope="session")
-def orc():
+def orc(tmp_path_factory):
     import oracle
+    src = os.environ.get("CLEF_ORACLE_MUTANT")
+    if src:
+        # a copy of the oracle with one planted mistake (see
+        # test_oracle_mutants.py): the same bindings over a build of that source
+        import importlib.util
+        spec = importlib.util.spec_from_file_location("oracle_mutant", oracle.__file__)
+        mod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mod)
+        mod._SRC = src
+        mod._BUILD = str(tmp_path_factory.mktemp("oracle_mutant"))
+        mod._LIB = os.path.join(mod._BUILD, "libclef_oracle.so")
+        mod.lib()
+        return mod
     oracle.lib()
     return oracle

@@ -1,0 +1,98 @@
+"""The oracle against the hand-derived fixtures in ``tests/golden/``.
+
+``e4m3_points.txt`` holds FP8 E4M3 encodings worked out from the format's
+definition (ties, subnormals, saturation, NaN); ``int8_h128_worked.txt`` a
+rotated INT8 linear on rows built from Sylvester-Hadamard rows, whose codes,
+scales, integer accumulators and bf16 outputs follow by hand.  Neither file
+was written by the oracle or by the CUDA path, so a slip in the oracle's
+rotation order, rounding, scale or epilogue operand order fails here.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield line
+
+
+def _f32(text):
+    if text in ("inf", "-inf", "nan"):
+        return float(text)
+    return float(np.float32(float.fromhex(text)))
+
+
+def test_e4m3_points(orc):
+    rows = [ln.split(None, 2) for ln in _lines("e4m3_points.txt")]
+    assert len(rows) >= 20
+    for value, code, why in rows:
+        v, c = _f32(value), int(code, 16)
+        assert orc.e4m3_encode(v) == c, (value, why)
+        d = orc.e4m3_decode(c)
+        if math.isnan(v):
+            assert math.isnan(d)
+        elif abs(v) <= 448 and "halfway" not in why and "above" not in why:
+            # an exactly representable value decodes back to itself
+            assert d == v and math.copysign(1.0, d) == math.copysign(1.0, v), (value, why)
+
+
+def _worked():
+    rows, codes, scales, acc, y = {}, {}, {}, {}, {}
+    for ln in _lines("int8_h128_worked.txt"):
+        kind, *rest = ln.split()
+        if kind == "row":
+            rows[rest[0]] = [(int(b), int(j), float(a)) for b, j, a in (t.split(":") for t in rest[1:])]
+        elif kind == "codes":
+            codes[rest[0]] = {int(i): int(q) for i, q in (t.split(":") for t in rest[1:])}
+        elif kind == "scale":
+            scales[rest[0]] = int(rest[1], 16)
+        elif kind == "acc":
+            acc[int(rest[0]), int(rest[1])] = int(rest[2])
+        elif kind == "y":
+            y[int(rest[0]), int(rest[1])] = (int(rest[2], 16), float(rest[3]))
+    return rows, codes, scales, acc, y
+
+
+def _build(parts, K=256):
+    """bf16 bits of a row that is a sum of scaled Sylvester rows per block."""
+    k = np.arange(128)
+    v = np.zeros(K)
+    for b, j, a in parts:
+        sign = np.array([1.0 if bin(j & kk).count("1") % 2 == 0 else -1.0 for kk in k])
+        v[b * 128:(b + 1) * 128] += a * sign
+    t = torch.tensor(v, dtype=torch.float64).to(torch.bfloat16)
+    assert torch.equal(t.to(torch.float64), torch.tensor(v)), "every element exact in bf16"
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_int8_h128_worked_example(orc):
+    rows, codes, scales, acc, y = _worked()
+    xs, ws = ["x0", "x1"], ["w0", "w1", "w2"]
+    X = np.stack([_build(rows[n]) for n in xs])
+    W = np.stack([_build(rows[n]) for n in ws])
+    qx, sx = orc.quant_int8_h128(X)
+    qw, sw = orc.quant_int8_h128(W)
+    for names, q, s in ((xs, qx, sx), (ws, qw, sw)):
+        for i, n in enumerate(names):
+            want = np.zeros(256, np.int8)
+            for idx, code in codes[n].items():
+                want[idx] = code
+            assert np.array_equal(q[i], want), n
+            assert int(np.float32(s[i]).view(np.uint32)) == scales[n], n
+    a = orc.int8_gemm_acc(qx, qw)
+    for (m, n), v in acc.items():
+        assert int(a[m, n]) == v, (m, n)
+    out = orc.int8_linear(qx, sx, qw, sw)
+    for (m, n), (bits, value) in y.items():
+        assert int(out[m, n]) == bits, (m, n)
+        as_bf16 = torch.from_numpy(np.array([bits], np.uint16).view(np.int16)).view(torch.bfloat16)
+        assert float(as_bf16) == value, (m, n)

@@ -171,8 +171,8 @@ def test_int8_quant_one_hot_and_zero_rows(orc):
 
 def test_int8_codes_are_rint_of_scaled_values(orc):
     """Codes are numpy's round-half-even rint of fp32(v * (127/amax)), on the
-    oracle's rotated values (the rotation is pinned above); a handmade row
-    whose scaled values sit on exact halves checks the tie rule."""
+    oracle's rotated values (the rotation is pinned above).  Random rows
+    almost never land on an exact half; the next test builds such cases."""
     x = S.activation(0, "pin/rint", 4, 256)
     q, _ = orc.quant_int8_h128(x)
     v = orc.rotate_rows(x)
@@ -182,6 +182,34 @@ def test_int8_codes_are_rint_of_scaled_values(orc):
     assert np.array_equal(q, want)
     # np.rint itself rounds ties to even (the rule the codes follow)
     assert np.array_equal(np.rint(np.array([0.5, 1.5, 2.5, -0.5, -2.5])), [0, 2, 2, -0, -2])
+
+
+def test_int8_code_ties_round_to_even(orc):
+    """Exact halves: a row of 0.5s rotates to v = fp32(64 c) at index 0 and
+    zeros elsewhere; static scales s found next to v / target give
+    fp32(v * fp32(1/s)) equal to target, an exact half with an even integer
+    below it.  Round-half-even keeps that integer (either sign), so a
+    round-half-up or half-away rule fails here."""
+    c = np.float32(1.0 / math.sqrt(128.0))
+    v = np.float32(np.float32(64.0) * c)
+    x = np.stack([S.f64_to_bf16_bits(np.full(128, 0.5)), S.f64_to_bf16_bits(np.full(128, -0.5))])
+    rot = orc.rotate_rows(x)
+    assert rot[0, 0] == v and rot[1, 0] == -v and not rot[:, 1:].any()
+    found = []
+    for target in (0.5, 2.5, 12.5, 62.5, 100.5, 126.5):
+        s0 = np.float32(v / np.float32(target))
+        for d in range(-64, 65):
+            sc = (np.array([s0], np.float32).view(np.int32) + d).view(np.float32)[0]
+            if np.float32(v * (np.float32(1.0) / sc)) == np.float32(target):
+                found.append((sc, target))
+                break
+    assert len(found) >= 3, found
+    for sc, target in found:
+        q, _ = orc.quant_static(x, float(sc), "int8_h128")
+        even = int(target - 0.5)
+        assert even % 2 == 0
+        assert q[0, 0] == even and q[1, 0] == -even, (target, q[:, 0])
+        assert not q[:, 1:].any()
 
 
 def test_static_int8_codes_are_clamped_rint(orc):
@@ -358,6 +386,16 @@ def test_int8_linear_exact_cases(orc):
     # fp32 add then cast
     want = want.float().to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
     assert np.array_equal(y2, want)
+    # a bias as large as the scaled products, one value per output channel:
+    # dropping it, or indexing it by row, changes the outputs
+    big = S.f64_to_bf16_bits(np.array([3.0, -5.0, 0.5, 7.0, -1.25]))
+    y3 = orc.int8_linear(a, np.full(3, 2.0 ** -8, np.float32), b, np.full(5, 2.0 ** -8, np.float32), big)
+    want3 = (torch.from_numpy(a.astype(np.int64) @ b.astype(np.int64).T).double() * 2.0 ** -16
+             + torch.tensor([3.0, -5.0, 0.5, 7.0, -1.25], dtype=torch.float64))
+    want3 = want3.float().to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    assert np.array_equal(y3, want3)
+    no_bias = orc.int8_linear(a, np.full(3, 2.0 ** -8, np.float32), b, np.full(5, 2.0 ** -8, np.float32))
+    assert (y3 != no_bias).all()
 
 
 # ------------------------------------------------------------------ SwiGLU
