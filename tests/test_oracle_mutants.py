@@ -72,6 +72,25 @@ MUTANTS = [
     ("lora: B read transposed",
      "double b = (j < r) ? (double)bf16_to_f32(B[n * r + j]) : 0.0;",
      "double b = (j < r) ? (double)bf16_to_f32(B[j * N + n]) : 0.0;"),
+    ("fp8 gate/up: gate and up swapped",
+     "h[m * ldh + n] = f32_to_bf16(swiglu_f32(gu[0], gu[1]));",
+     "h[m * ldh + n] = f32_to_bf16(swiglu_f32(gu[1], gu[0]));"),
+    ("unfused swiglu: up read from the gate half",
+     "float u = bf16_to_f32(y_gu[m * ldg + N + n]);", "float u = bf16_to_f32(y_gu[m * ldg + n]);"),
+    ("fp8: rotation flag ignored",
+     "        if (rotate)\n            orc_rotate_rows_f32(x + m * ldx, 1, K, ldx, v);\n        else\n"
+     "            for (int64_t k = 0; k < K; k++)\n                v[k] = bf16_to_f32(x[m * ldx + k]);\n"
+     "        quant_row_fp8(",
+     "        if (0)\n            orc_rotate_rows_f32(x + m * ldx, 1, K, ldx, v);\n        else\n"
+     "            for (int64_t k = 0; k < K; k++)\n                v[k] = bf16_to_f32(x[m * ldx + k]);\n"
+     "        quant_row_fp8("),
+    ("static: scale used as the reciprocal",
+     "const float r = 1.0f / s;", "const float r = s;"),
+    ("lora: padding columns not zero",
+     "t[m * r_pad + j] = 0;", "t[m * r_pad + j] = 0x3F80;"),
+    ("fp8 linear: bias dropped",
+     "            if (bias)\n                v = v + bf16_to_f32(bias[n]);",
+     "            if (bias)\n                v = v + 0.0f * bf16_to_f32(bias[n]);"),
     ("lora: t rounded by truncation",
      "t[m * r_pad + j] = f64_to_bf16(a);",
      "{ float tf = (float)a; uint32_t tu; memcpy(&tu, &tf, 4); t[m * r_pad + j] = (uint16_t)(tu >> 16); }"),

@@ -469,6 +469,12 @@ def test_fp8_linear_exact_sum(orc):
             v = np.float32(np.float32(acc * sx[m]) * sw[n])
             v = np.float32(v + np.float32(orc.bf16_to_f32(int(bias[n]))))
             assert y[m, n] == orc.f32_to_bf16(float(v))
+    # scales of 2^-40 shrink every product below 2^-15 of the bias, so the output is
+    # the per-channel bias itself (a dropped or row-indexed bias fails)
+    big = np.array([3.0, -5.0, 0.5, 7.0])
+    y2 = orc.fp8_linear(qx, np.full(M, 2.0 ** -40, np.float32), qw, np.full(N, 2.0 ** -40, np.float32),
+                        S.f64_to_bf16_bits(big))
+    assert np.array_equal(S.bf16_bits_to_f64(y2), np.tile(big, (M, 1)))
 
 
 def test_fp8_linear_approximates_projection(orc):
