@@ -43,6 +43,7 @@ S = C.c_void_p(None)             # stream
     (NUL, 4, 128, 128, 0, FAKE, FAKE, S),       # null x
     (FAKE, 4, 100, 128, 0, FAKE, FAKE, S),      # K not a multiple of 128 (rotated)
     (FAKE, 4, 80, 80, 1, FAKE, FAKE, S),        # K not a multiple of 32 (fp8)
+    (FAKE, 4, 96, 96, 2, FAKE, FAKE, S),        # K not a multiple of 128 (rotated fp8)
     (FAKE, 4, 128, 120, 0, FAKE, FAKE, S),      # ldx < K
     (ODD, 4, 128, 128, 0, FAKE, FAKE, S),       # misaligned x
     (FAKE, 4, 128, 128, 7, FAKE, FAKE, S),      # unknown mode
@@ -56,6 +57,11 @@ def test_quant_act_rejects_bad_arguments(args):
 @pytest.mark.parametrize("sc", [0.0, -1.0, float("inf"), float("nan")])
 def test_quant_act_static_rejects_bad_scales(sc):
     assert clef.library().clef_quant_act_static(FAKE, 4, 128, 128, 1, sc, FAKE, FAKE, S) == 1
+
+
+@pytest.mark.parametrize("mode", [0, 2])
+def test_quant_act_static_rotated_needs_whole_blocks(mode):
+    assert clef.library().clef_quant_act_static(FAKE, 4, 96, 96, mode, 0.5, FAKE, FAKE, S) == 1
 
 
 @pytest.mark.parametrize("name", ["clef_w8a8_linear", "clef_fp8_linear", "clef_w8a8_gateup_swiglu",
