@@ -2,9 +2,12 @@
 token rows with no exchange): each rank runs its own batch, and the job's
 time is the slowest rank's.  Its host logic runs here as two gloo ranks on
 the CPU: distinct per-rank inputs with shared weights, the max-over-ranks
-reduction of the timed seconds, and the whole-job throughput."""
+reduction of the timed seconds, and the whole-job throughput.  The reference
+arm (the oracle timed on the host cores) prints its one line on rank 0 only."""
+import json
 import os
 import socket
+import subprocess
 import sys
 
 import numpy as np
@@ -64,3 +67,29 @@ def test_single_rank_is_unchanged():
     acts, _, _ = S.layer_inputs(cfg, seed=0)
     assert bench.replica_activations(cfg, acts, 0) is acts
     assert bench.max_over_ranks(1.5, 1, None, "cpu") == 1.5
+
+
+def _bench(env_extra, *args):
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", *args],
+                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    p = _bench({"WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"},
+               "--steps", "1", "--warmup", "0", "--config", "int8-linear-m298-2048x2048")
+    assert p.returncode == 0 and p.stdout.strip() == ""
+
+
+def test_reference_arm_prints_one_line():
+    p = _bench({"WORLD_SIZE": "1", "RANK": "0", "LOCAL_RANK": "0"},
+               "--steps", "1", "--warmup", "0", "--config", "int8-linear-m298-2048x2048")
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [ln for ln in p.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["config"]["workload"] == "int8-linear-m298-2048x2048"
+    assert d["value"] > 0 and d["unit"] == "TOPS" and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
