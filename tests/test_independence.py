@@ -92,3 +92,24 @@ def test_bench_imports_the_oracle_only_for_the_cpu_baseline():
 def test_entry_points_import_the_oracle_only_to_build_and_check():
     tree = ast.parse(open(os.path.join(ROOT, "__graft_entry__.py"), encoding="utf-8").read())
     assert set(_imports_of(tree, "oracle")) <= {"build", "smoke"}
+
+
+# torch calls that would compute a step of the path (any of them in the package
+# would be a fallback around the CUDA kernels)
+COMPUTE = {"matmul", "mm", "bmm", "addmm", "einsum", "linear", "_int_mm", "_scaled_mm", "silu", "sigmoid",
+           "exp", "softmax", "amax", "abs", "round", "clamp", "clip", "sum", "mul", "add", "div", "mul_",
+           "add_", "div_", "hadamard", "fft", "functional", "rint"}
+
+
+def test_package_python_computes_nothing_itself():
+    """The binding and the layer runner only allocate, pack weights at set-up
+    and marshal arguments; every step of the path runs in the library."""
+    for path in _sources(PKG):
+        if not path.endswith(".py"):
+            continue
+        tree = ast.parse(open(path, encoding="utf-8").read())
+        for node in ast.walk(tree):
+            if isinstance(node, ast.Attribute) and node.attr in COMPUTE:
+                raise AssertionError(f"{path}:{node.lineno}: .{node.attr}")
+            if isinstance(node, ast.BinOp) and isinstance(node.op, ast.MatMult):
+                raise AssertionError(f"{path}:{node.lineno}: @")
