@@ -8,6 +8,8 @@ oracle (a static scan of the sources; no GPU).
   the reference arm.
 - ``__graft_entry__.py`` imports it only in ``build()`` (which compiles the
   checker) and ``smoke()`` (which checks against it).
+- The package's Python calls no torch arithmetic: no CPU or library fallback
+  stands in for a kernel.
 """
 import ast
 import os
