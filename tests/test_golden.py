@@ -3,7 +3,10 @@
 ``e4m3_points.txt`` holds FP8 E4M3 encodings worked out from the format's
 definition (ties, subnormals, saturation, NaN); ``int8_h128_worked.txt`` a
 rotated INT8 linear on rows built from Sylvester-Hadamard rows, whose codes,
-scales, integer accumulators and bf16 outputs follow by hand.  Neither file
+scales, integer accumulators and bf16 outputs follow by hand;
+``fp8_worked.txt`` an FP8 dynamic linear whose scales are powers of two, so
+that its codes (a tie and a subnormal among them), accumulators and bf16
+outputs (one an exact tie) follow by hand.  None of the files
 was written by the oracle or by the CUDA path, so a slip in the oracle's
 rotation order, rounding, scale or epilogue operand order fails here.
 """
@@ -92,6 +95,59 @@ def test_int8_h128_worked_example(orc):
     for (m, n), v in acc.items():
         assert int(a[m, n]) == v, (m, n)
     out = orc.int8_linear(qx, sx, qw, sw)
+    for (m, n), (bits, value) in y.items():
+        assert int(out[m, n]) == bits, (m, n)
+        as_bf16 = torch.from_numpy(np.array([bits], np.uint16).view(np.int16)).view(torch.bfloat16)
+        assert float(as_bf16) == value, (m, n)
+
+
+def _fp8_worked():
+    rows, codes, scales, acc, y = {}, {}, {}, {}, {}
+    for ln in _lines("fp8_worked.txt"):
+        kind, *rest = ln.split()
+        if kind == "row":
+            rows[rest[0]] = {int(i): float(v) for i, v in (t.split(":") for t in rest[1:])}
+        elif kind == "codes":
+            codes[rest[0]] = {int(i): int(c, 16) for i, c in (t.split(":") for t in rest[1:])}
+        elif kind == "scale":
+            scales[rest[0]] = int(rest[1], 16)
+        elif kind == "acc":
+            acc[int(rest[0]), int(rest[1])] = int(rest[2])
+        elif kind == "y":
+            y[int(rest[0]), int(rest[1])] = (int(rest[2], 16), float(rest[3]))
+    return rows, codes, scales, acc, y
+
+
+def test_fp8_worked_example(orc):
+    import clef_synth as S
+    rows, codes, scales, acc, y = _fp8_worked()
+    K = 32
+
+    def build(name):
+        v = np.zeros(K)
+        for i, val in rows[name].items():
+            v[i] = val
+        bits = S.f64_to_bf16_bits(v)
+        assert np.array_equal(S.bf16_bits_to_f64(bits), v), "every element exact in bf16"
+        return bits
+
+    xs, ws = ["x0", "x1"], ["w0", "w1"]
+    X = np.stack([build(n) for n in xs])
+    W = np.stack([build(n) for n in ws])
+    qx, sx = orc.quant_fp8(X)
+    qw, sw = orc.quant_fp8(W)
+    for names, q, s in ((xs, qx, sx), (ws, qw, sw)):
+        for i, n in enumerate(names):
+            want = np.zeros(K, np.uint8)
+            for idx, c in codes[n].items():
+                want[idx] = c
+            assert np.array_equal(q[i], want), (n, q[i][:8])
+            assert int(np.float32(s[i]).view(np.uint32)) == scales[n], n
+    dec = np.vectorize(orc.e4m3_decode)
+    a = dec(qx.astype(np.int64)) @ dec(qw.astype(np.int64)).T
+    for (m, n), v in acc.items():
+        assert a[m, n] == v, (m, n)
+    out = orc.fp8_linear(qx, sx, qw, sw)
     for (m, n), (bits, value) in y.items():
         assert int(out[m, n]) == bits, (m, n)
         as_bf16 = torch.from_numpy(np.array([bits], np.uint16).view(np.int16)).view(torch.bfloat16)
