@@ -6,7 +6,9 @@ rotated INT8 linear on rows built from Sylvester-Hadamard rows, whose codes,
 scales, integer accumulators and bf16 outputs follow by hand;
 ``fp8_worked.txt`` an FP8 dynamic linear whose scales are powers of two, so
 that its codes (a tie and a subnormal among them), accumulators and bf16
-outputs (one an exact tie) follow by hand.  None of the files
+outputs (one an exact tie) follow by hand; ``lora_worked.txt`` a LoRA add whose
+one output element sits on a tie only when t is rounded to bf16 first (the
+pull request's intermediate rounding point).  None of the files
 was written by the oracle or by the CUDA path, so a slip in the oracle's
 rotation order, rounding, scale or epilogue operand order fails here.
 """
@@ -152,3 +154,33 @@ def test_fp8_worked_example(orc):
         assert int(out[m, n]) == bits, (m, n)
         as_bf16 = torch.from_numpy(np.array([bits], np.uint16).view(np.int16)).view(torch.bfloat16)
         assert float(as_bf16) == value, (m, n)
+
+
+def test_lora_worked_example(orc):
+    import clef_synth as S
+    M, K, N, r = 2, 8, 16, 8
+    mats = {"x": np.zeros((M, K)), "A": np.zeros((r, K)), "B": np.zeros((N, r)), "yin": np.zeros((M, N))}
+    t_want, y_want = {}, {}
+    for ln in _lines("lora_worked.txt"):
+        kind, *rest = ln.split()
+        if kind in mats:
+            for tok in rest[1:]:
+                i, v = tok.split(":")
+                mats[kind][int(rest[0]), int(i)] = float(v)
+        elif kind in ("t", "y"):
+            (t_want if kind == "t" else y_want)[int(rest[0]), int(rest[1])] = (int(rest[2], 16), float(rest[3]))
+    bits = {}
+    for k, v in mats.items():
+        bits[k] = S.f64_to_bf16_bits(v)
+        assert np.array_equal(S.bf16_bits_to_f64(bits[k]), v), k
+    t = orc.lora_t(bits["x"], bits["A"])
+    assert t.shape == (M, 64)                      # rank 8 padded to one 64-group
+    expect_t = np.zeros((M, 64), np.uint16)
+    for (m, j), (b, _) in t_want.items():
+        expect_t[m, j] = b
+    assert np.array_equal(t, expect_t)
+    y = orc.lora_y(t, bits["B"], bits["yin"])
+    expect_y = bits["yin"].copy()
+    for (m, n), (b, _) in y_want.items():
+        expect_y[m, n] = b
+    assert np.array_equal(y, expect_y)
