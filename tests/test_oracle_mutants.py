@@ -91,6 +91,20 @@ MUTANTS = [
     ("fp8 linear: bias dropped",
      "            if (bias)\n                v = v + bf16_to_f32(bias[n]);",
      "            if (bias)\n                v = v + 0.0f * bf16_to_f32(bias[n]);"),
+    ("static int8: lower clamp at -128",
+     "if (c < -127.0f) c = -127.0f;", "if (c < -128.0f) c = -128.0f;"),
+    ("int8: all-zero row gets scale 1",
+     "    if (amax == 0.0f) {\n        *s = 0.0f;\n        memset(q, 0, (size_t)K);\n        return;\n    }\n"
+     "    *s = amax / 127.0f;",
+     "    if (amax == 0.0f) {\n        *s = 1.0f;\n        memset(q, 0, (size_t)K);\n        return;\n    }\n"
+     "    *s = amax / 127.0f;"),
+    ("int8: absmax over the first 128-block only",
+     "    float amax = 0.0f;\n    for (int64_t k = 0; k < K; k++)\n        amax = fmaxf(amax, fabsf(v[k]));\n"
+     "    if (amax == 0.0f) {\n        *s = 0.0f;\n        memset(q, 0, (size_t)K);\n        return;\n    }\n"
+     "    *s = amax / 127.0f;",
+     "    float amax = 0.0f;\n    for (int64_t k = 0; k < 128; k++)\n        amax = fmaxf(amax, fabsf(v[k]));\n"
+     "    if (amax == 0.0f) {\n        *s = 0.0f;\n        memset(q, 0, (size_t)K);\n        return;\n    }\n"
+     "    *s = amax / 127.0f;"),
     ("lora: t rounded by truncation",
      "t[m * r_pad + j] = f64_to_bf16(a);",
      "{ float tf = (float)a; uint32_t tu; memcpy(&tu, &tf, 4); t[m * r_pad + j] = (uint16_t)(tu >> 16); }"),
