@@ -3,17 +3,21 @@
 
 A step is one pass of the whole workload's hot path over one batch: every
 activation quantizer call and every projection GEMM (with its fused epilogue;
-LoRA adds where the workload has them).  Default workload: the INT8 MLP of
-one 27B-shaped layer at 1,502 tokens (packed gate/up 5120 -> 2 x 17408 with the
-fused SwiGLU epilogue, then down 17408 -> 5120).
+LoRA adds where the workload has them).  Headline workload (the largest one
+that fits one GPU): all INT8 projections of one 27B-shaped decoder layer at
+24,032 tokens (16 records of 1,502) -- q|k|v packed 5120 -> 6144 + 1024 +
+1024, o 6144 -> 5120, gate/up 5120 -> 2 x 17408 with SwiGLU, down 17408 ->
+5120 -- each with a rank-256 runtime LoRA pair.
 
 Printed (rank 0, one JSON line): whole-step W8A8 GEMM throughput in TOPS
 (2*M*N*K per projection, counted once), the end-to-end figure through the
 C ABI with host buffers, the roofline of the dominant kernel from CUDA events
 recorded on its stream (in a separate pass of up to 100 steps with an event
 pair around every launch; the timed steps carry only the step's own pair),
-the quantizer's GB/s, clocks sampled during the timed region, and the CPU
-oracle timed on a bounded sample on the host cores.
+the quantizer's GB/s, clocks sampled during the timed region, the CPU oracle
+timed on a bounded sample on the host cores, and under "configs" the other
+four workloads timed in the same process (step throughput, every GEMM's
+fraction of its tensor peak, kernel times; the FP8 layer among them).
 ``--impl reference`` times that oracle as the reference arm instead.
 """
 from __future__ import annotations
@@ -43,11 +47,13 @@ INSTRUMENTED_STEPS = 100   # steps of the per-kernel timing pass
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="clef", choices=["clef", "reference"])
-    ap.add_argument("--config", default="int8-mlp-27b-m1502",
-                    help="workload name (or its position 0-4 in the workload table)")
+    ap.add_argument("--config", default="int8-layer-27b-m24032-lora256",
+                    help="workload name (or its position 0-4 in the workload table) of the headline line")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the other workloads in the same process")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -291,15 +297,110 @@ def main():
 
     import torch
     import torch.distributed as dist
-    import w8a8_quantized_projections_gb300 as clef
-    from w8a8_quantized_projections_gb300.layer import QuantizedLayer
 
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
     cfg = S.workload(args.config)
-    hbm_gbs, bf16_peak, bf16_sust, peak_src = peaks()
+    env = Env(args, rank, world, dev, dist, torch)
+
+    line = measure(env, cfg, args.steps, headline=True)
+    line["peaks"] = env.peaks_line()
+    # ---- CPU oracle on a bounded sample of the headline workload (rank 0,
+    # N = 1): a probe of two rows per host thread sizes a sample of about
+    # CPU_SAMPLE_S seconds
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        acts_np, weights_np, lora_np = env.inputs
+        threads = cpu_threads()
+        qw = oracle_weights(cfg, weights_np, threads)
+        probe = sample_rows(cfg, 2 * threads)
+        dt0, _ = oracle_sample(cfg, acts_np, weights_np, qw, lora_np, probe, threads)
+        n = int(min(cfg.M, max(len(probe), len(probe) * CPU_SAMPLE_S / max(dt0, 1e-3))))
+        rows = sample_rows(cfg, n)
+        dt, ops = oracle_sample(cfg, acts_np, weights_np, qw, lora_np, rows, threads)
+        line["cpu_baseline"] = {"value": ops / dt / 1e12, "unit": "TOPS", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"{len(rows)} of {cfg.M} token rows through every projection "
+                                          f"of {cfg.name} ({dt:.1f} s on {threads} threads)"}
+        del qw
+    env.inputs = None
+    # the other workloads, timed in the same process (rank 0 at N = 1): each
+    # with its own step throughput, dominant kernel fraction and kernel times
+    if rank == 0 and world == 1 and not args.no_configs:
+        line["configs"] = {}
+        for c in S.CONFIGS.values():
+            if c.name == cfg.name:
+                continue
+            line["configs"][c.name] = measure(env, c, max(args.steps, MIN_STEPS_OTHER), headline=False)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+MIN_STEPS_OTHER = 100   # timed steps of each further workload (their steps take 0.03-1.5 ms)
+MMA_PEAK_ITERS = {"bf16": 100_000, "e4m3": 100_000, "s8_mma_sync": 10_000}
+
+
+class Env:
+    """What every measurement shares: arguments, ranks, device, library, peaks."""
+
+    def __init__(self, args, rank, world, dev, dist, torch):
+        import w8a8_quantized_projections_gb300 as clef
+        self.args, self.rank, self.world, self.dev, self.dist, self.torch = args, rank, world, dev, dist, torch
+        self.clef = clef
+        self.hbm_gbs, self.bf16_peak, self.bf16_sust, self.peak_src = peaks()
+        self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        # dense tensor rates of the three instruction routes, from the
+        # library's own microbenchmark on this device (TFLOP/s)
+        self.mma = {k: clef.mma_peak(k, n) for k, n in MMA_PEAK_ITERS.items()}
+
+    def peaks_line(self):
+        return {"bf16_matmul_measured": self.bf16_peak, "bf16_source": f"{self.peak_src} (cuBLAS bf16, burst)",
+                "microbenchmark_tflops": self.mma,
+                "note": "clef_mma_peak: tcgen05 kind::f16 (bf16) and kind::f8f6f4 (e4m3) MMAs issued back "
+                        "to back from shared memory by one CTA pair per two SMs; mma.sync m16n8k32 s8 "
+                        "(the legacy integer route) on register operands"}
+
+    def fp8_ratio(self):
+        """e4m3 over bf16 dense rate of the tensor pipe, measured by the
+        microbenchmark (both routes at the same clock in one process)."""
+        return self.mma["e4m3"] / self.mma["bf16"]
+
+    def tensor_peak(self, scheme):
+        """(peak TFLOP/s, source) of the tensor pipe a scheme's GEMMs run on.
+
+        The bf16 figure is the measured cuBLAS bf16 matmul rate; the e4m3 one
+        is that figure times the e4m3/bf16 ratio the microbenchmark measures
+        on this GPU, so both denominators are full GEMMs under the same power
+        and clock behaviour.  The microbenchmark's own figures (MMAs issued
+        from shared memory with no copies, a short burst at full clock) are
+        higher and are reported beside them."""
+        if scheme == "fp8":
+            r = self.fp8_ratio()
+            return (self.bf16_peak * r,
+                    f"{self.peak_src} bf16 dense burst x {r:.3f}, the e4m3/bf16 ratio measured by the "
+                    f"tcgen05 microbenchmark (kind::f8f6f4 {self.mma['e4m3']:.0f}, kind::f16 "
+                    f"{self.mma['bf16']:.0f} TFLOP/s)")
+        return (self.bf16_peak, f"{self.peak_src} bf16 dense burst (INT8 runs exactly on the fp16 "
+                                f"tensor pipe: sm_103a has no tcgen05 integer MMA; the legacy mma.sync "
+                                f"s8 route measures {self.mma['s8_mma_sync']:.0f})")
+
+
+def measure(env, cfg, steps, headline):
+    """One workload: its step timed `steps` times (L2 flushed between steps),
+    per-kernel times from a separate instrumented pass, the dominant GEMM's
+    roofline, the LoRA and quantizer figures, and the step replayed from a
+    CUDA graph.  The headline workload also gets the clocks, the quantizer
+    streaming figure and the end-to-end figure with host buffers, its dict is
+    the bench line itself, and its host inputs are kept in env.inputs for the
+    CPU oracle baseline."""
+    torch, clef, args = env.torch, env.clef, env.args
+    from w8a8_quantized_projections_gb300.layer import QuantizedLayer
+    dev, stream, flush, world, rank = env.dev, env.stream, env.flush, env.world, env.rank
 
     # replicas: each rank works on its own batch (seeded by rank), weights shared by seed
     acts_np, weights_np, lora_np = S.layer_inputs(cfg, seed=0)
@@ -312,24 +413,25 @@ def main():
     lora = {k: (bf(A), bf(B)) for k, (A, B) in lora_np.items()}
     acts = {k: bf(x) for k, x in acts_np.items()}
     layer = QuantizedLayer(cfg, weights, lora or None, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    del weights
+    ops_step = cfg.gemm_ops()
 
     for _ in range(args.warmup):
         layer.step(acts)
     torch.cuda.synchronize(dev)
-    assert clef.poll_status() == 0
+    assert layer.poll_status() == 0
 
     # ---- device-timed steps (inputs resident in HBM)
     events = {}
     step_ev = []
-    clocks = ClockSampler(local)
-    clocks.start()
-    if world > 1:
-        dist.barrier()
+    clocks = ClockSampler(dev.index) if headline else None
+    if clocks:
+        clocks.start()
+    if world > 1 and headline:
+        env.dist.barrier()
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter()
-    for _ in range(args.steps):
+    for _ in range(steps):
         flush.zero_()
         s0 = torch.cuda.Event(enable_timing=True)
         s1 = torch.cuda.Event(enable_timing=True)
@@ -338,37 +440,36 @@ def main():
         s1.record(stream)
         step_ev.append((s0, s1))
     torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
+    if world > 1 and headline:
+        env.dist.barrier()
     wall = time.perf_counter() - t_wall
-    clk = clocks.stop()
-    status = clef.poll_status()
+    clk = clocks.stop() if clocks else None
+    status = layer.poll_status()
     if status:
         raise RuntimeError(f"device status word reported {status}")
     # per-kernel times from a separate pass with an event pair around every
     # launch (the events themselves cost about 2 us each, so the timed steps
     # above carry only the step's own pair)
-    for _ in range(min(args.steps, INSTRUMENTED_STEPS)):
+    n_inst = min(steps, INSTRUMENTED_STEPS)
+    for _ in range(n_inst):
         flush.zero_()
-        layer.step(acts, events=events)   # every launch of the step, with its event pair
+        layer.step(acts, events=events)
     torch.cuda.synchronize(dev)
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
-    t_sum = max_over_ranks(sum(step_ms) / 1e3, world, dist, dev)
-    ops_step = cfg.gemm_ops()
-    value = whole_job_tops(ops_step, args.steps, world, t_sum)
+    t_sum = sum(step_ms) / 1e3
+    if headline:
+        t_sum = max_over_ranks(t_sum, world, env.dist, dev)
+    value = whole_job_tops(ops_step, steps, world if headline else 1, t_sum)
 
-    # per-kernel times
-    kt = {}
-    for key, lst in events.items():
-        kt[key] = [a.elapsed_time(b) / 1e3 for a, b in lst]
+    kt = {key: [a.elapsed_time(b) / 1e3 for a, b in lst] for key, lst in events.items()}
     gemm_keys = [k for k in kt if k[0] == "gemm"]
     units = {u[0]: u for u in layer.units()}   # name -> (name, weight rows, K, ops)
     dom = max(gemm_keys, key=lambda k: sum(kt[k]))
     dom_name, dom_rows, dom_K, dom_ops = units[dom[1]]
     dom_t = statistics.mean(kt[dom])
     achieved = dom_ops / dom_t / 1e12
-    q_bytes = 0
-    q_time = 0.0
+    peak, peak_source = env.tensor_peak(cfg.scheme)
+    q_bytes, q_time = 0, 0.0
     for key, lst in kt.items():
         if key[0] != "quant":
             continue
@@ -377,37 +478,42 @@ def main():
         q_time += sum(lst)
     q_gbs = q_bytes / q_time / 1e9 if q_time else None
     gemm_time = sum(sum(kt[k]) for k in gemm_keys)
-    n_inst = min(args.steps, INSTRUMENTED_STEPS)   # steps of the per-kernel pass
     gemm_tops = ops_step * n_inst / gemm_time / 1e12
+    gemms = {}
+    for k in gemm_keys:
+        _, rows, K, ops = units[k[1]]
+        t = statistics.mean(kt[k])
+        gemms[k[1]] = {"shape": f"{cfg.M}x{rows}x{K}", "ms": 1e3 * t, "tops": ops / t / 1e12,
+                       "frac": ops / t / 1e12 / peak,
+                       "frac_of_microbenchmark": ops / t / 1e12 / env.mma["e4m3" if cfg.scheme == "fp8" else "bf16"]}
 
     line = {
-        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": 1e3 * t_sum / args.steps, "higher_is_better": True,
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t_sum / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8" if cfg.scheme == "fp8" else "int8", "data": "synthetic",
         "config": workload_config(cfg),
         "roofline": {
             "kernel": f"{'fp8' if cfg.scheme == 'fp8' else 'w8a8'} {dom_name} GEMM "
                       f"({cfg.M}x{dom_rows}x{dom_K})",
-            "bound": "tensor", "achieved": achieved,
-            "peak": bf16_peak * (2.0 if cfg.scheme == "fp8" else 1.0),
-            "unit": "TFLOP/s",
-            "frac": achieved / (bf16_peak * (2.0 if cfg.scheme == "fp8" else 1.0)),
-            "traffic": measured_traffic(cfg, dom_name),
+            "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak,
+            "traffic": measured_traffic(cfg, dom_name) if headline else None,
             "traffic_unit": "bytes per launch",
-            "peak_source": (f"{peak_src} bf16 dense burst x2 (fp8 nominal ratio)" if cfg.scheme == "fp8"
-                            else f"{peak_src} bf16 dense burst (INT8 runs exactly on the fp16 tensor "
-                                 f"pipe: sm_103a has no tcgen05 integer MMA)"),
+            "ops_per_launch": dom_ops, "launch_ms": 1e3 * dom_t,
+            "peak_source": peak_source,
         },
         "gemm_only_tops": gemm_tops,
-        "quantizer": {"achieved": q_gbs, "unit": "GB/s", "peak": hbm_gbs,
-                      "frac": (q_gbs / hbm_gbs) if q_gbs else None,
+        "gemms": gemms,
+        "quantizer": {"achieved": q_gbs, "unit": "GB/s", "peak": env.hbm_gbs,
+                      "frac": (q_gbs / env.hbm_gbs) if q_gbs else None,
                       "bytes_per_element": 3, "bytes_per_row": 4},
         "kernel_ms": {f"{k[0]}:{k[1]}": 1e3 * statistics.mean(v) for k, v in kt.items()},
-        "gpu_launches": layer.launches_per_step() * args.steps,
-        "clocks": clk,
-        "wall_s_timed_region": wall,
+        "gpu_launches": layer.launches_per_step() * steps,
     }
+    if headline:
+        line["clocks"] = clk
+        line["wall_s_timed_region"] = wall
 
     # ---- LoRA launches (runtime adapters): bf16 tensor-core work, near the ridge
     lora_keys = [k for k in kt if k[0] == "lora"]
@@ -415,8 +521,8 @@ def main():
         l_fl, l_by = layer.lora_work()
         l_t = sum(statistics.mean(kt[k]) for k in lora_keys)
         line["lora"] = {"ms_per_step": 1e3 * l_t, "launches_per_step": len(lora_keys),
-                        "tflops": l_fl / l_t / 1e12, "tflops_frac": l_fl / l_t / 1e12 / bf16_peak,
-                        "gbs": l_by / l_t / 1e9, "gbs_frac": l_by / l_t / 1e9 / hbm_gbs,
+                        "tflops": l_fl / l_t / 1e12, "tflops_frac": l_fl / l_t / 1e12 / env.bf16_peak,
+                        "gbs": l_by / l_t / 1e9, "gbs_frac": l_by / l_t / 1e9 / env.hbm_gbs,
                         "flops_per_step": l_fl, "min_bytes_per_step": l_by,
                         "note": "2 M r (K + N) flops per adapter; bytes: x once per shrink launch, "
                                 "t written and read, y read and written (gate/up: base halves "
@@ -424,7 +530,9 @@ def main():
                                 "bandwidth"}
 
     # ---- the quantizer streaming: alone on 16 records of the widest activation
-    line["quantizer"]["stream"] = quantizer_stream(cfg, acts_np, dev, stream, flush, hbm_gbs, clef, torch)
+    if headline:
+        line["quantizer"]["stream"] = quantizer_stream(cfg, acts_np, dev, stream, flush, env.hbm_gbs,
+                                                       clef, torch)
 
     # ---- the same step replayed from a CUDA graph (launch overhead removed)
     layer.capture(acts)
@@ -432,7 +540,7 @@ def main():
     for _ in range(args.warmup):
         layer.replay()
     torch.cuda.synchronize(dev)
-    for _ in range(args.steps):
+    for _ in range(steps):
         flush.zero_()
         g0 = torch.cuda.Event(enable_timing=True)
         g1 = torch.cuda.Event(enable_timing=True)
@@ -442,33 +550,19 @@ def main():
         g_ev.append((g0, g1))
     torch.cuda.synchronize(dev)
     g_t = sum(a.elapsed_time(b) for a, b in g_ev) / 1e3
-    line["graph"] = {"value": ops_step * args.steps / g_t / 1e12, "unit": "TOPS",
-                     "ms_per_step": 1e3 * g_t / args.steps,
+    line["graph"] = {"value": ops_step * steps / g_t / 1e12, "unit": "TOPS",
+                     "ms_per_step": 1e3 * g_t / steps,
                      "note": "the step captured once in a CUDA graph and replayed (one launch per step)"}
 
     # ---- end to end through the C ABI with host buffers
-    if not args.no_e2e:
+    if headline and not args.no_e2e:
         line["e2e"] = e2e(args, layer, acts, acts_np, cfg, dev, stream, world, torch)
 
-    # ---- CPU oracle on a bounded sample (rank 0, N = 1): a probe of two rows
-    # per host thread sizes a sample of about CPU_SAMPLE_S seconds
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        threads = cpu_threads()
-        qw = oracle_weights(cfg, weights_np, threads)
-        probe = sample_rows(cfg, 2 * threads)
-        dt0, _ = oracle_sample(cfg, acts_np, weights_np, qw, lora_np, probe, threads)
-        n = int(min(cfg.M, max(len(probe), len(probe) * CPU_SAMPLE_S / max(dt0, 1e-3))))
-        rows = sample_rows(cfg, n)
-        dt, ops = oracle_sample(cfg, acts_np, weights_np, qw, lora_np, rows, threads)
-        line["cpu_baseline"] = {"value": ops / dt / 1e12, "unit": "TOPS", "cores": threads,
-                                "kind": "oracle",
-                                "sample": f"{len(rows)} of {cfg.M} token rows through every projection "
-                                          f"of {cfg.name} ({dt:.1f} s on {threads} threads)"}
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    if headline:
+        env.inputs = (acts_np, weights_np, lora_np)
+    del layer, acts, lora
+    torch.cuda.empty_cache()
+    return line
 
 
 def proj_input_K(cfg, act):

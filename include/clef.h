@@ -111,7 +111,10 @@ int clef_quant_act_static(const void *x, int64_t M, int64_t K, int64_t ldx, int 
  *   y[m][n]   = bf16(((float)acc * sx[m]) * sw[n] + bias[n])
  * qx: int8 [M][K] dense; sx: fp32 [M]; qw: int8 [N][K] dense; sw: fp32 [N];
  * bias: bf16 [N] or NULL; y: bf16 [M][N], row pitch ldy elements.
- * Requirements: K % 16 == 0, N % 8 == 0, ldy >= N, ldy % 8 == 0.
+ * Requirements: K % 16 == 0, N % 8 == 0, ldy >= N, ldy % 8 == 0.  The
+ * library receives bare pointers and cannot check buffer lengths: sx must
+ * hold M values and sw and bias N (the packed gate/up calls: 2N), else the
+ * kernels read past their ends.
  */
 int clef_w8a8_linear(const int8_t *qx, const float *sx, const int8_t *qw, const float *sw,
                      const void *bias, int64_t M, int64_t N, int64_t K,
@@ -257,7 +260,10 @@ int clef_w8a8_gemm_s32(const int8_t *qx, const int8_t *qw, int64_t M, int64_t N,
  * call before any stream capture.  All calls share the array and it keeps the
  * previous call's contents (nothing needs clearing: each call rewrites every
  * element it reads), so calls whose kernels may overlap on the GPU race and
- * must be serialised.  Other arguments and requirements as clef_lora_add.
+ * must be serialised.  It runs the same launches as clef_lora_add (tile
+ * widths, the clef_set_wait_limit_ns limit and the clef_test_force_timeout
+ * knob included), so its output bytes equal clef_lora_add's.  Other
+ * arguments and requirements as clef_lora_add.
  */
 int clef_lora_add_noalloc(const void *x, int64_t ldx, const void *A, const void *B,
                           int64_t M, int64_t K, int64_t N, int64_t r,
@@ -269,7 +275,9 @@ int clef_lora_add_noalloc(const void *x, int64_t ldx, const void *A, const void 
  * tiles across SMs when the last wave of whole 256 x 256 tiles would leave
  * more than 8% of the CTA pairs idle ("stream-K": the whole waves run as
  * whole tiles, the remaining tiles' K is dealt to all pairs in even runs of
- * at least 1024, and the pieces of a tile meet as exact int32 partial sums,
+ * at least 16 k-blocks of 64 (1,024 K elements; 8 k-blocks, 512 elements,
+ * for a launch of under one wave), and the pieces of a tile meet as exact
+ * int32 partial sums,
  * so the bytes of every output equal those of an unsplit launch).  The GEMM
  * time follows the number of tile waves (1502 x 5120 x 17408 and 1502 x 6400
  * x 17408 take the same time unsplit), so a shape with a partly empty last
@@ -296,6 +304,26 @@ int clef_gemm_workspace_bytes(int64_t *bytes);
 int clef_bind_workspace(void *stream, void *ws, int64_t bytes);
 
 /*
+ * clef_mma_peak -- dense tensor-core rate of this device for one instruction
+ * route, measured by the library's own microbenchmark (the denominators of
+ * the GEMMs' roofline fractions; not part of the projection path):
+ *   kind 0: tcgen05.mma kind::f16 with bf16 operands and an fp32 accumulator
+ *           (the route of the INT8 GEMMs, whose int8 codes are multiplied
+ *           exactly as fp16, and of the LoRA products);
+ *   kind 1: tcgen05.mma kind::f8f6f4 with e4m3 operands (the FP8 GEMMs);
+ *   kind 2: mma.sync m16n8k32 s8 x s8 -> s32 (the legacy integer route).
+ * The tcgen05 kinds run one CTA pair per two SMs issuing 256 x 256 MMAs back
+ * to back from shared memory into two TMEM accumulators (no copies); kind 2
+ * runs register-operand MMA chains in every warp.  One warm-up launch, then
+ * `iters` iterations (4 MMAs of 256 x 256 x 64 (bf16) or x 128 (e4m3) per
+ * iteration; 8 m16n8k32 MMAs per warp for kind 2) timed with CUDA events on
+ * a private stream; *tflops = 2 x multiply-adds / seconds / 1e12.
+ * Synchronises; not for use during stream capture.
+ * Requirements: kind in 0..2, 0 < iters <= 2^24.
+ */
+int clef_mma_peak(int kind, int64_t iters, double *tflops);
+
+/*
  * clef_poll_status -- synchronises the device, then returns and clears the
  * device-side status word (CLEF_OK if no kernel recorded an error).
  */
@@ -310,11 +338,14 @@ void clef_set_wait_limit_ns(uint64_t ns);
 
 /*
  * clef_test_force_timeout -- test knob for the device-side failure path.
- * While on (non-zero), the W8A8/FP8/LoRA GEMM kernels launched afterwards
- * make their MMA issuer wait on a barrier that nothing signals; the wait runs
- * out after the clef_set_wait_limit_ns limit, CLEF_ERR_TIMEOUT is recorded in
- * the status word and the kernel winds down (their outputs are then
- * undefined).  Off by default.
+ * on = 1: the W8A8/FP8/LoRA GEMM kernels launched afterwards make their MMA
+ * issuer wait on a barrier that nothing signals; the wait runs out after the
+ * clef_set_wait_limit_ns limit, CLEF_ERR_TIMEOUT is recorded in the status
+ * word and the kernel winds down (their outputs are then undefined).
+ * on = n >= 2: only the CTA (or CTA pair) working through tile-loop slot
+ * n - 2 does so, while the others finish their tiles (a stream-K launch then
+ * leaves the counters of the tiles that slot shared nonzero: the case
+ * clef_bind_workspace's refill rule is for).  0 (default) or negative: off.
  */
 void clef_test_force_timeout(int on);
 

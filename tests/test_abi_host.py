@@ -168,3 +168,11 @@ def test_python_binding_rejects_cpu_tensors():
     import torch
     with pytest.raises(ValueError):
         clef.quant_act(torch.zeros(4, 128, dtype=torch.bfloat16))
+
+
+@pytest.mark.parametrize("kind,iters,out", [(3, 10, True), (-1, 10, True), (0, 0, True), (1, 1 << 25, True),
+                                            (0, 10, False)])
+def test_mma_peak_rejects_bad_arguments(kind, iters, out):
+    d = C.c_double(0.0)
+    ptr = C.c_void_p(C.addressof(d)) if out else NUL
+    assert clef.library().clef_mma_peak(kind, iters, ptr) == 1

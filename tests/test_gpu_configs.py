@@ -16,7 +16,11 @@ from w8a8_quantized_projections_gb300.layer import QuantizedLayer
 
 pytestmark = pytest.mark.gpu
 
-ROWS = 12  # sampled token rows per workload (first, last and random ones)
+# rows checked per 128-row block (one CTA's tile rows, TMEM lanes 0..127): the
+# first and last (so both rows at every 256-row CTA-pair boundary) and one in
+# each middle lane quadrant; every row block is covered, so every stream-K
+# split tile and the partial last block are checked in the layer's own launches
+BLOCK_OFFSETS = (0, 37, 86, 127)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -28,9 +32,15 @@ def _gpu():
 
 
 def sample(M):
-    rng = np.random.default_rng(M)
-    mid = rng.choice(np.arange(1, M - 1), size=min(ROWS - 2, M - 2), replace=False)
-    return np.unique(np.concatenate([[0, M - 1], mid]))
+    """Rows 128 b + o for every block b and offset o (clipped to the last row),
+    whole rows so that every column tile is covered."""
+    rows = [min(M - 1, 128 * b + o) for b in range(-(-M // 128)) for o in BLOCK_OFFSETS]
+    return np.unique(np.array(rows, dtype=np.int64))
+
+
+def prow(fn, *arrays):
+    """fn over the sampled rows in threads: every array argument is row-sliced."""
+    return par_rows(lambda a, b: fn(*[x[a:b] for x in arrays]), arrays[0].shape[0])
 
 
 def lora_y_bound(t_ref, B, y_ref, K, r_pad, x, A):
@@ -90,7 +100,7 @@ def test_workload_full_size(orc, name, pack):
         if p.chained:
             # quantizer fed the GPU's own h; then the projection fed those codes
             h_rows = bf16_host(h_gpu)[rows]
-            rq, rs = qfn(h_rows)
+            rq, rs = prow(qfn, h_rows)
             gq, gs = layer.q[p.act]
             assert np.array_equal(host(gs)[rows], rs), "chained scales"
             assert np.array_equal(host(gq)[rows].view(rq.dtype), rq), "chained codes"
@@ -101,7 +111,8 @@ def test_workload_full_size(orc, name, pack):
         if p.kind == "gateup" and lora:
             # the packed base gate|up values (bit-exact INT8 linear)
             packed = bf16_host(out[p.name + "/packed"])[rows]
-            base = (orc.fp8_linear if fp8 else orc.int8_linear)(rq, rs, wq, ws, bias)
+            lin = orc.fp8_linear if fp8 else orc.int8_linear
+            base = prow(lambda q_, s_: lin(q_, s_, wq, ws, bias), rq, rs)
             assert np.array_equal(packed, base), "packed gate/up base"
             # the adapters' adds, through lora_add on the sampled rows (row-invariant
             # kernels), against the oracle; then the unfused SwiGLU against the oracle
@@ -110,8 +121,8 @@ def test_workload_full_size(orc, name, pack):
             for half, sl in (("gate", slice(0, p.N)), ("up", slice(p.N, 2 * p.N))):
                 A, B = lora_np[p.name + "/" + half]
                 clef.lora_add(bf16_dev(x), bf16_dev(A), bf16_dev(B), upd[:, sl])
-                t_ref = orc.lora_t(x, A)
-                y_ref = orc.lora_y(t_ref, B, np.ascontiguousarray(base[:, sl]))
+                t_ref = prow(lambda x_: orc.lora_t(x_, A), x)
+                y_ref = prow(lambda t_, b_: orc.lora_y(t_, B, b_), t_ref, np.ascontiguousarray(base[:, sl]))
                 tol = lora_y_bound(t_ref, B, y_ref, p.K, clef.lora_pad(A.shape[0]), x, A)
                 d = np.abs(S.bf16_bits_to_f64(bf16_host(upd)[:, sl]) - S.bf16_bits_to_f64(y_ref))
                 assert np.all(d <= tol), f"{p.name}/{half} lora: excess {(d - tol).max():.3g}"
@@ -123,7 +134,8 @@ def test_workload_full_size(orc, name, pack):
             h_gpu = out[p.name]
         elif p.kind == "gateup":
             h = bf16_host(out[p.name])[rows]
-            ref = (orc.fp8_gateup_swiglu if fp8 else orc.int8_gateup_swiglu)(rq, rs, wq, ws, bias)
+            gfn = orc.fp8_gateup_swiglu if fp8 else orc.int8_gateup_swiglu
+            ref = prow(lambda q_, s_: gfn(q_, s_, wq, ws, bias), rq, rs)
             if fp8:
                 from test_gpu_parity import assert_rms_close
                 assert_rms_close(h, ref, 1e-2, p.name)
@@ -132,12 +144,13 @@ def test_workload_full_size(orc, name, pack):
             h_gpu = out[p.name]
         else:
             y = bf16_host(out[p.name])[rows]
-            ref = (orc.fp8_linear if fp8 else orc.int8_linear)(rq, rs, wq, ws, bias)
+            lin = orc.fp8_linear if fp8 else orc.int8_linear
+            ref = prow(lambda q_, s_: lin(q_, s_, wq, ws, bias), rq, rs)
             if lora and p.name in lora_np:
                 A, B = lora_np[p.name]
                 x = acts_np[p.act][rows]
-                t_ref = orc.lora_t(x, A)
-                y_ref = orc.lora_y(t_ref, B, ref)
+                t_ref = prow(lambda x_: orc.lora_t(x_, A), x)
+                y_ref = prow(lambda t_, r_: orc.lora_y(t_, B, r_), t_ref, ref)
                 tol = lora_y_bound(t_ref, B, y_ref, p.K, clef.lora_pad(A.shape[0]), x, A)
                 d = np.abs(S.bf16_bits_to_f64(y) - S.bf16_bits_to_f64(y_ref))
                 assert np.all(d <= tol), f"{p.name} lora: excess {(d - tol).max():.3g}"

@@ -25,7 +25,7 @@ __all__ = [
     "lora_gateup_swiglu", "swiglu_bf16",
     "w8a8_gemm_s32",
     "poll_status", "set_wait_limit_ns", "set_quant_staging", "ACT_MODES", "gemm_workspace_bytes",
-    "bind_workspace",
+    "bind_workspace", "mma_peak",
 ]
 
 ACT_MODES = {"int8_h128": 0, "fp8": 1, "fp8_h128": 2}
@@ -73,6 +73,7 @@ def library():
                 "clef_lora_gateup_swiglu": [vp, i64, vp, vp, vp, vp, i64, i64, i64, i64, vp, vp, i64,
                                             vp, i64, vp],
                 "clef_w8a8_gemm_s32": [vp, vp, i64, i64, i64, vp, i64, vp],
+                "clef_mma_peak": [i32, i64, vp],
                 "clef_poll_status": [],
                 "clef_abi_version": [],
             }
@@ -161,15 +162,29 @@ def quant_act_static(x: torch.Tensor, s: float, mode: str = "fp8", q=None, scale
 
 
 def _w8a8(name, codes, qx, sx, qw, sw, bias, out, n_out, stream):
+    """The library takes bare pointers and cannot check buffer lengths, so
+    they are checked here: a short scale or bias vector would be read past
+    its end by the epilogue."""
     _cuda(qx, "qx", codes)
     _cuda(qw, "qw", codes)
     _dense(qx, "qx"); _dense(qw, "qw")
+    if qx.dim() != 2 or qw.dim() != 2:
+        raise ValueError("qx and qw must be 2-D")
     _cuda(sx, "sx", (torch.float32,)); _cuda(sw, "sw", (torch.float32,))
-    if bias is not None:
-        _cuda(bias, "bias", (torch.bfloat16,))
+    _dense(sx, "sx"); _dense(sw, "sw")
     M, K = qx.shape
+    rows = qw.shape[0]
     if qw.shape[1] != K:
         raise ValueError("qx and qw disagree on K")
+    if sx.numel() != M:
+        raise ValueError(f"sx has {sx.numel()} values for {M} rows of qx")
+    if sw.numel() != rows:
+        raise ValueError(f"sw has {sw.numel()} values for {rows} weight rows")
+    if bias is not None:
+        _cuda(bias, "bias", (torch.bfloat16,))
+        _dense(bias, "bias")
+        if bias.numel() != rows:
+            raise ValueError(f"bias has {bias.numel()} values for {rows} weight rows")
     if out is None:
         out = torch.empty((M, n_out), dtype=torch.bfloat16, device=qx.device)
     _cuda(out, "out", (torch.bfloat16,))
@@ -184,8 +199,15 @@ def w8a8_linear(qx, sx, qw, sw, bias=None, y=None, stream=None):
     return _w8a8("clef_w8a8_linear", (torch.int8,), qx, sx, qw, sw, bias, y, qw.shape[0], stream)
 
 
+def _gateup_half(qw_gu) -> int:
+    if qw_gu.dim() != 2 or qw_gu.shape[0] % 2 != 0:
+        raise ValueError("packed gate/up weights need an even row count (gate rows, then up rows)")
+    return qw_gu.shape[0] // 2
+
+
 def w8a8_gateup_swiglu(qx, sx, qw_gu, sw_gu, bias_gu=None, h=None, stream=None):
     """h = bf16(silu(g) * u) for packed gate/up INT8 weights [2N][K]."""
+    _gateup_half(qw_gu)
     return _w8a8("clef_w8a8_gateup_swiglu", (torch.int8,), qx, sx, qw_gu, sw_gu, bias_gu, h,
                  qw_gu.shape[0] // 2, stream)
 
@@ -195,6 +217,7 @@ def fp8_linear(qx, sx, qw, sw, bias=None, y=None, stream=None):
 
 
 def fp8_gateup_swiglu(qx, sx, qw_gu, sw_gu, bias_gu=None, h=None, stream=None):
+    _gateup_half(qw_gu)
     return _w8a8("clef_fp8_gateup_swiglu", _FP8, qx, sx, qw_gu, sw_gu, bias_gu, h,
                  qw_gu.shape[0] // 2, stream)
 
@@ -352,6 +375,18 @@ def swiglu_bf16(y_gu, h=None, stream=None):
     return h
 
 
+MMA_KINDS = {"bf16": 0, "e4m3": 1, "s8_mma_sync": 2}
+
+
+def mma_peak(kind: str, iters: int = 200_000) -> float:
+    """Dense tensor-core rate (TFLOP/s) of one instruction route on the
+    current device, from the library's microbenchmark: "bf16" (tcgen05
+    kind::f16), "e4m3" (tcgen05 kind::f8f6f4) or "s8_mma_sync"."""
+    out = C.c_double(0.0)
+    _call("clef_mma_peak", MMA_KINDS[kind], int(iters), C.c_void_p(C.addressof(out)))
+    return out.value
+
+
 def poll_status() -> int:
     """Synchronise and return (then clear) the device-side status word."""
     return int(library().clef_poll_status())
@@ -371,9 +406,11 @@ def set_quant_staging(mode: int) -> None:
     L.clef_set_quant_staging(int(mode))
 
 
-def test_force_timeout(on: bool) -> None:
-    """Test knob: make the GEMM kernels' MMA issuer wait on a barrier nothing signals."""
+def test_force_timeout(on) -> None:
+    """Test knob: make the GEMM kernels' MMA issuer wait on a barrier nothing
+    signals.  True / 1: every CTA; an int n >= 2: only the CTA (pair) of
+    tile-loop slot n - 2; False / 0: off."""
     L = library()
     L.clef_test_force_timeout.argtypes = [C.c_int]
     L.clef_test_force_timeout.restype = None
-    L.clef_test_force_timeout(1 if on else 0)
+    L.clef_test_force_timeout(int(on) if not isinstance(on, bool) else (1 if on else 0))

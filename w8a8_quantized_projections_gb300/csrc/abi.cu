@@ -245,6 +245,16 @@ int internal_device(int *num_sms, unsigned int **status) {
     return CLEF_OK;
 }
 
+int internal_lora_add(const void *x, int64_t ldx, const void *A, const void *B, int64_t M, int64_t K,
+                      int64_t N, int64_t r, void *t, void *y, int64_t ldy, cudaStream_t st) {
+    DeviceState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc) return rc;
+    const int64_t r_pad = (r + 63) / 64 * 64;
+    if ((rc = lora_shrink_launch(d, x, ldx, A, M, K, r, t, r_pad, st))) return rc;
+    return lora_expand_launch(d, t, r_pad, B, M, N, r, y, ldy, st);
+}
+
 int internal_make_tmap(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
                        uint64_t rows, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows,
                        CUtensorMapSwizzle sw) {
@@ -377,13 +387,7 @@ int clef_lora_add(const void *x, int64_t ldx, const void *A, const void *B, int6
     if (!x || !A || !B || !t_scratch || !y) return arg_fail("null pointer");
     if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(t_scratch) || !aligned16(y))
         return arg_fail("pointers must be 16-byte aligned");
-    DeviceState *d = nullptr;
-    int rc = device_state(&d);
-    if (rc) return rc;
-    const int64_t r_pad = (r + 63) / 64 * 64;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if ((rc = lora_shrink_launch(d, x, ldx, A, M, K, r, t_scratch, r_pad, st))) return rc;
-    return lora_expand_launch(d, t_scratch, r_pad, B, M, N, r, y, ldy, st);
+    return internal_lora_add(x, ldx, A, B, M, K, N, r, t_scratch, y, ldy, static_cast<cudaStream_t>(stream));
 }
 
 int clef_lora_shrink(const void *x, int64_t ldx, const void *A, int64_t M, int64_t K, int64_t r,
@@ -533,7 +537,7 @@ int clef_poll_status(void) {
 
 void clef_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
 
-void clef_test_force_timeout(int on) { g_force_timeout.store(on ? 1 : 0); }
+void clef_test_force_timeout(int on) { g_force_timeout.store(on < 0 ? 0 : on); }
 
 void clef_set_quant_staging(int mode) { g_quant_staging.store(mode < 0 ? 0 : (mode > 2 ? 2 : mode)); }
 

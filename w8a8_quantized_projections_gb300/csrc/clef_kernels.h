@@ -57,7 +57,8 @@ struct GemmArgs {
     unsigned int *status;    // device status word
     uint64_t wait_limit_ns;
     int *dbg;                // optional: per CTA, its own TMEM base and the one it uses
-    int force_timeout;       // test knob: make the MMA issuer's wait run out
+    int force_timeout;       // test knob: 1 = every CTA's MMA issuer waits on a barrier
+                             // nothing signals; n >= 2: only the CTA (pair) of tile-loop slot n - 2
     // kEpiLoraSwiGLU: the base gate|up values (bf16 [M][2 * n_half], pitch
     // ld_aux elements), and the K offset of the up half's factor: up rows of
     // the B operand come from the second tensor map at K coordinate k - k_shift
@@ -115,6 +116,11 @@ cudaError_t launch_swiglu_bf16(const uint16_t *y_gu, int64_t M, int64_t N, int64
 // set-up (SM count, status-word address), TMA tensor maps, and the calling
 // thread's last-error text.
 int internal_device(int *num_sms, unsigned int **status);
+// clef_lora_add's two launches (arguments already checked) with t at the
+// given dense [M][round_up(r, 64)] scratch: the same tile widths, wait limit
+// and test knob as the public call.
+int internal_lora_add(const void *x, int64_t ldx, const void *A, const void *B, int64_t M, int64_t K,
+                      int64_t N, int64_t r, void *t, void *y, int64_t ldy, cudaStream_t st);
 int internal_make_tmap(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
                        uint64_t rows, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows,
                        CUtensorMapSwizzle sw);

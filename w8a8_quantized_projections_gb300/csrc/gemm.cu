@@ -391,7 +391,7 @@ struct Gemm {
         int slot, nslots;    // tile-loop start and stride
         int num_m, num_n, num_tiles, nkb;
         int n_fastest;       // tile order: 0 = M fastest, 1 = N fastest
-        int force_timeout;   // test knob: the MMA issuer waits on a barrier nothing signals
+        int force_timeout;   // test knob: this CTA's MMA issuer waits on a barrier nothing signals
         WaitCtx w;
     };
 
@@ -1263,7 +1263,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     c.nkb = C::kI8 ? (args.K + 63) / 64 : (args.K + C::BK - 1) / C::BK;
     c.n_fastest = args.n_fastest;
 
-    c.force_timeout = args.force_timeout;
+    c.force_timeout = args.force_timeout == 1 || (args.force_timeout >= 2 && args.force_timeout - 2 == c.slot);
     c.w.limit_ns = args.wait_limit_ns;
     c.w.abort = &bar->abort;
     c.w.status = args.status;

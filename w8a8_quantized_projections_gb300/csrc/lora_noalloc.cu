@@ -103,35 +103,11 @@ extern "C" int clef_lora_add_noalloc(const void *x, int64_t ldx, const void *A, 
         return fail("invalid argument: pointers must be 16-byte aligned");
     int num_sms = 0;
     unsigned int *status = nullptr;
-    int rc = internal_device(&num_sms, &status);
+    int rc = internal_device(&num_sms, &status);   // device checks (sm_103) first
     if (rc) return rc;
     uint16_t *t = nullptr;
     if ((rc = scratch_address(&t))) return rc;
-
-    const int bn = lora_shrink_width(M, r_pad, num_sms, 0);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    GemmArgs a1 = {};
-    a1.M = (int)M;
-    a1.N = (int)r_pad;
-    a1.K = (int)K;
-    a1.out = t;
-    a1.ldo = r_pad;
-    a1.n_fastest = 1;
-    a1.status = status;
-    a1.wait_limit_ns = 1000000000ull;
-    rc = launch_gemm(kOpBF16, kEpiStoreBF16, bn, Operand{x, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2},
-                     Operand{A, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2}, a1, num_sms, st);
-    if (rc) return rc;
-    GemmArgs a2 = {};
-    a2.M = (int)M;
-    a2.N = (int)N;
-    a2.K = (int)r_pad;
-    a2.out = y;
-    a2.ldo = ldy;
-    a2.n_fastest = 1;
-    a2.status = status;
-    a2.wait_limit_ns = 1000000000ull;
-    return launch_gemm(kOpBF16, kEpiAddBF16, 128,
-                       Operand{t, (uint64_t)r_pad, (uint64_t)M, (uint64_t)r_pad * 2},
-                       Operand{B, (uint64_t)r, (uint64_t)N, (uint64_t)r * 2}, a2, num_sms, st);
+    // the launches of clef_lora_add (tile widths, wait limit and test knob
+    // included), on the built-in array in place of a caller scratch
+    return internal_lora_add(x, ldx, A, B, M, K, N, r, t, y, ldy, static_cast<cudaStream_t>(stream));
 }

@@ -36,8 +36,10 @@ from typing import Dict, Optional, Tuple
 import torch
 
 from . import (bind_workspace, fp8_gateup_swiglu, fp8_linear, gemm_workspace_bytes, lora_add,
-               lora_expand_add, lora_gateup_swiglu, lora_pad, lora_shrink, quant_act, w8a8_gateup_swiglu,
-               w8a8_linear)
+               lora_expand_add, lora_gateup_swiglu, lora_pad, lora_shrink, poll_status, quant_act,
+               w8a8_gateup_swiglu, w8a8_linear)
+
+TIMEOUT = 4   # CLEF_ERR_TIMEOUT
 
 
 class QuantizedLayer:
@@ -263,6 +265,20 @@ class QuantizedLayer:
                         lora_add(acts[p.act] if not p.chained else prev_h, A, B, y,
                                  t_scratch=self._t(A))
         return self.out
+
+    def poll_status(self) -> int:
+        """Synchronise, then return (and clear) the library's device status
+        word.  After a device-side time-out the stream-K workspace may hold
+        arrival counts of pieces that never arrived (a CTA pair that gave up
+        partway through a split tile), which would make a later launch finish
+        that tile early or never; so on CLEF_ERR_TIMEOUT the workspace is
+        refilled with zeros here, before any further step (a captured graph
+        keeps the same buffer, so its replays see the refill too)."""
+        st = poll_status()
+        if st == TIMEOUT and self.ws is not None:
+            self.ws.zero_()
+            torch.cuda.synchronize(self.ws.device)
+        return st
 
     def capture(self, acts: Dict[str, torch.Tensor]) -> "torch.cuda.CUDAGraph":
         """Record one step on ``acts`` into a CUDA graph (after a warm-up step
