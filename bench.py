@@ -42,6 +42,7 @@ METRIC = "W8A8 linear TOPS & % of GB300 dense INT8/FP8 peak; quantizer GB/s vs H
 L2_FLUSH_BYTES = 256 << 20
 CPU_SAMPLE_S = 10.0   # target length of the timed oracle sample
 INSTRUMENTED_STEPS = 100   # steps of the per-kernel timing pass
+HOST_AHEAD_CYCLES = 2_000_000   # about 1 ms of device sleep before each instrumented step
 
 
 def parse():
@@ -449,10 +450,14 @@ def measure(env, cfg, steps, headline):
         raise RuntimeError(f"device status word reported {status}")
     # per-kernel times from a separate pass with an event pair around every
     # launch (the events themselves cost about 2 us each, so the timed steps
-    # above carry only the step's own pair)
+    # above carry only the step's own pair); each instrumented step is queued
+    # behind a short device sleep so that the host has issued all of its
+    # launches before the first one starts, and no host gap sits between an
+    # event pair
     n_inst = min(steps, INSTRUMENTED_STEPS)
     for _ in range(n_inst):
         flush.zero_()
+        torch.cuda._sleep(HOST_AHEAD_CYCLES)
         layer.step(acts, events=events)
     torch.cuda.synchronize(dev)
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
@@ -463,9 +468,10 @@ def measure(env, cfg, steps, headline):
 
     kt = {key: [a.elapsed_time(b) / 1e3 for a, b in lst] for key, lst in events.items()}
     gemm_keys = [k for k in kt if k[0] == "gemm"]
-    units = {u[0]: u for u in layer.units()}   # name -> (name, weight rows, K, ops)
+    units = {u[0]: u for u in layer.units()}   # name -> (name, weight rows, K, ops, fused LoRA flops)
     dom = max(gemm_keys, key=lambda k: sum(kt[k]))
-    dom_name, dom_rows, dom_K, dom_ops = units[dom[1]]
+    dom_name, dom_rows, dom_K, dom_base, dom_lora = units[dom[1]]
+    dom_ops = dom_base + dom_lora   # a fused LoRA expand's tensor work is part of the launch
     dom_t = statistics.mean(kt[dom])
     achieved = dom_ops / dom_t / 1e12
     peak, peak_source = env.tensor_peak(cfg.scheme)
@@ -481,9 +487,11 @@ def measure(env, cfg, steps, headline):
     gemm_tops = ops_step * n_inst / gemm_time / 1e12
     gemms = {}
     for k in gemm_keys:
-        _, rows, K, ops = units[k[1]]
+        _, rows, K, base, lora_fl = units[k[1]]
+        ops = base + lora_fl
         t = statistics.mean(kt[k])
         gemms[k[1]] = {"shape": f"{cfg.M}x{rows}x{K}", "ms": 1e3 * t, "tops": ops / t / 1e12,
+                       "fused_lora_flops": lora_fl,
                        "frac": ops / t / 1e12 / peak,
                        "frac_of_microbenchmark": ops / t / 1e12 / env.mma["e4m3" if cfg.scheme == "fp8" else "bf16"]}
 
@@ -500,7 +508,7 @@ def measure(env, cfg, steps, headline):
             "frac": achieved / peak,
             "traffic": measured_traffic(cfg, dom_name) if headline else None,
             "traffic_unit": "bytes per launch",
-            "ops_per_launch": dom_ops, "launch_ms": 1e3 * dom_t,
+            "ops_per_launch": dom_ops, "fused_lora_flops_per_launch": dom_lora, "launch_ms": 1e3 * dom_t,
             "peak_source": peak_source,
         },
         "gemm_only_tops": gemm_tops,
@@ -524,10 +532,12 @@ def measure(env, cfg, steps, headline):
                         "tflops": l_fl / l_t / 1e12, "tflops_frac": l_fl / l_t / 1e12 / env.bf16_peak,
                         "gbs": l_by / l_t / 1e9, "gbs_frac": l_by / l_t / 1e9 / env.hbm_gbs,
                         "flops_per_step": l_fl, "min_bytes_per_step": l_by,
-                        "note": "2 M r (K + N) flops per adapter; bytes: x once per shrink launch, "
-                                "t written and read, y read and written (gate/up: base halves "
-                                "read, h written); against the bf16 burst peak and the copy "
-                                "bandwidth"}
+                        "note": ("LoRA expands fused into the INT8 GEMMs: these launches are the x A^T "
+                                 "shrinks (2 M r K flops per adapter; x read, t written); the expand's "
+                                 "2 M N r flops count in the GEMMs' figures" if layer.fused else
+                                 "2 M r (K + N) flops per adapter; bytes: x once per shrink launch, "
+                                 "t written and read, y read and written (gate/up: base halves "
+                                 "read, h written)") + "; against the bf16 burst peak and the copy bandwidth"}
 
     # ---- the quantizer streaming: alone on 16 records of the widest activation
     if headline:

@@ -175,6 +175,33 @@ int clef_lora_add(const void *x, int64_t ldx, const void *A, const void *B,
                   void *t_scratch, void *y, int64_t ldy, void *stream);
 
 /*
+ * clef_w8a8_linear_lora -- the INT8 linear with the runtime LoRA expand
+ * fused into the same GEMM [LORA; INT8: Benefits].  t = bf16(x A^T) comes
+ * from a clef_lora_shrink call made before (t's columns past r must be
+ * finite); each output tile accumulates t B^T as a last bf16 tensor-core
+ * chunk, and its epilogue adds it to the rounded base value, so y is never
+ * written and read back between the two:
+ *   y[m][n] = bf16(bf16(((float)acc * sx[m]) * sw[n] + bias[n])
+ *                  + sum_{j<r} t[m][tcol(n) + j] * B[n][j])
+ * -- the same bytes as clef_w8a8_linear followed by clef_lora_expand_add from
+ * t + tcol(n).  B: bf16 [N][r] dense (for packed projections, the adapters'
+ * B factors stacked in output-column order; zero rows for columns without
+ * an adapter).  nseg (0..4) column segments map output columns to t columns:
+ * columns below seg_end[i] (and at or above seg_end[i-1]) read t columns
+ * seg_tcol[i] .. seg_tcol[i] + r_pad - 1 (r_pad = r rounded up to 64);
+ * nseg = 0 means one segment at t column 0.  seg_end increasing, every end
+ * but the last a multiple of 256, the last equal to N; seg_tcol multiples of
+ * 8 with seg_tcol + r_pad <= ldt.  t: bf16, row pitch ldt (multiple of 8).
+ * Other arguments and requirements as clef_w8a8_linear; 0 < r <= 1024,
+ * r % 8 == 0.  This call never splits tiles across SMs (no stream-K
+ * workspace is used).
+ */
+int clef_w8a8_linear_lora(const int8_t *qx, const float *sx, const int8_t *qw, const float *sw,
+                          const void *bias, int64_t M, int64_t N, int64_t K, const void *t, int64_t ldt,
+                          const void *B, int64_t r, int nseg, const int64_t *seg_end,
+                          const int64_t *seg_tcol, void *y, int64_t ldy, void *stream);
+
+/*
  * clef_lora_shrink / clef_lora_expand_add -- the two stages of clef_lora_add
  * as separate calls [LORA], for adapters that share an input: with their A
  * factors stacked (each zero-padded to a multiple of 64 rows) one shrink

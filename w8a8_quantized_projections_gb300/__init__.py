@@ -23,7 +23,7 @@ __all__ = [
     "ClefError", "library", "library_path", "quant_act", "quant_act_static", "w8a8_linear", "w8a8_gateup_swiglu",
     "fp8_linear", "fp8_gateup_swiglu", "lora_add", "lora_add_noalloc", "lora_shrink", "lora_expand_add",
     "lora_gateup_swiglu", "swiglu_bf16",
-    "w8a8_gemm_s32",
+    "w8a8_gemm_s32", "w8a8_linear_lora",
     "poll_status", "set_wait_limit_ns", "set_quant_staging", "ACT_MODES", "gemm_workspace_bytes",
     "bind_workspace", "mma_peak",
 ]
@@ -73,6 +73,8 @@ def library():
                 "clef_lora_gateup_swiglu": [vp, i64, vp, vp, vp, vp, i64, i64, i64, i64, vp, vp, i64,
                                             vp, i64, vp],
                 "clef_w8a8_gemm_s32": [vp, vp, i64, i64, i64, vp, i64, vp],
+                "clef_w8a8_linear_lora": [vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp, i64, i32, vp, vp,
+                                          vp, i64, vp],
                 "clef_mma_peak": [i32, i64, vp],
                 "clef_poll_status": [],
                 "clef_abi_version": [],
@@ -162,6 +164,18 @@ def quant_act_static(x: torch.Tensor, s: float, mode: str = "fp8", q=None, scale
 
 
 def _w8a8(name, codes, qx, sx, qw, sw, bias, out, n_out, stream):
+    _w8a8_checks(codes, qx, sx, qw, sw, bias)
+    M, K = qx.shape
+    if out is None:
+        out = torch.empty((M, n_out), dtype=torch.bfloat16, device=qx.device)
+    _cuda(out, "out", (torch.bfloat16,))
+    ldo = _rows(out, "out")
+    _call(name, _ptr(qx), _ptr(sx), _ptr(qw), _ptr(sw), _ptr(bias), M, n_out, K, _ptr(out), ldo,
+          _stream(qx, stream))
+    return out
+
+
+def _w8a8_checks(codes, qx, sx, qw, sw, bias):
     """The library takes bare pointers and cannot check buffer lengths, so
     they are checked here: a short scale or bias vector would be read past
     its end by the epilogue."""
@@ -185,13 +199,6 @@ def _w8a8(name, codes, qx, sx, qw, sw, bias, out, n_out, stream):
         _dense(bias, "bias")
         if bias.numel() != rows:
             raise ValueError(f"bias has {bias.numel()} values for {rows} weight rows")
-    if out is None:
-        out = torch.empty((M, n_out), dtype=torch.bfloat16, device=qx.device)
-    _cuda(out, "out", (torch.bfloat16,))
-    ldo = _rows(out, "out")
-    _call(name, _ptr(qx), _ptr(sx), _ptr(qw), _ptr(sw), _ptr(bias), M, n_out, K, _ptr(out), ldo,
-          _stream(qx, stream))
-    return out
 
 
 def w8a8_linear(qx, sx, qw, sw, bias=None, y=None, stream=None):
@@ -220,6 +227,52 @@ def fp8_gateup_swiglu(qx, sx, qw_gu, sw_gu, bias_gu=None, h=None, stream=None):
     _gateup_half(qw_gu)
     return _w8a8("clef_fp8_gateup_swiglu", _FP8, qx, sx, qw_gu, sw_gu, bias_gu, h,
                  qw_gu.shape[0] // 2, stream)
+
+
+def _lora_t(t, B, r_cols, M):
+    _cuda(t, "t", (torch.bfloat16,))
+    _cuda(B, "B", (torch.bfloat16,))
+    _dense(B, "B")
+    if t.dim() != 2 or t.shape[0] != M or t.shape[1] < r_cols:
+        raise ValueError(f"t must have {M} rows and at least {r_cols} columns")
+    return _rows(t, "t")
+
+
+def w8a8_linear_lora(qx, sx, qw, sw, bias, t, B, y=None, segments=None, stream=None):
+    """INT8 linear with the LoRA expand fused: y = bf16(bf16(linear) + t B^T),
+    the bytes of w8a8_linear followed by lora_expand_add.  t: bf16 [M][>= r_pad]
+    from lora_shrink; B: bf16 [N][r] (adapters stacked in output order for a
+    packed projection).  segments: optional [(column end, t column)] pairs
+    (at most 4) mapping output column ranges to their adapter's t columns."""
+    N, r = B.shape
+    if qw.shape[0] != N:
+        raise ValueError("B must have one row per output column")
+    segs = list(segments) if segments else []
+    if len(segs) > 4:
+        raise ValueError("at most 4 segments")
+    tmax = max([c for _, c in segs], default=0) + lora_pad(r)
+    ldt = _lora_t(t, B, tmax, qx.shape[0])
+    ends = (C.c_int64 * 4)(*[e for e, _ in segs] + [0] * (4 - len(segs)))
+    cols = (C.c_int64 * 4)(*[c for _, c in segs] + [0] * (4 - len(segs)))
+    return _w8a8_lora("clef_w8a8_linear_lora", qx, sx, qw, sw, bias, y, N, stream,
+                      (_ptr(t), ldt, _ptr(B), r, len(segs), ends, cols))
+
+
+def _w8a8_lora(name, qx, sx, qw, sw, bias, out, n_out, stream, lora_args):
+    # the same checks as the plain calls (lengths the C ABI cannot see)
+    _w8a8_checks((torch.int8,), qx, sx, qw, sw, bias)
+    M, K = qx.shape
+    if out is None:
+        out = torch.empty((M, n_out), dtype=torch.bfloat16, device=qx.device)
+    _cuda(out, "out", (torch.bfloat16,))
+    ldo = _rows(out, "out")
+    L = library()
+    fn = getattr(L, name)
+    rc = fn(_ptr(qx), _ptr(sx), _ptr(qw), _ptr(sw), _ptr(bias), M, n_out, K, *lora_args, _ptr(out), ldo,
+            _stream(qx, stream))
+    if rc != 0:
+        raise ClefError(name, rc, L.clef_last_error().decode(errors="replace"))
+    return out
 
 
 def w8a8_gemm_s32(qx, qw, acc=None, stream=None):

@@ -233,6 +233,65 @@ int run_w8a8(int op, int epi, const void *qx, const float *sx, const void *qw, c
     return launch_gemm(op, epi, 256, A, B, a, d->num_sms, static_cast<cudaStream_t>(stream));
 }
 
+// The INT8 linear with the LoRA expand fused (checks, then one launch): nseg
+// column segments of the output read t at their own column offsets (nseg = 0:
+// one segment at column 0).
+int run_w8a8_lora(const void *qx, const float *sx, const void *qw, const float *sw, const void *bias,
+                  int64_t M, int64_t N, int64_t K, const void *t, int64_t ldt, const void *B, int64_t r,
+                  int nseg, const int64_t *seg_end, const int64_t *seg_tcol, void *out, int64_t ldo,
+                  void *stream) {
+    bool empty = false;
+    int rc = check_gemm(qx, sx, qw, sw, bias, M, N, K, out, ldo, true, &empty);
+    if (rc) return rc;
+    if (r <= 0 || r > 1024 || r % 8 != 0) return arg_fail("rank must be in (0, 1024] and a multiple of 8");
+    const int64_t r_pad = (r + 63) / 64 * 64;
+    if (ldt <= 0 || ldt % 8 != 0 || ldt > kMaxDim) return arg_fail("ldt must be a positive multiple of 8");
+    GemmArgs a;
+    memset(&a, 0, sizeof a);
+    if (nseg < 0 || nseg > kLoraMaxSegs) return arg_fail("nseg must be in 0..4");
+    if (nseg > 0 && (!seg_end || !seg_tcol)) return arg_fail("null segment array");
+    const int n = nseg > 0 ? nseg : 1;
+    int64_t prev = 0;
+    for (int i = 0; i < n; ++i) {
+        const int64_t end = nseg > 0 ? seg_end[i] : N;
+        const int64_t tc = nseg > 0 ? seg_tcol[i] : 0;
+        if (end <= prev || end > N) return arg_fail("segment ends must increase and stay within N");
+        if (i + 1 < n && end % 256 != 0) return arg_fail("segment ends other than the last must be multiples of 256");
+        if (i + 1 == n && end != N) return arg_fail("the last segment must end at N");
+        if (tc < 0 || tc % 8 != 0 || tc + r_pad > ldt)
+            return arg_fail("segment t columns must be multiples of 8 with tcol + round_up(r, 64) <= ldt");
+        a.lora_seg_end[i] = (int)end;
+        a.lora_seg_tcol[i] = (int)tc;
+        prev = end;
+    }
+    a.lora_nseg = n;
+    if (empty) return CLEF_OK;
+    if (!t || !B) return arg_fail("null LoRA pointer");
+    if (!aligned16(t) || !aligned16(B)) return arg_fail("LoRA pointers must be 16-byte aligned");
+    DeviceState *d = nullptr;
+    if ((rc = device_state(&d))) return rc;
+    const GemmArgs b = base_args(d, M, N, K);
+    a.M = b.M;
+    a.N = b.N;
+    a.K = b.K;
+    a.status = b.status;
+    a.wait_limit_ns = b.wait_limit_ns;
+    a.force_timeout = b.force_timeout;
+    a.sa = sx;
+    a.sb = sw;
+    a.bias = static_cast<const uint16_t *>(bias);
+    a.out = out;
+    a.ldo = ldo;
+    a.lora_t = t;
+    a.lora_ldt = ldt;
+    a.lora_b = B;
+    a.lora_r = (int)r;
+    a.lora_nkb = (int)(r_pad / 64);
+    const Operand A = {qx, (uint64_t)K, (uint64_t)M, (uint64_t)K};
+    const Operand W = {qw, (uint64_t)K, (uint64_t)N, (uint64_t)K};
+    return launch_gemm(kOpI8, kEpiScaleBiasLora, 256, A, W, a, d->num_sms, static_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 // Internal services for other translation units of this library.
@@ -368,6 +427,13 @@ int clef_fp8_gateup_swiglu(const void *qx, const float *sx, const void *qw_gu, c
                            const void *bias_gu, int64_t M, int64_t N, int64_t K, void *h,
                            int64_t ldh, void *stream) {
     return run_w8a8(kOpF8, kEpiSwiGLU, qx, sx, qw_gu, sw_gu, bias_gu, M, N, K, h, ldh, stream);
+}
+
+int clef_w8a8_linear_lora(const int8_t *qx, const float *sx, const int8_t *qw, const float *sw,
+                          const void *bias, int64_t M, int64_t N, int64_t K, const void *t, int64_t ldt,
+                          const void *B, int64_t r, int nseg, const int64_t *seg_end,
+                          const int64_t *seg_tcol, void *y, int64_t ldy, void *stream) {
+    return run_w8a8_lora(qx, sx, qw, sw, bias, M, N, K, t, ldt, B, r, nseg, seg_end, seg_tcol, y, ldy, stream);
 }
 
 int clef_w8a8_gemm_s32(const int8_t *qx, const int8_t *qw, int64_t M, int64_t N, int64_t K,

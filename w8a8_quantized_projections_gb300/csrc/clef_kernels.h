@@ -44,7 +44,15 @@ enum GemmEpi : int {
     kEpiLoraSwiGLU = 5, // gate/up LoRA adds then SwiGLU: g = bf16(yg + acc_g),
                         // u = bf16(yu + acc_u), h = bf16(silu(g) * u); yg|yu read
                         // from aux, h written to out (bf16 operands only)
+    // INT8 linear with the runtime LoRA expand fused (a last bf16 accumulator
+    // chunk per tile, lora = t B^T over the padded rank):
+    kEpiScaleBiasLora = 6,  // y = bf16(bf16((acc * sa) * sb + bias) + lora)
 };
+
+// Column segments of a fused LoRA expand: output columns below seg_end[i]
+// (and at or above seg_end[i - 1]) read t's columns seg_tcol[i] ..
+// seg_tcol[i] + r_pad - 1 (adapters of a packed projection group).
+constexpr int kLoraMaxSegs = 4;
 
 struct GemmArgs {
     int M, N, K;             // output rows, output columns (h columns for SwiGLU), depth
@@ -81,6 +89,17 @@ struct GemmArgs {
     int *sk_cnt;
     int4 *sk_ws;
     int64_t sk_ws_bytes;
+    // fused LoRA expand (kEpiScaleBiasLora): lora_t is t (bf16 [M][lora_ldt]),
+    // lora_b the B factor (bf16 [N][lora_r]); lora_nkb: bf16 k-blocks of 64
+    // per tile (r_pad / 64)
+    const void *lora_t;
+    int64_t lora_ldt;
+    const void *lora_b;
+    int lora_r;
+    int lora_nkb;
+    int lora_nseg;
+    int lora_seg_end[kLoraMaxSegs];
+    int lora_seg_tcol[kLoraMaxSegs];
 };
 
 // Stream-K workspace: counters for up to kSkMaxTiles tiles, then per CTA pair

@@ -117,11 +117,18 @@ struct Cfg {
     static constexpr int kColsPerThread = BN / kParts;     // columns one epilogue thread owns
     static constexpr int kChunks32 = kColsPerThread / 32;
     static constexpr bool kSwiGLU = (EPI == kEpiSwiGLU || EPI == kEpiLoraSwiGLU);  // gate|up tile
+    // INT8 with the LoRA expand fused: after a tile's INT8 k-blocks, the
+    // producer loads the tile's t rows and B-factor rows (bf16) by TMA straight
+    // into the fp16 operand ring, the converters pass those stages through,
+    // and the MMA issuer accumulates t B^T as the tile's last chunk
+    static constexpr bool kLoraFused = (EPI == kEpiScaleBiasLora);
+    // epilogues that apply the row and column scales and the bias
+    static constexpr bool kScaled = (EPI == kEpiScaleBias || EPI == kEpiSwiGLU || EPI == kEpiScaleBiasLora);
     // INT8 stream-K is compiled into the pair kernels (exact int32 pieces)
     // but not the SwiGLU one: the gate/up launches of the workloads fill at
     // least 94% of their last wave, and with the split path compiled in the
     // unsplit gate/up kernel ran 1.2% slower (352.7 against 344.5 us)
-    static constexpr bool kStreamK = kI8 && PAIR && !kSwiGLU;
+    static constexpr bool kStreamK = kI8 && PAIR && !kSwiGLU && !kLoraFused;
     static constexpr int kOutColsPerTile = kSwiGLU ? BN / 2 : BN;
     // full[s]: TMA (native) or the local converter warps (INT8); in pair mode
     // the leader's barrier also counts the peer's forwarded readiness.
@@ -148,6 +155,8 @@ struct Cfg {
     // stream-K counters and pieces are laid out for eight epilogue warps of
     // 128 int32 columns each
     static_assert(!kStreamK || (kEpiWarps == 8 && kColsPerThread == 128), "stream-K layout");
+    static_assert(!kLoraFused || (kI8 && !kSwiGLU && NSTAGE <= 4),
+                  "the fused LoRA expand rides the INT8 fp16 operand ring of the scale/bias kernel");
 };
 
 struct Barriers {
@@ -157,6 +166,7 @@ struct Barriers {
     uint64_t drain;
     uint64_t never;      // nothing arrives here: the forced-timeout test waits on it
     uint64_t ybar[4];    // y += acc: the y tile in buffer b has landed
+    uint64_t ltma[4];    // fused LoRA: the t and B tiles in fp16 operand slot s have landed
     uint64_t epi_done;   // y += acc: every epilogue warp has written the tile's y
     uint32_t tmem_slot;
     int abort;
@@ -179,6 +189,42 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, 
             return false;
         }
     }
+}
+
+// Arrive with an expected transaction count and return the phase token,
+// which a later wait names unambiguously (unlike a parity).
+__device__ __forceinline__ uint64_t mbar_arrive_expect_tx_token(uint64_t *bar, uint32_t bytes) {
+    uint64_t st;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 %0, [%1], %2;"
+                 : "=l"(st) : "r"(smem_u32(bar)), "r"(bytes) : "memory");
+    return st;
+}
+
+// Time-limited wait for the phase a token was taken in; like
+// mbar_wait_drain it ignores the abort flag (used for copies that must land
+// before their shared memory may be reused or released).
+__device__ __forceinline__ bool mbar_wait_token(uint64_t *bar, uint64_t token, uint64_t limit_ns,
+                                                unsigned int *status, unsigned int site) {
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(ok) : "r"(a), "l"(token) : "memory");
+        if (ok) return true;
+        if ((it & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) {
+            record_status(status, kStatusTimeout | (site << 8));
+            return false;
+        }
+    }
+}
+
+// Arrive `count` times at once.
+__device__ __forceinline__ void mbar_arrive_n(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
@@ -384,7 +430,7 @@ struct Gemm {
         uint8_t *raw;        // NRAW x (raw A, raw B) for INT8
         uint8_t *epi;        // kEpiStage bytes of epilogue buffers
         const CUtensorMap *tmC;  // y += acc: the y tensor map; LoRA gate/up: the base g|u map
-        const CUtensorMap *tmD;  // LoRA gate/up: the h tensor map
+        const CUtensorMap *tmD;  // LoRA gate/up: the h tensor map; fused LoRA: the B factor
         Barriers *bar;
         uint32_t tmem;       // accumulator base (the leader's allocation in pair mode)
         uint32_t rank;       // rank in the CTA pair (0 in single mode)
@@ -392,6 +438,7 @@ struct Gemm {
         int num_m, num_n, num_tiles, nkb;
         int n_fastest;       // tile order: 0 = M fastest, 1 = N fastest
         int force_timeout;   // test knob: this CTA's MMA issuer waits on a barrier nothing signals
+        int nl;              // fused LoRA: bf16 k-blocks per tile (0 = none)
         WaitCtx w;
     };
 
@@ -487,6 +534,23 @@ struct Gemm {
         return nb * BN + (int)c.rank * C::kBRows;
     }
 
+    // Fused LoRA: the LoRA k-blocks that follow a segment's k-blocks (a whole
+    // tile's; the fused kernels never split tiles).
+    static __device__ __forceinline__ int lora_kblocks(const Ctx &c, const Seg &sg) {
+        return (C::kLoraFused && sg.part < 0) ? c.nl : 0;
+    }
+
+    // Fused LoRA: first column of t read by the tiles of column block nb (the
+    // segment of the adapter whose output columns the tile covers).
+    static __device__ __forceinline__ int lora_tcol(const GemmArgs &a, int nb) {
+        const int n0 = nb * C::kOutColsPerTile;
+        int tcol = a.lora_seg_tcol[0];
+#pragma unroll
+        for (int k = 1; k < kLoraMaxSegs; ++k)
+            if (k < a.lora_nseg && n0 >= a.lora_seg_end[k - 1]) tcol = a.lora_seg_tcol[k];
+        return tcol;
+    }
+
     // ---------------------------------------------------------------- producer
     static __device__ void producer(const Ctx &c, const CUtensorMap *tmA, const CUtensorMap *tmB0,
                                     const CUtensorMap *tmB2, const GemmArgs &a, uint32_t (&fills)[8]) {
@@ -513,8 +577,16 @@ struct Gemm {
             int mb, nb;
             tile_coords(c, sg.tile, mb, nb);
             const int row_a = mb * C::kTileRows + (int)c.rank * C::BM;
-            for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                if (C::kI8) {
+            const int kb_end = sg.kb1 + lora_kblocks(c, sg);
+            for (int kb = sg.kb0; kb < kb_end; ++kb) {
+                if (C::kLoraFused && kb >= sg.kb1) {
+                    // a LoRA k-block: its t and B tiles go straight into the fp16
+                    // operand slot, copied by the converter group that owns the
+                    // k-block (it alone knows when the slot is free); the raw slot
+                    // is passed on empty, to keep the two rings in step
+                    if (!mbar_wait(&c.bar->raw_empty[s], ph ^ 1u, c.w, kSiteTmaEmpty)) return;
+                    mbar_arrive(&c.bar->raw_full[s]);
+                } else if (C::kI8) {
                     if (!mbar_wait(&c.bar->raw_empty[s], ph ^ 1u, c.w, kSiteTmaEmpty)) return;
                     uint64_t *full = &c.bar->raw_full[s];
                     uint8_t *ra = c.raw + s * C::kRawStage;
@@ -575,13 +647,42 @@ struct Gemm {
         }
     }
 
+    // Fused LoRA, one converter lane, once fp16 operand slot cs is free: copy
+    // the LoRA k-block kin of this CTA's tile number ktile into it (the tile's
+    // t rows and B-factor rows, bf16, 64 of K, already in the MMA's swizzled
+    // layout) by TMA, wait for the bytes to land, then arrive for the whole
+    // converter group on the slot's "full" barrier and release raw slot rs.
+    // Returns false if the copy did not land in time.
+    static __device__ bool lora_copy(const Ctx &c, const GemmArgs &a, uint32_t cs, uint32_t rs, int ktile,
+                                     int kin) {
+        int mb, nb;
+        tile_coords(c, c.slot + ktile * c.nslots, mb, nb);
+        const int row_a = mb * C::kTileRows + (int)c.rank * C::BM;
+        uint8_t *sa = c.stage + cs * C::kStage;
+        uint8_t *sb = sa + C::kAStage;
+        const int k0 = 64 * (kin - c.nkb);
+        uint64_t *lb = &c.bar->ltma[cs];
+        const uint64_t tok = mbar_arrive_expect_tx_token(lb, C::kStage);
+        tma_load_2d(sa, c.tmC, lora_tcol(a, nb) + k0, row_a, lb);
+        tma_load_2d(sb, c.tmD, k0, b_row(c, a, nb, (int)c.rank), lb);
+        // the copy must land before anyone may read or release the slot,
+        // also when another role has given up (hence no abort check)
+        if (!mbar_wait_token(lb, tok, 200000000ull, c.w.status, kSiteConvEmpty)) {
+            *c.w.abort = 1;
+            return false;
+        }
+        mbar_arrive_n(&c.bar->full[cs], C::kGroupWarps);
+        mbar_arrive_n(&c.bar->raw_empty[rs], C::kGroupWarps);
+        return true;
+    }
+
     // ---------------------------------------------------------------- converters
     // Each converter thread owns the same 16-byte raw pieces in every k-block:
     // piece = ctid & 3 of rows (ctid >> 2) + S j (A rows 0..127, then B rows),
     // where S = threads / 4 is a multiple of 8, so the 128-byte swizzle phase
     // (row & 7) of a thread's rows is constant and all shared addresses are a
     // per-thread base plus compile-time offsets.
-    static __device__ void converter(const Ctx &c, int ctid_all) {
+    static __device__ void converter(const Ctx &c, const GemmArgs &a, int ctid_all) {
         constexpr int kThr = (C::kI8 ? C::kGroupWarps : 2) * 32;  // native ops never call this
         constexpr int kG = C::kI8 ? C::kConvGroups : 1;
         constexpr int kRows = C::BM + C::kBRows;
@@ -598,11 +699,38 @@ struct Gemm {
         // this CTA's k-blocks in order, over all its segments: its whole tiles,
         // then (stream-K) its run of the remaining tiles' k-blocks
         const int whole_end = sk_of(c) ? sk_tail0(c) : c.num_tiles;
-        int total = (c.slot < whole_end ? (whole_end - 1 - c.slot) / c.nslots + 1 : 0) * c.nkb;
+        // k-blocks per whole tile (fused LoRA: the tile's INT8 k-blocks, then its
+        // bf16 LoRA k-blocks, which the producer has already placed by TMA)
+        const int per = c.nkb + (C::kLoraFused ? c.nl : 0);
+        int total = (c.slot < whole_end ? (whole_end - 1 - c.slot) / c.nslots + 1 : 0) * per;
         if (sk_of(c) && c.slot < sk_of(c)) total += sk_bound(c, c.slot + 1) - sk_bound(c, c.slot);
         uint32_t rs = (uint32_t)group, rph = 0, cs = (uint32_t)group, cph = 0;
+        int kin = group;   // fused LoRA: the k-block's index within its tile
+        int ktile = 0;     // and its tile's index in this CTA's tile sequence
+        while (C::kLoraFused && kin >= per) { kin -= per; ++ktile; }
         for (int kidx = group; kidx < total; kidx += kG) {
             if (!mbar_wait(&c.bar->raw_full[rs], rph, c.w, kSiteConvRaw)) return;
+            if (C::kLoraFused && kin >= c.nkb) {
+                // a LoRA k-block: every warp of the group waits for the slot to be
+                // free, as for an INT8 k-block (each warp's successive waits on the
+                // ring's "empty" barriers must stay at most NSTAGE k-blocks apart,
+                // or a parity wait could pass a phase two behind); then one lane
+                // copies the tile's t rows and B-factor rows (bf16, 64 of K,
+                // already in the MMA's swizzled layout) into it by TMA, waits for
+                // them to land, and arrives for the whole group
+                if (!wait_pair(&c.bar->empty[cs], cph ^ 1u, c, kSiteConvEmpty)) return;
+                bool ok = true;
+                if (ctid == 0) ok = lora_copy(c, a, cs, rs, ktile, kin);
+                __syncwarp();
+                if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) return;
+                rs += kG;
+                if (rs >= (uint32_t)C::NRAW) { rs -= C::NRAW; rph ^= 1u; }
+                cs += kG;
+                if (cs >= (uint32_t)C::NSTAGE) { cs -= C::NSTAGE; cph ^= 1u; }
+                kin += kG;
+                while (kin >= per) { kin -= per; ++ktile; }
+                continue;
+            }
             if (!wait_pair(&c.bar->empty[cs], cph ^ 1u, c, kSiteConvEmpty)) return;
             const uint32_t src = raw_base + rs * C::kRawStage + src0;
             const uint32_t dst = stage_base + cs * C::kStage;
@@ -637,6 +765,10 @@ struct Gemm {
             if (rs >= (uint32_t)C::NRAW) { rs -= C::NRAW; rph ^= 1u; }
             cs += kG;
             if (cs >= (uint32_t)C::NSTAGE) { cs -= C::NSTAGE; cph ^= 1u; }
+            if (C::kLoraFused) {
+                kin += kG;
+                while (kin >= per) { kin -= per; ++ktile; }
+            }
         }
     }
 
@@ -652,7 +784,8 @@ struct Gemm {
         const Segs sp = seg_plan(c);
         for (int si = 0; si < sp.total; ++si) {
             const Seg sg = seg_at(c, sp, si);
-            for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+            const int kb_end = sg.kb1 + lora_kblocks(c, sg);
+            for (int kb = sg.kb0; kb < kb_end; ++kb) {
                 if (!mbar_wait(&c.bar->full[s], ph, c.w, kSiteMmaFull)) return;
                 arrive_cluster_relaxed(leader_addr(&c.bar->full[s]));
                 if (++s == (uint32_t)C::NSTAGE) { s = 0; ph ^= 1u; }
@@ -703,6 +836,35 @@ struct Gemm {
                 else mma_commit(&c.bar->acc_full[acc]);
                 if (++acc == (uint32_t)C::kAccBufs) { acc = 0; aph ^= 1u; }
             }
+            const int nl = lora_kblocks(c, sg);
+            if (C::kLoraFused && nl > 0) {
+                // the tile's LoRA chunk: t B^T with bf16 operands into a fresh
+                // accumulator, which the epilogue adds to the rounded base values
+                constexpr uint32_t idesc_l = idesc_f32acc(1u, 1u, C::kTileRows, BN);
+                if (!wait_pair(&c.bar->acc_empty[acc], aph ^ 1u, c, kSiteMmaAccEmpty)) return;
+                tc_fence_after();
+                const uint32_t d = c.tmem + acc * BN;
+                for (int j = 0; j < nl; ++j) {
+                    if (!wait_pair(&c.bar->full[s], ph, c, kSiteMmaFull)) return;
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(c.stage + s * C::kStage);
+                    const uint32_t sb = sa + C::kAStage;
+#pragma unroll
+                    for (int k = 0; k < C::kMmaPerKBlock; ++k) {
+                        const uint64_t ad = sdesc_sw128(sa + 32 * k);
+                        const uint64_t bd = sdesc_sw128(sb + 32 * k);
+                        const uint32_t accum = (j > 0 || k > 0) ? 1u : 0u;
+                        if (PAIR) mma2_f16(d, ad, bd, idesc_l, accum);
+                        else mma_f16(d, ad, bd, idesc_l, accum);
+                    }
+                    if (PAIR) mma2_commit_both(&c.bar->empty[s]);
+                    else mma_commit(&c.bar->empty[s]);
+                    if (++s == (uint32_t)C::NSTAGE) { s = 0; ph ^= 1u; }
+                }
+                if (PAIR) mma2_commit_both(&c.bar->acc_full[acc]);
+                else mma_commit(&c.bar->acc_full[acc]);
+                if (++acc == (uint32_t)C::kAccBufs) { acc = 0; aph ^= 1u; }
+            }
         }
     }
 
@@ -731,13 +893,13 @@ struct Gemm {
                                                     int n0, const float (&v)[32],
                                                     const float (&u)[32]) {
         if (!row_ok) return;
-        const float sa = (EPI == kEpiScaleBias || EPI == kEpiSwiGLU) ? __ldg(a.sa + row) : 0.0f;
+        const float sa = C::kScaled ? __ldg(a.sa + row) : 0.0f;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             const int n = n0 + 8 * g;
             if (n >= a.N) break;  // N % 8 == 0: whole groups in or out
             float y[8];
-            if (EPI == kEpiScaleBias || EPI == kEpiSwiGLU) {
+            if (C::kScaled) {
                 const float4 s0 = __ldg(reinterpret_cast<const float4 *>(a.sb + n));
                 const float4 s1 = __ldg(reinterpret_cast<const float4 *>(a.sb + n) + 1);
                 const float sb[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
@@ -768,6 +930,49 @@ struct Gemm {
             uint4 pk = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
                                   pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
             *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + (int64_t)row * a.ldo + n) = pk;
+        }
+    }
+
+    // Fused LoRA, scale/bias: 16 columns n0.. of one row from the exact int32
+    // totals and the fp32 LoRA sums: y = bf16(bf16(base) + lora) with base the
+    // scale/bias value, the same rounded operations as the INT8 linear
+    // followed by the LoRA add's expand.
+    static __device__ __forceinline__ void finish16_lora(const GemmArgs &a, int row, int n0, const int32_t *tot,
+                                                         const uint32_t (&lv)[16]) {
+        const float sa = __ldg(a.sa + row);
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            const int n = n0 + 8 * g;
+            if (n >= a.N) break;   // N % 8 == 0: whole groups in or out
+            const float4 s0 = __ldg(reinterpret_cast<const float4 *>(a.sb + n));
+            const float4 s1 = __ldg(reinterpret_cast<const float4 *>(a.sb + n) + 1);
+            const float sb[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+            float y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float base = bf16_round(scale_bias(__int2float_rn(tot[8 * g + i]), sa, sb[i], a.bias, n + i));
+                y[i] = __fadd_rn(base, __uint_as_float(lv[8 * g + i]));
+            }
+            uint4 pk = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                  pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+            *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + (int64_t)row * a.ldo + n) = pk;
+        }
+    }
+
+    // Fused LoRA: finish this thread's row from its int32 totals and the LoRA
+    // accumulator at tbase, 16 columns at a time (the accumulator is released
+    // once its last columns are in registers).
+    static __device__ __forceinline__ void finish_row_lora(const Ctx &c, const GemmArgs &a, int row, bool row_ok,
+                                                           int nb, int half, const int32_t *tot, uint32_t tbase,
+                                                           uint32_t acc, int lane) {
+#pragma unroll
+        for (int q = 0; q < 2 * C::kChunks32; ++q) {
+            const int j = q >> 1, o = 16 * (q & 1);
+            uint32_t lv[16];
+            tmem_ld16(tbase + chunk_col(j, half) + o, lv);
+            tmem_ld_wait();
+            if (q == 2 * C::kChunks32 - 1) release_acc(c, acc, lane);
+            if (row_ok) finish16_lora(a, row, nb * BN + chunk_col(j, half) + o, tot + 32 * j + o, lv);
         }
     }
 
@@ -1069,8 +1274,18 @@ struct Gemm {
                 }
                 // the tile's exact int32 accumulators are complete (stream-K:
                 // once the last piece to arrive has added the others)
-                if (sg.part < 0 || sk_combine(c, a, sg, e, lane, tot))
+                if constexpr (C::kLoraFused) {
+                    if (lora_kblocks(c, sg) > 0) {
+                        if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
+                        tc_fence_after();
+                        finish_row_lora(c, a, row, row_ok, nb, half, tot, c.tmem + acc * BN + lane_off, acc, lane);
+                        if (++acc == (uint32_t)C::kAccBufs) { acc = 0; aph ^= 1u; }
+                    } else {
+                        finish_row(a, row, row_ok, nb, half, tot);
+                    }
+                } else if (sg.part < 0 || sk_combine(c, a, sg, e, lane, tot)) {
                     finish_row(a, row, row_ok, nb, half, tot);
+                }
             } else if constexpr (C::kLoraSwi) {
                 // base g|u tiles by TMA through the ring (kYBufs - 1 tiles ahead),
                 // h computed in place over the gate columns, stored by TMA after a
@@ -1204,6 +1419,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
         mbar_init(&bar->drain, 1);
         for (int i = 0; i < C::kYBufs; ++i) mbar_init(&bar->ybar[i], 1);
+        if (C::kLoraFused)
+            for (int i = 0; i < C::NSTAGE; ++i) mbar_init(&bar->ltma[i], 1);
         mbar_init(&bar->epi_done, C::kEpiWarps);
         mbar_init(&bar->never, 1);
         bar->abort = 0;
@@ -1215,8 +1432,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         if (C::kLoraSwi) tma_prefetch_desc(&tmB2);
-        if (EPI == kEpiAddBF16 || C::kLoraSwi) tma_prefetch_desc(&tmC);
-        if (C::kLoraSwi) tma_prefetch_desc(&tmD);
+        if (EPI == kEpiAddBF16 || C::kLoraSwi || C::kLoraFused) tma_prefetch_desc(&tmC);
+        if (C::kLoraSwi || C::kLoraFused) tma_prefetch_desc(&tmD);
     }
     if (warp == 1) {
         if (PAIR) {
@@ -1264,6 +1481,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     c.n_fastest = args.n_fastest;
 
     c.force_timeout = args.force_timeout == 1 || (args.force_timeout >= 2 && args.force_timeout - 2 == c.slot);
+    c.nl = C::kLoraFused ? args.lora_nkb : 0;
     c.w.limit_ns = args.wait_limit_ns;
     c.w.abort = &bar->abort;
     c.w.status = args.status;
@@ -1290,7 +1508,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 G::forwarder(c);
             }
         } else if (C::kI8 && warp < 2 + C::kConvWarps) {
-            G::converter(c, threadIdx.x - 64);
+            G::converter(c, args, threadIdx.x - 64);
         }
     } else {
         if (C::kI8) asm volatile("setmaxnreg.inc.sync.aligned.u32 192;");
@@ -1346,6 +1564,16 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
         if (rc) return rc;
         rc = internal_make_tmap(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, args.out, (uint64_t)args.N,
                                 (uint64_t)args.M, (uint64_t)args.ldo * 2, 64, C::BM,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc) return rc;
+    }
+    if (C::kLoraFused) {   // t rows (A of the LoRA chunk) and the B factor(s), bf16, 64 of K per box
+        rc = internal_make_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, args.lora_t, (uint64_t)args.lora_ldt,
+                                (uint64_t)args.M, (uint64_t)args.lora_ldt * 2, 64, C::BM,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc) return rc;
+        rc = internal_make_tmap(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, args.lora_b, (uint64_t)args.lora_r,
+                                (uint64_t)args.N, (uint64_t)args.lora_r * 2, 64, C::kBRows,
                                 CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc) return rc;
     }
@@ -1459,6 +1687,7 @@ int launch_gemm(int op, int epi, int bn, const Operand &A, const Operand &B, con
         if (epi == kEpiScaleBias) CLEF_GEMM(kOpI8, kEpiScaleBias, 256);
         if (epi == kEpiSwiGLU) CLEF_GEMM(kOpI8, kEpiSwiGLU, 256);
         if (epi == kEpiStoreS32) CLEF_GEMM(kOpI8, kEpiStoreS32, 256);
+        if (epi == kEpiScaleBiasLora) CLEF_GEMM(kOpI8, kEpiScaleBiasLora, 256);
     } else if (op == kOpF8 && bn == 256) {
         if (epi == kEpiScaleBias) CLEF_GEMM(kOpF8, kEpiScaleBias, 256);
         if (epi == kEpiSwiGLU) CLEF_GEMM(kOpF8, kEpiSwiGLU, 256);

@@ -37,7 +37,7 @@ import torch
 
 from . import (bind_workspace, fp8_gateup_swiglu, fp8_linear, gemm_workspace_bytes, lora_add,
                lora_expand_add, lora_gateup_swiglu, lora_pad, lora_shrink, poll_status, quant_act,
-               w8a8_gateup_swiglu, w8a8_linear)
+               w8a8_gateup_swiglu, w8a8_linear, w8a8_linear_lora)
 
 TIMEOUT = 4   # CLEF_ERR_TIMEOUT
 
@@ -45,11 +45,15 @@ TIMEOUT = 4   # CLEF_ERR_TIMEOUT
 class QuantizedLayer:
     def __init__(self, cfg, weights: Dict[str, Tuple[torch.Tensor, Optional[torch.Tensor]]],
                  lora: Optional[Dict[str, Tuple[torch.Tensor, torch.Tensor]]] = None,
-                 device="cuda", pack_shared_input: bool = True):
+                 device="cuda", pack_shared_input: bool = True, fuse_lora: bool = True):
         """weights: projection name -> (W bf16 [rows][K], bias bf16 [rows] or None);
         lora: name (or name + "/gate", name + "/up" for gate/up) -> (A, B);
         pack_shared_input: run consecutive plain projections of one activation
-        as one packed GEMM."""
+        as one packed GEMM;
+        fuse_lora (INT8): add the LoRA of each adapted linear launch unit
+        inside its GEMM (one x A^T launch, then the GEMM with the expand fused)
+        instead of expand launches over the GEMM's output; the bytes are the
+        same.  Gate/up keeps its separate adapter + SwiGLU launch."""
         self.cfg = cfg
         self.M = cfg.M
         self.fp8 = cfg.scheme == "fp8"
@@ -82,6 +86,15 @@ class QuantizedLayer:
         self.ws = None if self.fp8 else torch.zeros(gemm_workspace_bytes(), dtype=torch.uint8,
                                                      device=device)
         self._ws_stream = None   # the stream the workspace was last bound to
+        # fused LoRA (INT8): per adapted launch unit, its stacked A factors, its
+        # t, its stacked B factor(s) and the column segments of its adapters
+        self.fused = {}
+        if fuse_lora and not self.fp8 and self.lora:
+            for gi, g in enumerate(self.groups):
+                f = _fused_unit(g, self.lora, M, device)
+                if f is not None:
+                    self.fused[gi] = f
+        fused_names = {p.name for gi in self.fused for p in self.groups[gi]}
         code = torch.uint8 if self.fp8 else torch.int8
         self.q = {}
         for name, K in cfg.activations():
@@ -104,7 +117,7 @@ class QuantizedLayer:
                 continue
             if p.kind == "gateup":
                 self.out[p.name] = torch.empty((M, p.N), dtype=torch.bfloat16, device=device)
-                if self.lora:
+                if self.lora and p.name not in fused_names:
                     self.out[p.name + "/packed"] = torch.empty((M, 2 * p.N), dtype=torch.bfloat16,
                                                                device=device)
             else:
@@ -119,7 +132,7 @@ class QuantizedLayer:
         self.t = {}
         self.lora_groups = {}   # group index -> (stacked A, t, [(name, col0, r_pad)])
         for gi, g in enumerate(self.groups):
-            members = [p for p in g if p.name in self.lora] if len(g) > 1 else []
+            members = [p for p in g if p.name in self.lora] if len(g) > 1 and gi not in self.fused else []
             if not members:
                 continue
             K = g[0].K
@@ -135,18 +148,25 @@ class QuantizedLayer:
             self.lora_groups[gi] = (A_cat, t, blocks)
         grouped = {name for _, _, blocks in self.lora_groups.values() for name, _, _ in blocks}
         for key, (A, _) in self.lora.items():
-            if key in grouped:
+            if key in grouped or key.split("/")[0] in fused_names:
                 continue
             width = lora_pad(A.shape[0]) * (2 if key.endswith("/gate") or key.endswith("/up") else 1)
             if width not in self.t:
                 self.t[width] = torch.empty((M, width), dtype=torch.bfloat16, device=device)
 
     def units(self):
-        """The GEMM launches of a step: (event name, weight rows, K, 2*M*rows*K)."""
+        """The GEMM launches of a step: (event name, weight rows, K, 2*M*rows*K,
+        the flops of the LoRA expand fused into the launch: 2*M*N*r per adapter)."""
         out = []
-        for g in self.groups:
+        for gi, g in enumerate(self.groups):
             rows = sum(p.weight_rows for p in g)
-            out.append((_unit_name(g), rows, g[0].K, 2 * self.M * rows * g[0].K))
+            fused = 0
+            if gi in self.fused:
+                for p in g:
+                    if p.name in self.lora:
+                        N, r = self.lora[p.name][1].shape
+                        fused += 2 * self.M * N * r
+            out.append((_unit_name(g), rows, g[0].K, 2 * self.M * rows * g[0].K, fused))
         return out
 
     def lora_work(self) -> Tuple[int, int]:
@@ -155,6 +175,15 @@ class QuantizedLayer:
         back, y read and written (gate/up: both base halves read, h written)."""
         M, fl, by = self.M, 0, 0
         for gi, g in enumerate(self.groups):
+            if gi in self.fused:
+                # fused: the LoRA launch is x A^T alone (x read, t written); the
+                # expand's flops belong to the GEMM (units())
+                f = self.fused[gi]
+                by += M * g[0].K * 2 + M * f.t.shape[1] * 2
+                for p in g:
+                    if p.name in self.lora:
+                        fl += 2 * M * self.lora[p.name][0].shape[0] * p.K
+                continue
             if gi in self.lora_groups:
                 _, t, blocks = self.lora_groups[gi]
                 by += M * g[0].K * 2 + 2 * M * t.shape[1] * 2
@@ -182,7 +211,9 @@ class QuantizedLayer:
             n += 1 if p.chained else 0
         if self.lora:
             for gi, g in enumerate(self.groups):
-                if gi in self.lora_groups:      # one shared x A^T, one expand per adapter
+                if gi in self.fused:            # x A^T, then the GEMM with the expand fused
+                    n += 1
+                elif gi in self.lora_groups:    # one shared x A^T, one expand per adapter
                     n += 1 + len(self.lora_groups[gi][2])
                 elif g[0].kind == "gateup":     # stacked x A^T, one fused add + SwiGLU
                     n += 2
@@ -220,6 +251,9 @@ class QuantizedLayer:
         for gi, g in enumerate(self.groups):
             if gi == last and final_wait is not None:
                 torch.cuda.current_stream().wait_event(final_wait)
+            if gi in self.fused:
+                prev_h = self._step_fused(gi, g, acts, prev_h, ev)
+                continue
             if len(g) > 1:
                 qw, sw, b = self.unit_w[gi]
                 qx, sx = self.q[g[0].act]
@@ -265,6 +299,28 @@ class QuantizedLayer:
                         lora_add(acts[p.act] if not p.chained else prev_h, A, B, y,
                                  t_scratch=self._t(A))
         return self.out
+
+    def _step_fused(self, gi, g, acts, prev_h, ev):
+        """One linear launch unit with its LoRA fused: x A^T for all of the
+        unit's adapters in one launch, then the INT8 GEMM whose tiles add
+        t B^T to their rounded base values."""
+        f = self.fused[gi]
+        qw, sw, b = self.unit_w[gi]
+        p = g[0]
+        name = _unit_name(g)
+        x = prev_h if p.chained else acts[p.act]
+        if p.chained:
+            qx, sx = self.q[p.act]
+            with ev("quant", p.act):
+                quant_act(prev_h, self.mode, q=qx, scale=sx)
+        else:
+            qx, sx = self.q[p.act]
+        with ev("lora", name + ":xA"):
+            lora_shrink(x, f.A, t=f.t)
+        y = self.unit_out[gi] if len(g) > 1 else self.out[p.name]
+        with ev("gemm", name):
+            w8a8_linear_lora(qx, sx, qw, sw, b, f.t, f.B, y=y, segments=f.segments)
+        return prev_h
 
     def poll_status(self) -> int:
         """Synchronise, then return (and clear) the library's device status
@@ -313,6 +369,47 @@ class QuantizedLayer:
 
     def _t(self, A):
         return self.t[lora_pad(A.shape[0])]
+
+
+def _fused_unit(g, lora, M, device):
+    """The fused-LoRA buffers of one linear launch unit, or None when it has
+    no adapter or its adapters cannot share one fused launch (a gate/up unit,
+    different ranks, more than four adapters, or column segments off the
+    256-column tiles).
+
+    A = the adapters' A factors stacked, each padded with zero rows to r_pad;
+    t = [M][sum r_pad]; B = [N_unit][r] with each adapter's B rows at its
+    projection's output columns (zero rows for a projection without an
+    adapter, which then adds exact zeros); segments map each projection's
+    columns to its t block."""
+    if g[0].kind == "gateup":
+        return None
+    members = [p for p in g if p.name in lora]
+    if not members:
+        return None
+    ranks = {lora[p.name][0].shape[0] for p in members}
+    if len(ranks) != 1 or len(g) > 4:
+        return None
+    r = ranks.pop()
+    rp = lora_pad(r)
+    K = g[0].K
+    A = torch.zeros((rp * len(members), K), dtype=torch.bfloat16, device=device)
+    B = torch.zeros((sum(p.N for p in g), r), dtype=torch.bfloat16, device=device)
+    segments, c0, tb = [], 0, 0
+    for p in g:
+        if p.name in lora:
+            Ap, Bp = lora[p.name]
+            A[tb:tb + r] = Ap
+            B[c0:c0 + p.N] = Bp
+            tcol, tb = tb, tb + rp
+        else:
+            tcol = 0     # its B rows are zeros
+        c0 += p.N
+        if c0 % 256 != 0 and p is not g[-1]:
+            return None
+        segments.append((c0, tcol))
+    t = torch.empty((M, tb), dtype=torch.bfloat16, device=device)
+    return SimpleNamespace(A=A, t=t, B=B, segments=segments)
 
 
 def _unit_name(group) -> str:
