@@ -202,6 +202,26 @@ int clef_w8a8_linear_lora(const int8_t *qx, const float *sx, const int8_t *qw, c
                           const int64_t *seg_tcol, void *y, int64_t ldy, void *stream);
 
 /*
+ * clef_w8a8_gateup_swiglu_lora -- the INT8 gate/up SwiGLU call with the gate
+ * and up LoRA adds fused [LORA; USAGE: fuse_mlp]: with t_gu = [x A_gate^T |
+ * x A_up^T] from one clef_lora_shrink over the stacked A factors (each padded
+ * with zero rows to r_pad),
+ *   g = bf16(bf16(gate epilogue value) + sum_j t_gu[m][j] * B_gate[n][j])
+ *   u = bf16(bf16(up epilogue value) + sum_j t_gu[m][r_pad + j] * B_up[n][j])
+ *   h[m][n] = bf16(silu(g) * u)    (silu as in clef_swiglu_bf16)
+ * -- the same bytes as clef_w8a8_linear on the packed weight (bf16 [M][2N])
+ * followed by clef_lora_gateup_swiglu, without g and u ever reaching memory.
+ * t_gu: bf16 [M][>= 2 r_pad] at pitch ldt (t_gate in columns 0 .. r_pad - 1,
+ * t_up in r_pad .. 2 r_pad - 1; columns past r in each must be finite);
+ * B_gate, B_up: bf16 [N][r] dense.  Other arguments and requirements as
+ * clef_w8a8_gateup_swiglu; 0 < r <= 1024, r % 8 == 0, ldt % 8 == 0.
+ */
+int clef_w8a8_gateup_swiglu_lora(const int8_t *qx, const float *sx, const int8_t *qw_gu, const float *sw_gu,
+                                 const void *bias_gu, int64_t M, int64_t N, int64_t K, const void *t_gu,
+                                 int64_t ldt, const void *B_gate, const void *B_up, int64_t r, void *h,
+                                 int64_t ldh, void *stream);
+
+/*
  * clef_lora_shrink / clef_lora_expand_add -- the two stages of clef_lora_add
  * as separate calls [LORA], for adapters that share an input: with their A
  * factors stacked (each zero-padded to a multiple of 64 rows) one shrink

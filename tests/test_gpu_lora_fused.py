@@ -1,13 +1,14 @@
-"""The runtime LoRA expand fused into the INT8 linear GEMM (the pull
-request's y = bf16(y + bf16(x A^T) B^T) with y the rounded base projection).
+"""The runtime LoRA expand fused into the INT8 GEMMs (the pull request's
+y = bf16(y + bf16(x A^T) B^T) with y the rounded base projection).
 
-The fused call must give the bytes of the unfused chain it replaces --
-clef_w8a8_linear then clef_lora_expand_add -- on CTA-pair tiles (M > 128)
-and single tiles, ragged M and N, ranks that need padding, several tiles per
-CTA pair, packed projections with several adapters (column segments), and
-rows checked against the oracle through the same chain.  A layer with the
-fused path equals one without it, and the fused call keeps a row's bits
-independent of the call's row count."""
+The fused calls must give the bytes of the unfused chains they replace --
+clef_w8a8_linear then clef_lora_expand_add, or the packed clef_w8a8_linear
+then clef_lora_gateup_swiglu -- on CTA-pair tiles (M > 128) and single
+tiles, ragged M and N, ranks that need padding, several tiles per CTA pair,
+packed projections with several adapters (column segments), and rows checked
+against the oracle through the same chain.  A layer with the fused path
+equals one without it, and the fused calls keep a row's bits independent of
+the call's row count."""
 import numpy as np
 import pytest
 import torch
@@ -76,6 +77,22 @@ def test_linear_lora_segments(M):
     _eq(got, ref, "segments")
 
 
+@pytest.mark.parametrize("M,N,K,r", [(300, 512, 1024, 256), (130, 264, 2048, 48), (1, 8, 128, 8),
+                                     (600, 1280, 5120, 256), (2048, 4096, 1024, 256)])
+def test_gateup_swiglu_lora_equals_unfused(M, N, K, r):
+    x, qx, sx, qw, sw, b = _codes(f"gu{M}", M, 2 * N, K)
+    Ag, Bg = (bf16_dev(v) for v in S.lora_pair(0, f"t/fl/gu{M}/g", r, K, N))
+    Au, Bu = (bf16_dev(v) for v in S.lora_pair(0, f"t/fl/gu{M}/u", r, K, N))
+    rp = clef.lora_pad(r)
+    A = torch.zeros((2 * rp, K), dtype=torch.bfloat16, device="cuda")
+    A[:r], A[rp:rp + r] = Ag, Au
+    t = clef.lora_shrink(x, A)
+    ygu = clef.w8a8_linear(qx, sx, qw, sw, b)
+    ref = clef.lora_gateup_swiglu(x, Ag, Bg, Au, Bu, ygu)
+    got = clef.w8a8_gateup_swiglu_lora(qx, sx, qw, sw, b, t, Bg, Bu)
+    _eq(got, ref, "fused gate/up")
+
+
 def test_fused_rows_match_oracle(orc):
     """Sampled rows of a fused linear against the oracle's chain (INT8 linear,
     LoRA t, LoRA y), within the derived LoRA bound."""
@@ -111,13 +128,20 @@ def test_fused_row_invariance():
     for a, c in pieces(M):
         clef.w8a8_linear_lora(qx[a:c], sx[a:c], qw, sw, b, t[a:c], B, y=part[a:c], segments=segs)
     _eq(whole, part, "linear")
+    Ag, Bg = (bf16_dev(v) for v in S.lora_pair(0, "t/fl/inv/g", r, K, N // 2))
+    Au, Bu = (bf16_dev(v) for v in S.lora_pair(0, "t/fl/inv/u", r, K, N // 2))
+    t = clef.lora_shrink(x, torch.cat([Ag, Au]))
+    whole = clef.w8a8_gateup_swiglu_lora(qx, sx, qw, sw, b, t, Bg, Bu)
+    part = torch.empty_like(whole)
+    for a, c in pieces(M):
+        clef.w8a8_gateup_swiglu_lora(qx[a:c], sx[a:c], qw, sw, b, t[a:c], Bg, Bu, h=part[a:c])
+    _eq(whole, part, "gate/up")
 
 
 def test_layer_fused_equals_unfused():
     """A 27B-shaped layer (q|k|v packed, o, gate/up, down) at 300 tokens with
     rank-256 adapters on every projection: the fused step's outputs equal
-    the unfused step's byte for byte (gate/up keeps its separate adapter and
-    SwiGLU launch in both)."""
+    the unfused step's byte for byte."""
     from clef_synth.configs import Config, Projection
     from w8a8_quantized_projections_gb300.layer import QuantizedLayer
     cfg = Config(91, "fused-test-27b-m300", 300, "int8", [
@@ -131,7 +155,7 @@ def test_layer_fused_equals_unfused():
     acts = {k: bf16_dev(x) for k, x in acts_np.items()}
     fused = QuantizedLayer(cfg, weights, lora, fuse_lora=True)
     plain = QuantizedLayer(cfg, weights, lora, fuse_lora=False)
-    assert len(fused.fused) == 3, "q|k|v, o and down fused"
+    assert len(fused.fused) == 4, "q|k|v, o, gate/up and down fused"
     of = {k: v.clone() for k, v in fused.step(acts).items()}
     op = plain.step(acts)
     for p in cfg.projections:

@@ -23,7 +23,7 @@ __all__ = [
     "ClefError", "library", "library_path", "quant_act", "quant_act_static", "w8a8_linear", "w8a8_gateup_swiglu",
     "fp8_linear", "fp8_gateup_swiglu", "lora_add", "lora_add_noalloc", "lora_shrink", "lora_expand_add",
     "lora_gateup_swiglu", "swiglu_bf16",
-    "w8a8_gemm_s32", "w8a8_linear_lora",
+    "w8a8_gemm_s32", "w8a8_linear_lora", "w8a8_gateup_swiglu_lora",
     "poll_status", "set_wait_limit_ns", "set_quant_staging", "ACT_MODES", "gemm_workspace_bytes",
     "bind_workspace", "mma_peak",
 ]
@@ -75,6 +75,8 @@ def library():
                 "clef_w8a8_gemm_s32": [vp, vp, i64, i64, i64, vp, i64, vp],
                 "clef_w8a8_linear_lora": [vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp, i64, i32, vp, vp,
                                           vp, i64, vp],
+                "clef_w8a8_gateup_swiglu_lora": [vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp, vp, i64, vp,
+                                                 i64, vp],
                 "clef_mma_peak": [i32, i64, vp],
                 "clef_poll_status": [],
                 "clef_abi_version": [],
@@ -256,6 +258,22 @@ def w8a8_linear_lora(qx, sx, qw, sw, bias, t, B, y=None, segments=None, stream=N
     cols = (C.c_int64 * 4)(*[c for _, c in segs] + [0] * (4 - len(segs)))
     return _w8a8_lora("clef_w8a8_linear_lora", qx, sx, qw, sw, bias, y, N, stream,
                       (_ptr(t), ldt, _ptr(B), r, len(segs), ends, cols))
+
+
+def w8a8_gateup_swiglu_lora(qx, sx, qw_gu, sw_gu, bias_gu, t_gu, B_gate, B_up, h=None, stream=None):
+    """INT8 gate/up SwiGLU with the gate and up LoRA adds fused: the bytes of
+    w8a8_linear on the packed weight followed by lora_gateup_swiglu.  t_gu:
+    bf16 [M][2 r_pad] = [x A_gate^T | x A_up^T] (one lora_shrink over the
+    stacked, padded A factors); B_gate, B_up: bf16 [N][r]."""
+    N = _gateup_half(qw_gu)
+    r = B_gate.shape[1]
+    if B_gate.shape != (N, r) or B_up.shape != (N, r):
+        raise ValueError("B_gate and B_up must be [N][r]")
+    _cuda(B_up, "B_up", (torch.bfloat16,))
+    _dense(B_up, "B_up")
+    ldt = _lora_t(t_gu, B_gate, 2 * lora_pad(r), qx.shape[0])
+    return _w8a8_lora("clef_w8a8_gateup_swiglu_lora", qx, sx, qw_gu, sw_gu, bias_gu, h, N, stream,
+                      (_ptr(t_gu), ldt, _ptr(B_gate), _ptr(B_up), r))
 
 
 def _w8a8_lora(name, qx, sx, qw, sw, bias, out, n_out, stream, lora_args):

@@ -233,21 +233,25 @@ int run_w8a8(int op, int epi, const void *qx, const float *sx, const void *qw, c
     return launch_gemm(op, epi, 256, A, B, a, d->num_sms, static_cast<cudaStream_t>(stream));
 }
 
-// The INT8 linear with the LoRA expand fused (checks, then one launch): nseg
-// column segments of the output read t at their own column offsets (nseg = 0:
-// one segment at column 0).
-int run_w8a8_lora(const void *qx, const float *sx, const void *qw, const float *sw, const void *bias,
-                  int64_t M, int64_t N, int64_t K, const void *t, int64_t ldt, const void *B, int64_t r,
-                  int nseg, const int64_t *seg_end, const int64_t *seg_tcol, void *out, int64_t ldo,
-                  void *stream) {
+// The INT8 linear or gate/up SwiGLU with the LoRA expand fused (checks,
+// then one launch).  Linear: nseg column segments of the output read t at
+// their own column offsets (nseg = 0: one segment at column 0).  Gate/up: t
+// holds t_gate then t_up (2 r_pad columns) and B2 is the up factor.
+int run_w8a8_lora(bool gateup, const void *qx, const float *sx, const void *qw, const float *sw,
+                  const void *bias, int64_t M, int64_t N, int64_t K, const void *t, int64_t ldt,
+                  const void *B, const void *B2, int64_t r, int nseg, const int64_t *seg_end,
+                  const int64_t *seg_tcol, void *out, int64_t ldo, void *stream) {
     bool empty = false;
     int rc = check_gemm(qx, sx, qw, sw, bias, M, N, K, out, ldo, true, &empty);
     if (rc) return rc;
+    if (gateup && 2 * N > kMaxDim) return arg_fail("2N out of range");
     if (r <= 0 || r > 1024 || r % 8 != 0) return arg_fail("rank must be in (0, 1024] and a multiple of 8");
     const int64_t r_pad = (r + 63) / 64 * 64;
     if (ldt <= 0 || ldt % 8 != 0 || ldt > kMaxDim) return arg_fail("ldt must be a positive multiple of 8");
+    if (gateup && ldt < 2 * r_pad) return arg_fail("ldt must be >= 2 round_up(r, 64)");
     GemmArgs a;
     memset(&a, 0, sizeof a);
+    if (gateup) nseg = 0;   // one segment: t_gate | t_up from column 0
     if (nseg < 0 || nseg > kLoraMaxSegs) return arg_fail("nseg must be in 0..4");
     if (nseg > 0 && (!seg_end || !seg_tcol)) return arg_fail("null segment array");
     const int n = nseg > 0 ? nseg : 1;
@@ -266,8 +270,9 @@ int run_w8a8_lora(const void *qx, const float *sx, const void *qw, const float *
     }
     a.lora_nseg = n;
     if (empty) return CLEF_OK;
-    if (!t || !B) return arg_fail("null LoRA pointer");
-    if (!aligned16(t) || !aligned16(B)) return arg_fail("LoRA pointers must be 16-byte aligned");
+    if (!t || !B || (gateup && !B2)) return arg_fail("null LoRA pointer");
+    if (!aligned16(t) || !aligned16(B) || (gateup && !aligned16(B2)))
+        return arg_fail("LoRA pointers must be 16-byte aligned");
     DeviceState *d = nullptr;
     if ((rc = device_state(&d))) return rc;
     const GemmArgs b = base_args(d, M, N, K);
@@ -277,6 +282,7 @@ int run_w8a8_lora(const void *qx, const float *sx, const void *qw, const float *
     a.status = b.status;
     a.wait_limit_ns = b.wait_limit_ns;
     a.force_timeout = b.force_timeout;
+    a.n_half = gateup ? (int)N : 0;
     a.sa = sx;
     a.sb = sw;
     a.bias = static_cast<const uint16_t *>(bias);
@@ -285,11 +291,13 @@ int run_w8a8_lora(const void *qx, const float *sx, const void *qw, const float *
     a.lora_t = t;
     a.lora_ldt = ldt;
     a.lora_b = B;
+    a.lora_b2 = B2;
     a.lora_r = (int)r;
-    a.lora_nkb = (int)(r_pad / 64);
+    a.lora_nkb = (int)((gateup ? 2 : 1) * r_pad / 64);
     const Operand A = {qx, (uint64_t)K, (uint64_t)M, (uint64_t)K};
-    const Operand W = {qw, (uint64_t)K, (uint64_t)N, (uint64_t)K};
-    return launch_gemm(kOpI8, kEpiScaleBiasLora, 256, A, W, a, d->num_sms, static_cast<cudaStream_t>(stream));
+    const Operand W = {qw, (uint64_t)K, (gateup ? 2 : 1) * (uint64_t)N, (uint64_t)K};
+    return launch_gemm(kOpI8, gateup ? kEpiSwiGLULora : kEpiScaleBiasLora, 256, A, W, a, d->num_sms,
+                       static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -433,7 +441,16 @@ int clef_w8a8_linear_lora(const int8_t *qx, const float *sx, const int8_t *qw, c
                           const void *bias, int64_t M, int64_t N, int64_t K, const void *t, int64_t ldt,
                           const void *B, int64_t r, int nseg, const int64_t *seg_end,
                           const int64_t *seg_tcol, void *y, int64_t ldy, void *stream) {
-    return run_w8a8_lora(qx, sx, qw, sw, bias, M, N, K, t, ldt, B, r, nseg, seg_end, seg_tcol, y, ldy, stream);
+    return run_w8a8_lora(false, qx, sx, qw, sw, bias, M, N, K, t, ldt, B, nullptr, r, nseg, seg_end, seg_tcol,
+                         y, ldy, stream);
+}
+
+int clef_w8a8_gateup_swiglu_lora(const int8_t *qx, const float *sx, const int8_t *qw_gu, const float *sw_gu,
+                                 const void *bias_gu, int64_t M, int64_t N, int64_t K, const void *t_gu,
+                                 int64_t ldt, const void *B_gate, const void *B_up, int64_t r, void *h,
+                                 int64_t ldh, void *stream) {
+    return run_w8a8_lora(true, qx, sx, qw_gu, sw_gu, bias_gu, M, N, K, t_gu, ldt, B_gate, B_up, r, 0, nullptr,
+                         nullptr, h, ldh, stream);
 }
 
 int clef_w8a8_gemm_s32(const int8_t *qx, const int8_t *qw, int64_t M, int64_t N, int64_t K,

@@ -44,9 +44,11 @@ enum GemmEpi : int {
     kEpiLoraSwiGLU = 5, // gate/up LoRA adds then SwiGLU: g = bf16(yg + acc_g),
                         // u = bf16(yu + acc_u), h = bf16(silu(g) * u); yg|yu read
                         // from aux, h written to out (bf16 operands only)
-    // INT8 linear with the runtime LoRA expand fused (a last bf16 accumulator
+    // INT8 GEMMs with the runtime LoRA expand fused (a last bf16 accumulator
     // chunk per tile, lora = t B^T over the padded rank):
     kEpiScaleBiasLora = 6,  // y = bf16(bf16((acc * sa) * sb + bias) + lora)
+    kEpiSwiGLULora = 7,     // g = bf16(bf16(epilogue(gate)) + lora_g), u likewise,
+                            // h = bf16(silu(g) * u)
 };
 
 // Column segments of a fused LoRA expand: output columns below seg_end[i]
@@ -89,12 +91,15 @@ struct GemmArgs {
     int *sk_cnt;
     int4 *sk_ws;
     int64_t sk_ws_bytes;
-    // fused LoRA expand (kEpiScaleBiasLora): lora_t is t (bf16 [M][lora_ldt]),
-    // lora_b the B factor (bf16 [N][lora_r]); lora_nkb: bf16 k-blocks of 64
-    // per tile (r_pad / 64)
+    // fused LoRA expand (kEpiScaleBiasLora, kEpiSwiGLULora): lora_t is t (bf16
+    // [M][lora_ldt]), lora_b the B factor (bf16 [N][lora_r]; for SwiGLU the
+    // gate factor, the up factor being lora_b2, and t holds t_gate in columns
+    // 0 .. r_pad - 1 and t_up after); lora_nkb: bf16 k-blocks of 64 per tile
+    // (r_pad / 64, twice that for SwiGLU)
     const void *lora_t;
     int64_t lora_ldt;
     const void *lora_b;
+    const void *lora_b2;
     int lora_r;
     int lora_nkb;
     int lora_nseg;

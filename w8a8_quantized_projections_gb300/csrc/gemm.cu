@@ -116,14 +116,16 @@ struct Cfg {
     static constexpr int kTmemCols = kAccBufs * BN;
     static constexpr int kColsPerThread = BN / kParts;     // columns one epilogue thread owns
     static constexpr int kChunks32 = kColsPerThread / 32;
-    static constexpr bool kSwiGLU = (EPI == kEpiSwiGLU || EPI == kEpiLoraSwiGLU);  // gate|up tile
+    static constexpr bool kSwiGLU =   // gate|up tile
+        (EPI == kEpiSwiGLU || EPI == kEpiLoraSwiGLU || EPI == kEpiSwiGLULora);
     // INT8 with the LoRA expand fused: after a tile's INT8 k-blocks, the
     // producer loads the tile's t rows and B-factor rows (bf16) by TMA straight
     // into the fp16 operand ring, the converters pass those stages through,
     // and the MMA issuer accumulates t B^T as the tile's last chunk
-    static constexpr bool kLoraFused = (EPI == kEpiScaleBiasLora);
+    static constexpr bool kLoraFused = (EPI == kEpiScaleBiasLora || EPI == kEpiSwiGLULora);
     // epilogues that apply the row and column scales and the bias
-    static constexpr bool kScaled = (EPI == kEpiScaleBias || EPI == kEpiSwiGLU || EPI == kEpiScaleBiasLora);
+    static constexpr bool kScaled =
+        (EPI == kEpiScaleBias || EPI == kEpiSwiGLU || EPI == kEpiScaleBiasLora || EPI == kEpiSwiGLULora);
     // INT8 stream-K is compiled into the pair kernels (exact int32 pieces)
     // but not the SwiGLU one: the gate/up launches of the workloads fill at
     // least 94% of their last wave, and with the split path compiled in the
@@ -155,8 +157,7 @@ struct Cfg {
     // stream-K counters and pieces are laid out for eight epilogue warps of
     // 128 int32 columns each
     static_assert(!kStreamK || (kEpiWarps == 8 && kColsPerThread == 128), "stream-K layout");
-    static_assert(!kLoraFused || (kI8 && !kSwiGLU && NSTAGE <= 4),
-                  "the fused LoRA expand rides the INT8 fp16 operand ring of the scale/bias kernel");
+    static_assert(!kLoraFused || (kI8 && NSTAGE <= 4), "the fused LoRA expand rides the INT8 fp16 operand ring");
 };
 
 struct Barriers {
@@ -431,6 +432,7 @@ struct Gemm {
         uint8_t *epi;        // kEpiStage bytes of epilogue buffers
         const CUtensorMap *tmC;  // y += acc: the y tensor map; LoRA gate/up: the base g|u map
         const CUtensorMap *tmD;  // LoRA gate/up: the h tensor map; fused LoRA: the B factor
+        const CUtensorMap *tmB2; // fused LoRA, SwiGLU: the up factor
         Barriers *bar;
         uint32_t tmem;       // accumulator base (the leader's allocation in pair mode)
         uint32_t rank;       // rank in the CTA pair (0 in single mode)
@@ -664,7 +666,21 @@ struct Gemm {
         uint64_t *lb = &c.bar->ltma[cs];
         const uint64_t tok = mbar_arrive_expect_tx_token(lb, C::kStage);
         tma_load_2d(sa, c.tmC, lora_tcol(a, nb) + k0, row_a, lb);
-        tma_load_2d(sb, c.tmD, k0, b_row(c, a, nb, (int)c.rank), lb);
+        if (C::kSwiGLU) {
+            // gate rows see B_gate over t's first r_pad columns and zeros
+            // after (past B_gate's end); up rows zeros first (before B_up's
+            // start) and B_up after, so each half sums only its own adapter
+            const int rp = c.nl * 32;
+            if (PAIR) {
+                if (c.rank == 0) tma_load_2d(sb, c.tmD, k0, nb * (BN / 2), lb);
+                else tma_load_2d(sb, c.tmB2, k0 - rp, nb * (BN / 2), lb);
+            } else {
+                tma_load_2d(sb, c.tmD, k0, nb * (BN / 2), lb);
+                tma_load_2d(sb + (BN / 2) * 128, c.tmB2, k0 - rp, nb * (BN / 2), lb);
+            }
+        } else {
+            tma_load_2d(sb, c.tmD, k0, b_row(c, a, nb, (int)c.rank), lb);
+        }
         // the copy must land before anyone may read or release the slot,
         // also when another role has given up (hence no abort check)
         if (!mbar_wait_token(lb, tok, 200000000ull, c.w.status, kSiteConvEmpty)) {
@@ -905,7 +921,7 @@ struct Gemm {
                 const float sb[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) y[i] = scale_bias(v[8 * g + i], sa, sb[i], a.bias, n + i);
-                if (EPI == kEpiSwiGLU) {
+                if (EPI == kEpiSwiGLU || EPI == kEpiSwiGLULora) {
                     const int nu = a.n_half + n;
                     const float4 t0 = __ldg(reinterpret_cast<const float4 *>(a.sb + nu));
                     const float4 t1 = __ldg(reinterpret_cast<const float4 *>(a.sb + nu) + 1);
@@ -959,20 +975,65 @@ struct Gemm {
         }
     }
 
+    // Fused LoRA, SwiGLU: 16 gate columns n0.. from the gate and up totals and
+    // their LoRA sums: g = bf16(bf16(base_g) + lora_g), u likewise, h =
+    // bf16(silu(g) * u) -- the rounded operations of the packed INT8 linear,
+    // the gate/up LoRA adds and the unfused SwiGLU.
+    static __device__ __forceinline__ void finish16_swiglu_lora(const GemmArgs &a, int row, int n0,
+                                                                const int32_t *tg, const int32_t *tu,
+                                                                const uint32_t (&lg)[16],
+                                                                const uint32_t (&lu)[16]) {
+        const float sa = __ldg(a.sa + row);
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            const int n = n0 + 8 * g;
+            if (n >= a.N) break;
+            const int nu = a.n_half + n;
+            float h[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float gb = bf16_round(scale_bias(__int2float_rn(tg[8 * g + i]), sa, __ldg(a.sb + n + i), a.bias, n + i));
+                const float ub = bf16_round(scale_bias(__int2float_rn(tu[8 * g + i]), sa, __ldg(a.sb + nu + i), a.bias, nu + i));
+                const float gv = bf16_round(__fadd_rn(gb, __uint_as_float(lg[8 * g + i])));
+                const float uv = bf16_round(__fadd_rn(ub, __uint_as_float(lu[8 * g + i])));
+                h[i] = silu_mul_fast(gv, uv);
+            }
+            uint4 pk = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]),
+                                  pack_bf16x2(h[4], h[5]), pack_bf16x2(h[6], h[7]));
+            *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + (int64_t)row * a.ldo + n) = pk;
+        }
+    }
+
     // Fused LoRA: finish this thread's row from its int32 totals and the LoRA
     // accumulator at tbase, 16 columns at a time (the accumulator is released
     // once its last columns are in registers).
     static __device__ __forceinline__ void finish_row_lora(const Ctx &c, const GemmArgs &a, int row, bool row_ok,
                                                            int nb, int half, const int32_t *tot, uint32_t tbase,
                                                            uint32_t acc, int lane) {
+        if constexpr (C::kSwiGLU) {
+            constexpr int kH = C::kChunks32 / 2;   // 32-column chunks of gate (then as many of up)
 #pragma unroll
-        for (int q = 0; q < 2 * C::kChunks32; ++q) {
-            const int j = q >> 1, o = 16 * (q & 1);
-            uint32_t lv[16];
-            tmem_ld16(tbase + chunk_col(j, half) + o, lv);
-            tmem_ld_wait();
-            if (q == 2 * C::kChunks32 - 1) release_acc(c, acc, lane);
-            if (row_ok) finish16_lora(a, row, nb * BN + chunk_col(j, half) + o, tot + 32 * j + o, lv);
+            for (int q = 0; q < 2 * kH; ++q) {
+                const int j = q >> 1, o = 16 * (q & 1);
+                uint32_t lg[16], lu[16];
+                tmem_ld16(tbase + chunk_col(j, half) + o, lg);
+                tmem_ld16(tbase + chunk_col(j + kH, half) + o, lu);
+                tmem_ld_wait();
+                if (q == 2 * kH - 1) release_acc(c, acc, lane);
+                if (row_ok)
+                    finish16_swiglu_lora(a, row, nb * (BN / 2) + chunk_col(j, half) + o, tot + 32 * j + o,
+                                         tot + 32 * (j + kH) + o, lg, lu);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 2 * C::kChunks32; ++q) {
+                const int j = q >> 1, o = 16 * (q & 1);
+                uint32_t lv[16];
+                tmem_ld16(tbase + chunk_col(j, half) + o, lv);
+                tmem_ld_wait();
+                if (q == 2 * C::kChunks32 - 1) release_acc(c, acc, lane);
+                if (row_ok) finish16_lora(a, row, nb * BN + chunk_col(j, half) + o, tot + 32 * j + o, lv);
+            }
         }
     }
 
@@ -1431,7 +1492,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if (C::kLoraSwi) tma_prefetch_desc(&tmB2);
+        if (C::kLoraSwi || (C::kLoraFused && C::kSwiGLU)) tma_prefetch_desc(&tmB2);
         if (EPI == kEpiAddBF16 || C::kLoraSwi || C::kLoraFused) tma_prefetch_desc(&tmC);
         if (C::kLoraSwi || C::kLoraFused) tma_prefetch_desc(&tmD);
     }
@@ -1458,6 +1519,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     c.epi = smem + C::NSTAGE * C::kStage + C::NRAW * C::kRawStage;   // 1024-aligned
     c.tmC = &tmC;
     c.tmD = &tmD;
+    c.tmB2 = &tmB2;
     c.bar = bar;
     const uint32_t own_tmem = bar->tmem_slot;
     if (PAIR) {
@@ -1572,10 +1634,17 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
                                 (uint64_t)args.M, (uint64_t)args.lora_ldt * 2, 64, C::BM,
                                 CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc) return rc;
+        const uint32_t brows = C::kSwiGLU ? BN / 2 : C::kBRows;
         rc = internal_make_tmap(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, args.lora_b, (uint64_t)args.lora_r,
-                                (uint64_t)args.N, (uint64_t)args.lora_r * 2, 64, C::kBRows,
+                                (uint64_t)args.N, (uint64_t)args.lora_r * 2, 64, brows,
                                 CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc) return rc;
+        if (C::kSwiGLU) {   // the up factor
+            rc = internal_make_tmap(&tb2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, args.lora_b2, (uint64_t)args.lora_r,
+                                    (uint64_t)args.N, (uint64_t)args.lora_r * 2, 64, brows,
+                                    CU_TENSOR_MAP_SWIZZLE_128B);
+            if (rc) return rc;
+        }
     }
     if (C::kLoraSwi) {
         if (!B2) return internal_cuda_error(cudaErrorInvalidValue, "LoRA gate/up needs the up factor");
@@ -1688,6 +1757,7 @@ int launch_gemm(int op, int epi, int bn, const Operand &A, const Operand &B, con
         if (epi == kEpiSwiGLU) CLEF_GEMM(kOpI8, kEpiSwiGLU, 256);
         if (epi == kEpiStoreS32) CLEF_GEMM(kOpI8, kEpiStoreS32, 256);
         if (epi == kEpiScaleBiasLora) CLEF_GEMM(kOpI8, kEpiScaleBiasLora, 256);
+        if (epi == kEpiSwiGLULora) CLEF_GEMM(kOpI8, kEpiSwiGLULora, 256);
     } else if (op == kOpF8 && bn == 256) {
         if (epi == kEpiScaleBias) CLEF_GEMM(kOpF8, kEpiScaleBias, 256);
         if (epi == kEpiSwiGLU) CLEF_GEMM(kOpF8, kEpiSwiGLU, 256);

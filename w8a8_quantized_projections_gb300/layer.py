@@ -37,7 +37,7 @@ import torch
 
 from . import (bind_workspace, fp8_gateup_swiglu, fp8_linear, gemm_workspace_bytes, lora_add,
                lora_expand_add, lora_gateup_swiglu, lora_pad, lora_shrink, poll_status, quant_act,
-               w8a8_gateup_swiglu, w8a8_linear, w8a8_linear_lora)
+               w8a8_gateup_swiglu, w8a8_gateup_swiglu_lora, w8a8_linear, w8a8_linear_lora)
 
 TIMEOUT = 4   # CLEF_ERR_TIMEOUT
 
@@ -50,10 +50,10 @@ class QuantizedLayer:
         lora: name (or name + "/gate", name + "/up" for gate/up) -> (A, B);
         pack_shared_input: run consecutive plain projections of one activation
         as one packed GEMM;
-        fuse_lora (INT8): add the LoRA of each adapted linear launch unit
-        inside its GEMM (one x A^T launch, then the GEMM with the expand fused)
-        instead of expand launches over the GEMM's output; the bytes are the
-        same.  Gate/up keeps its separate adapter + SwiGLU launch."""
+        fuse_lora (INT8): add each adapted launch unit's LoRA inside its GEMM
+        (one x A^T launch, then the GEMM with the expand fused; for gate/up
+        before the SwiGLU) instead of adapter launches over the GEMM's
+        output; the bytes are the same."""
         self.cfg = cfg
         self.M = cfg.M
         self.fp8 = cfg.scheme == "fp8"
@@ -163,9 +163,10 @@ class QuantizedLayer:
             fused = 0
             if gi in self.fused:
                 for p in g:
-                    if p.name in self.lora:
-                        N, r = self.lora[p.name][1].shape
-                        fused += 2 * self.M * N * r
+                    for key in ((p.name + "/gate", p.name + "/up") if p.kind == "gateup" else (p.name,)):
+                        if key in self.lora:
+                            N, r = self.lora[key][1].shape
+                            fused += 2 * self.M * N * r
             out.append((_unit_name(g), rows, g[0].K, 2 * self.M * rows * g[0].K, fused))
         return out
 
@@ -181,8 +182,9 @@ class QuantizedLayer:
                 f = self.fused[gi]
                 by += M * g[0].K * 2 + M * f.t.shape[1] * 2
                 for p in g:
-                    if p.name in self.lora:
-                        fl += 2 * M * self.lora[p.name][0].shape[0] * p.K
+                    for key in ((p.name + "/gate", p.name + "/up") if p.kind == "gateup" else (p.name,)):
+                        if key in self.lora:
+                            fl += 2 * M * self.lora[key][0].shape[0] * p.K
                 continue
             if gi in self.lora_groups:
                 _, t, blocks = self.lora_groups[gi]
@@ -301,9 +303,9 @@ class QuantizedLayer:
         return self.out
 
     def _step_fused(self, gi, g, acts, prev_h, ev):
-        """One linear launch unit with its LoRA fused: x A^T for all of the
-        unit's adapters in one launch, then the INT8 GEMM whose tiles add
-        t B^T to their rounded base values."""
+        """One launch unit with its LoRA fused: x A^T for all of the unit's
+        adapters in one launch, then the INT8 GEMM whose tiles add t B^T to
+        their rounded base values (gate/up: before the SwiGLU)."""
         f = self.fused[gi]
         qw, sw, b = self.unit_w[gi]
         p = g[0]
@@ -317,6 +319,10 @@ class QuantizedLayer:
             qx, sx = self.q[p.act]
         with ev("lora", name + ":xA"):
             lora_shrink(x, f.A, t=f.t)
+        if p.kind == "gateup":
+            with ev("gemm", name):
+                w8a8_gateup_swiglu_lora(qx, sx, qw, sw, b, f.t, f.B, f.B_up, h=self.out[p.name])
+            return self.out[p.name]
         y = self.unit_out[gi] if len(g) > 1 else self.out[p.name]
         with ev("gemm", name):
             w8a8_linear_lora(qx, sx, qw, sw, b, f.t, f.B, y=y, segments=f.segments)
@@ -372,18 +378,30 @@ class QuantizedLayer:
 
 
 def _fused_unit(g, lora, M, device):
-    """The fused-LoRA buffers of one linear launch unit, or None when it has
-    no adapter or its adapters cannot share one fused launch (a gate/up unit,
-    different ranks, more than four adapters, or column segments off the
-    256-column tiles).
+    """The fused-LoRA buffers of one launch unit, or None when it has no
+    adapter or its adapters cannot share one fused launch (different ranks,
+    more than four adapters, or column segments off the 256-column tiles).
 
-    A = the adapters' A factors stacked, each padded with zero rows to r_pad;
-    t = [M][sum r_pad]; B = [N_unit][r] with each adapter's B rows at its
-    projection's output columns (zero rows for a projection without an
-    adapter, which then adds exact zeros); segments map each projection's
-    columns to its t block."""
+    Linear units: A = the adapters' A factors stacked, each padded with zero
+    rows to r_pad; t = [M][sum r_pad]; B = [N_unit][r] with each adapter's B
+    rows at its projection's output columns (zero rows for a projection
+    without an adapter, which then adds exact zeros); segments map each
+    projection's columns to its t block.  Gate/up: A = [A_gate; A_up], t =
+    [M][2 r_pad], and the two B factors."""
     if g[0].kind == "gateup":
-        return None
+        p = g[0]
+        if p.name + "/gate" not in lora:
+            return None
+        (Ag, Bg), (Au, Bu) = lora[p.name + "/gate"], lora[p.name + "/up"]
+        r = Ag.shape[0]
+        if Au.shape[0] != r or Bg.shape[1] != r or Bu.shape[1] != r:
+            return None
+        rp = lora_pad(r)
+        A = torch.zeros((2 * rp, p.K), dtype=torch.bfloat16, device=device)
+        A[:r] = Ag
+        A[rp:rp + r] = Au
+        t = torch.empty((M, 2 * rp), dtype=torch.bfloat16, device=device)
+        return SimpleNamespace(A=A, t=t, B=Bg.contiguous(), B_up=Bu.contiguous(), segments=None)
     members = [p for p in g if p.name in lora]
     if not members:
         return None
@@ -409,7 +427,7 @@ def _fused_unit(g, lora, M, device):
             return None
         segments.append((c0, tcol))
     t = torch.empty((M, tb), dtype=torch.bfloat16, device=device)
-    return SimpleNamespace(A=A, t=t, B=B, segments=segments)
+    return SimpleNamespace(A=A, t=t, B=B, B_up=None, segments=segments)
 
 
 def _unit_name(group) -> str:
