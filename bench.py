@@ -55,6 +55,9 @@ def parse():
                     help="workload name (or its position 0-4 in the workload table) of the headline line")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip timing the other workloads in the same process")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="run the headline workload at this many tokens instead (a smaller case of the "
+                         "same kernels, for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -304,6 +307,9 @@ def main():
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
     cfg = S.workload(args.config)
+    if args.tokens:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, M=args.tokens)
     env = Env(args, rank, world, dev, dist, torch)
 
     line = measure(env, cfg, args.steps, headline=True)
