@@ -123,6 +123,11 @@ struct Cfg {
     // into the fp16 operand ring, the converters pass those stages through,
     // and the MMA issuer accumulates t B^T as the tile's last chunk
     static constexpr bool kLoraFused = (EPI == kEpiScaleBiasLora || EPI == kEpiSwiGLULora);
+    // Fused LoRA, B-factor rows one LoRA k-block stages per CTA: gate/up
+    // k-blocks carry one factor's rows only (gate or up, halved between a
+    // pair), each the operand of an N = BN/2 MMA into its half of the
+    // accumulator
+    static constexpr int kLoraBRows = kSwiGLU ? (PAIR ? BN / 4 : BN / 2) : kBRows;
     // epilogues that apply the row and column scales and the bias
     static constexpr bool kScaled =
         (EPI == kEpiScaleBias || EPI == kEpiSwiGLU || EPI == kEpiScaleBiasLora || EPI == kEpiSwiGLULora);
@@ -664,20 +669,16 @@ struct Gemm {
         uint8_t *sb = sa + C::kAStage;
         const int k0 = 64 * (kin - c.nkb);
         uint64_t *lb = &c.bar->ltma[cs];
-        const uint64_t tok = mbar_arrive_expect_tx_token(lb, C::kStage);
+        const uint64_t tok = mbar_arrive_expect_tx_token(lb, C::kAStage + C::kLoraBRows * 128);
         tma_load_2d(sa, c.tmC, lora_tcol(a, nb) + k0, row_a, lb);
         if (C::kSwiGLU) {
-            // gate rows see B_gate over t's first r_pad columns and zeros
-            // after (past B_gate's end); up rows zeros first (before B_up's
-            // start) and B_up after, so each half sums only its own adapter
+            // t's first r_pad columns (the gate adapter's) meet the gate
+            // factor's rows, the rest the up factor's; a pair splits the
+            // tile's BN/2 rows of either factor by halves
             const int rp = c.nl * 32;
-            if (PAIR) {
-                if (c.rank == 0) tma_load_2d(sb, c.tmD, k0, nb * (BN / 2), lb);
-                else tma_load_2d(sb, c.tmB2, k0 - rp, nb * (BN / 2), lb);
-            } else {
-                tma_load_2d(sb, c.tmD, k0, nb * (BN / 2), lb);
-                tma_load_2d(sb + (BN / 2) * 128, c.tmB2, k0 - rp, nb * (BN / 2), lb);
-            }
+            const bool up = k0 >= rp;
+            const int brow = nb * (BN / 2) + (PAIR ? (int)c.rank * C::kLoraBRows : 0);
+            tma_load_2d(sb, up ? c.tmB2 : c.tmD, up ? k0 - rp : k0, brow, lb);
         } else {
             tma_load_2d(sb, c.tmD, k0, b_row(c, a, nb, (int)c.rank), lb);
         }
@@ -855,12 +856,16 @@ struct Gemm {
             const int nl = lora_kblocks(c, sg);
             if (C::kLoraFused && nl > 0) {
                 // the tile's LoRA chunk: t B^T with bf16 operands into a fresh
-                // accumulator, which the epilogue adds to the rounded base values
-                constexpr uint32_t idesc_l = idesc_f32acc(1u, 1u, C::kTileRows, BN);
+                // accumulator, which the epilogue adds to the rounded base values.
+                // Gate/up: the first nl/2 k-blocks sum the gate adapter into the
+                // gate half of the columns, the rest the up adapter into the up half
+                constexpr uint32_t idesc_l = idesc_f32acc(1u, 1u, C::kTileRows, C::kSwiGLU ? BN / 2 : BN);
                 if (!wait_pair(&c.bar->acc_empty[acc], aph ^ 1u, c, kSiteMmaAccEmpty)) return;
                 tc_fence_after();
-                const uint32_t d = c.tmem + acc * BN;
                 for (int j = 0; j < nl; ++j) {
+                    const bool up = C::kSwiGLU && 2 * j >= nl;
+                    const int j0 = up ? nl / 2 : 0;   // the half's first k-block
+                    const uint32_t d = c.tmem + acc * BN + (up ? BN / 2 : 0);
                     if (!wait_pair(&c.bar->full[s], ph, c, kSiteMmaFull)) return;
                     tc_fence_after();
                     const uint32_t sa = smem_u32(c.stage + s * C::kStage);
@@ -869,7 +874,7 @@ struct Gemm {
                     for (int k = 0; k < C::kMmaPerKBlock; ++k) {
                         const uint64_t ad = sdesc_sw128(sa + 32 * k);
                         const uint64_t bd = sdesc_sw128(sb + 32 * k);
-                        const uint32_t accum = (j > 0 || k > 0) ? 1u : 0u;
+                        const uint32_t accum = (j > j0 || k > 0) ? 1u : 0u;
                         if (PAIR) mma2_f16(d, ad, bd, idesc_l, accum);
                         else mma_f16(d, ad, bd, idesc_l, accum);
                     }
@@ -1641,7 +1646,7 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
                                 (uint64_t)args.M, (uint64_t)args.lora_ldt * 2, 64, C::BM,
                                 CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc) return rc;
-        const uint32_t brows = C::kSwiGLU ? BN / 2 : C::kBRows;
+        const uint32_t brows = C::kLoraBRows;
         rc = internal_make_tmap(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, args.lora_b, (uint64_t)args.lora_r,
                                 (uint64_t)args.N, (uint64_t)args.lora_r * 2, 64, brows,
                                 CU_TENSOR_MAP_SWIZZLE_128B);

@@ -16,8 +16,9 @@
 // lanes, so the Walsh-Hadamard butterfly runs its strides 1..16 (1..32) inside
 // a thread and the rest as lane exchanges (xor 1, xor 2), in the fixed order
 // 1, 2, 4, ..., 64 with explicitly rounded fp32 add/sub (no contraction),
-// then one multiply by fp32(1/sqrt(128)).  The row's absmax is a warp-shuffle
-// max plus one shared-memory step; codes are written as 16-byte stores.
+// then one multiply by fp32(1/sqrt(128)).  The row's absmax is a warp
+// reduction (redux.sync on the bit patterns) per warp, then one over the
+// warps' partials through shared memory; codes are written as 16-byte stores.
 // Reads 2 B and writes 1 B per element, plus a 4 B scale per row.
 //
 // What it computes follows the "CLEF Calibrated INT8 ConvRot" model card
@@ -129,11 +130,12 @@ __device__ __forceinline__ void wht128_lanes(float (&v)[32], int lane) {
 // E .. 64 exchange whole pairs with lanes xor 1, xor 2.  Each output is the
 // same fp32 add or subtract of the same two values in the same stage order as
 // wht128_lanes.
-template <int NP>
+template <int NP, bool kStride1Done>
 __device__ __forceinline__ void wht128_pairs(uint64_t (&p)[NP], int lane) {
     static_assert(NP == 16 || NP == 32, "32 or 64 values per thread");
 #pragma unroll
     for (int i = 0; i < NP; ++i) {   // stride 1
+        if (kStride1Done) break;
         float a, b;
         unf2(p[i], a, b);
         p[i] = f2(__fadd_rn(a, b), __fsub_rn(a, b));
@@ -166,6 +168,31 @@ __device__ __forceinline__ void wht128_pairs(uint64_t (&p)[NP], int lane) {
     const uint64_t c2 = f2(c, c);
 #pragma unroll
     for (int k = 0; k < NP; ++k) p[k] = mul2(p[k], c2);
+}
+
+// The stride-1 butterfly of the bf16 pair (v0, v1) held in w (v0 in the low
+// half), straight from bf16 by mixed-precision add/sub (each the single
+// rounded fp32 operation on the widened values): (v0 + v1, v1 - v0).  The
+// second lane is the negated difference; every later stage pairs such lanes
+// only with each other, and fp32 add, subtract and multiply commute with
+// negation except for the sign of an exact zero, so the whole odd lane comes
+// out negated in magnitude-exact form and the codes take the multiplier -r
+// there.  (INT8 codes do not see the sign of a zero.)
+__device__ __forceinline__ uint64_t stride1_bf16(uint32_t w) {
+    const float v0 = __uint_as_float(w << 16);
+    float s, d;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, h, %3;\n\tsub.rn.f32.bf16 %1, h, %3;\n\t}"
+        : "=f"(s), "=f"(d) : "r"(w), "f"(v0));
+    return f2(s, d);
+}
+
+// Warp-wide maximum of non-negative finite-or-infinite floats: their bit
+// patterns order like unsigned integers.
+__device__ __forceinline__ float warp_max_nonneg(float a) {
+    uint32_t m;
+    asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(m) : "r"(__float_as_uint(a)));
+    return __uint_as_float(m);
 }
 
 __device__ __forceinline__ void load_chunk(const uint16_t *p, float (&v)[32]) {
@@ -237,11 +264,10 @@ __device__ __forceinline__ void store_codes(const float (&v)[32], float r, bool 
 
 // Codes of 32 values held as natural pairs (as store_codes).
 template <bool kInt8, bool kClamp = false>
-__device__ __forceinline__ void store_codes_pairs(const uint64_t *p, float r, bool zero_row,
+__device__ __forceinline__ void store_codes_pairs(const uint64_t *p, uint64_t r2, bool zero_row,
                                                   uint8_t *dst8) {
     uint32_t w[8];
     if (kInt8) {
-        const uint64_t r2 = f2(r, r);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             float u[4];
@@ -258,10 +284,9 @@ __device__ __forceinline__ void store_codes_pairs(const uint64_t *p, float r, bo
                 w[i] = 0u;
             } else {
                 float u[4];
-                unf2(p[2 * i], u[0], u[1]);
-                unf2(p[2 * i + 1], u[2], u[3]);
-                w[i] = e4m3x2(__fmul_rn(u[0], r), __fmul_rn(u[1], r)) |
-                       (e4m3x2(__fmul_rn(u[2], r), __fmul_rn(u[3], r)) << 16);
+                unf2(mul2(p[2 * i], r2), u[0], u[1]);
+                unf2(mul2(p[2 * i + 1], r2), u[2], u[3]);
+                w[i] = e4m3x2(u[0], u[1]) | (e4m3x2(u[2], u[3]) << 16);
             }
         }
     }
@@ -304,19 +329,10 @@ __global__ void __launch_bounds__(MAXT, MINB) quant_act_kernel(const uint16_t *_
 #pragma unroll
         for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[c][j]));
     }
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, s));
+    amax = warp_max_nonneg(amax);
     if (lane == 0) red[warp] = amax;
     __syncthreads();
-    if (warp == 0) {
-        const int nw = (int)(blockDim.x >> 5);
-        float a = lane < nw ? red[lane] : 0.0f;
-#pragma unroll
-        for (int s = 16; s > 0; s >>= 1) a = fmaxf(a, __shfl_xor_sync(kFull, a, s));
-        if (lane == 0) red[0] = a;
-    }
-    __syncthreads();
-    amax = red[0];
+    amax = warp_max_nonneg(lane < (int)(blockDim.x >> 5) ? red[lane] : 0.0f);
 
     const float qmax = kInt8 ? 127.0f : 448.0f;
     const bool stat = static_r > 0.0f;   // static scale: the row's amax is not used
@@ -408,37 +424,37 @@ quant_staged_kernel(const __grid_constant__ CUtensorMap tmx, int M, int K, int n
     // E = 64: the whole line t (eight units).  Either way a quarter-warp's
     // eight reads of one step hit eight different bank groups.
     constexpr int kU = E / 8;   // 16-byte units per thread
+    // stride 1 straight from bf16 with the odd lanes negated (INT8 only: the
+    // FP8 codes keep the sign of a zero)
+    constexpr bool kFold = kRotate && kInt8;
     const bool active = tid < nchunk;
-    const uint32_t line = (uint32_t)(E == 64 ? tid : tid >> 1);
+    // a thread past the row's end reads line 0 (its values are left out of
+    // the max and its codes are not stored)
+    const uint32_t line = active ? (uint32_t)(E == 64 ? tid : tid >> 1) : 0u;
     uint32_t off[kU];
 #pragma unroll
     for (int j = 0; j < kU; ++j)
         off[j] = line * 128u + (((uint32_t)((E == 64 ? 0 : (tid & 1) * 4) + j) ^ (line & 7u)) << 4);
 
-    int it = 0;
+    int it = 0, slot = 0;
+    uint32_t phase = 0, src = smem_u32(ring);
     for (int m = (int)blockIdx.x; m < M; m += (int)gridDim.x, ++it) {
-        const int slot = it % nslot;
-        mbar_wait(&full[slot], (uint32_t)(it / nslot) & 1u, w, kSiteQuantFull);
+        mbar_wait(&full[slot], phase, w, kSiteQuantFull);
         uint64_t p[E / 2];   // the thread's E values as natural pairs (v[2i], v[2i+1])
-        if (active) {
-            const uint32_t src = smem_u32(ring) + (uint32_t)slot * slot_stride;
 #pragma unroll
-            for (int j = 0; j < kU; ++j) {
-                uint32_t a0, a1, a2, a3;
-                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(src + off[j]));
-                const uint32_t ws[4] = {a0, a1, a2, a3};
+        for (int j = 0; j < kU; ++j) {
+            uint32_t a0, a1, a2, a3;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(src + off[j]));
+            const uint32_t ws[4] = {a0, a1, a2, a3};
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    p[4 * j + k] = f2(__uint_as_float(ws[k] << 16), __uint_as_float(ws[k] & 0xFFFF0000u));
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < E / 2; ++j) p[j] = 0ull;
+            for (int k = 0; k < 4; ++k)
+                p[4 * j + k] = kFold ? stride1_bf16(ws[k])
+                                     : f2(__uint_as_float(ws[k] << 16), __uint_as_float(ws[k] & 0xFFFF0000u));
         }
         // whole 128-blocks are active or inactive together (K % 128 == 0 in
         // the rotated modes), and every lane of the warp exists
-        if (kRotate) wht128_pairs<E / 2>(p, lane);
+        if (kRotate) wht128_pairs<E / 2, kFold>(p, lane);
         float amax = 0.0f;
 #pragma unroll
         for (int j = 0; j < E / 2; ++j) {
@@ -446,8 +462,8 @@ quant_staged_kernel(const __grid_constant__ CUtensorMap tmx, int M, int K, int n
             unf2(p[j], a, b);
             amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
         }
-#pragma unroll
-        for (int sh = 16; sh > 0; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, sh));
+        if (!active) amax = 0.0f;
+        amax = warp_max_nonneg(amax);
         if (lane == 0) red[it & 1][warp] = amax;
         __syncthreads();
         if (abort_flag) break;
@@ -458,32 +474,29 @@ quant_staged_kernel(const __grid_constant__ CUtensorMap tmx, int M, int K, int n
                 issue(slot, mn);
             }
         }
-        // the nw partial maxima: lane l reads partial l and five shuffles
-        // combine them (24,032 rows: K = 17408, 17 warps, 269.3 -> 261.6 us;
-        // 6144, 6 warps, 90.4 -> 88.1; 5120, 5 warps, 78.8 -> 77.8), or, for
-        // 64 values per thread or two warps at most, each thread reads all
-        // (K = 12288 with 64 per thread: 172.0 against 176.1 us)
-        if (E == 32 && nw > 2) {
-            amax = lane < nw ? red[it & 1][lane] : 0.0f;
-#pragma unroll
-            for (int sh = 16; sh > 0; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, sh));
-        } else {
-            amax = red[it & 1][0];
-            for (int k = 1; k < nw; ++k) amax = fmaxf(amax, red[it & 1][k]);
-        }
+        // the nw partial maxima: lane l reads partial l, one warp reduction
+        amax = warp_max_nonneg(lane < nw ? red[it & 1][lane] : 0.0f);
 
         const float qmax = kInt8 ? 127.0f : 448.0f;
         const bool stat = static_r > 0.0f;   // static scale: the row's amax is not used
         const bool zero_row = !stat && !(amax > 0.0f);
         const float r = stat ? static_r : (zero_row ? 0.0f : __fdiv_rn(qmax, amax));
         if (tid == 0) scale[m] = stat ? static_s : (zero_row ? 0.0f : __fdiv_rn(amax, qmax));
+        const uint64_t r2 = f2(r, kFold ? -r : r);
         if (active) {
             uint8_t *dst = q + (int64_t)m * K + E * tid;
 #pragma unroll
             for (int g = 0; g < E / 32; ++g) {
-                if (stat) store_codes_pairs<kInt8, kInt8>(p + 16 * g, r, false, dst + 32 * g);
-                else store_codes_pairs<kInt8>(p + 16 * g, r, zero_row, dst + 32 * g);
+                if (stat) store_codes_pairs<kInt8, kInt8>(p + 16 * g, r2, false, dst + 32 * g);
+                else store_codes_pairs<kInt8>(p + 16 * g, r2, zero_row, dst + 32 * g);
             }
+        }
+        if (++slot == nslot) {
+            slot = 0;
+            phase ^= 1u;
+            src = smem_u32(ring);
+        } else {
+            src += slot_stride;
         }
     }
     if (abort_flag && tid == 0) {
