@@ -60,6 +60,8 @@ def parse():
                          "same kernels, for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="launch in plain stream order (no programmatic dependent launch)")
     return ap.parse_args()
 
 
@@ -252,10 +254,14 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+PDL = True   # the library's programmatic-dependent-launch switch for this run
+
+
 def workload_config(cfg):
     d = {"workload": cfg.name, "tokens": cfg.M, "scheme": cfg.scheme,
          "projections": {p.name: [p.K, p.weight_rows] for p in cfg.projections},
-         "l2": "flushed between steps (256 MiB write, outside the per-step events)"}
+         "l2": "flushed between steps (256 MiB write, outside the per-step events)",
+         "launch": "programmatic dependent launch" if PDL else "plain stream order"}
     if cfg.lora_rank:
         d["lora_rank"] = cfg.lora_rank
     return d
@@ -305,6 +311,10 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl")
+    import w8a8_quantized_projections_gb300 as clef
+    global PDL
+    PDL = not args.no_pdl
+    clef.set_pdl(PDL)
     dev = torch.device("cuda", local)
     cfg = S.workload(args.config)
     if args.tokens:

@@ -409,6 +409,19 @@ void clef_test_force_timeout(int on);
  */
 void clef_set_quant_staging(int mode);
 
+/*
+ * clef_set_pdl -- programmatic dependent launch for the kernels the library
+ * launches afterwards.  on != 0 (default): each launch carries CUDA's
+ * programmatic stream-serialization attribute, so that a kernel's CTAs may be
+ * scheduled, and run their set-up (barriers, tensor-memory allocation,
+ * descriptor prefetch), while the stream's previous kernel finishes; every
+ * kernel waits for the kernels it follows to complete, with their writes
+ * visible, before it reads or writes global memory, so results are the same
+ * bytes either way.  on == 0: plain stream order.  The switch exists so that
+ * both can be tested and timed.
+ */
+void clef_set_pdl(int on);
+
 /* Human-readable name of a status code (static string). */
 const char *clef_status_string(int status);
 

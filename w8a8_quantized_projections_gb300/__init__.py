@@ -24,7 +24,7 @@ __all__ = [
     "fp8_linear", "fp8_gateup_swiglu", "lora_add", "lora_add_noalloc", "lora_shrink", "lora_expand_add",
     "lora_gateup_swiglu", "swiglu_bf16",
     "w8a8_gemm_s32", "w8a8_linear_lora", "w8a8_gateup_swiglu_lora",
-    "poll_status", "set_wait_limit_ns", "set_quant_staging", "ACT_MODES", "gemm_workspace_bytes",
+    "poll_status", "set_wait_limit_ns", "set_quant_staging", "set_pdl", "ACT_MODES", "gemm_workspace_bytes",
     "bind_workspace", "mma_peak",
 ]
 
@@ -475,6 +475,16 @@ def set_quant_staging(mode: int) -> None:
     L.clef_set_quant_staging.argtypes = [C.c_int]
     L.clef_set_quant_staging.restype = None
     L.clef_set_quant_staging(int(mode))
+
+
+def set_pdl(on: bool) -> None:
+    """Programmatic dependent launch for later launches (default on): a
+    kernel may start its set-up while the stream's previous kernel finishes;
+    the bytes computed are the same either way."""
+    L = library()
+    L.clef_set_pdl.argtypes = [C.c_int]
+    L.clef_set_pdl.restype = None
+    L.clef_set_pdl(1 if on else 0)
 
 
 def test_force_timeout(on) -> None:

@@ -46,6 +46,7 @@ size_t g_ws_count = 0;
 std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
 std::atomic<int> g_force_timeout{0};
 std::atomic<int> g_quant_staging{1};
+std::atomic<int> g_pdl{1};
 thread_local char g_last_err[256] = "";
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -358,6 +359,8 @@ int internal_cuda_error(cudaError_t e, const char *what) { return cuda_fail(e, w
 
 void internal_set_error(const char *msg) { snprintf(g_last_err, sizeof g_last_err, "%s", msg); }
 
+bool internal_pdl() { return g_pdl.load() != 0; }
+
 }  // namespace clef
 
 using namespace clef;
@@ -623,6 +626,8 @@ void clef_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
 void clef_test_force_timeout(int on) { g_force_timeout.store(on < 0 ? 0 : on); }
 
 void clef_set_quant_staging(int mode) { g_quant_staging.store(mode < 0 ? 0 : (mode > 2 ? 2 : mode)); }
+
+void clef_set_pdl(int on) { g_pdl.store(on ? 1 : 0); }
 
 const char *clef_status_string(int status) {
     switch (status) {

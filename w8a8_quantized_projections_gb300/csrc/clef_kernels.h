@@ -3,10 +3,48 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace clef {
+
+// The library's programmatic-dependent-launch switch (clef_set_pdl).
+bool internal_pdl();
+
+// Launch a kernel of the library: cluster_x > 1 launches clusters of that
+// many CTAs; with pdl and the library's PDL switch on, the launch carries the
+// programmatic stream-serialization attribute, so the kernel's CTAs may be
+// scheduled (and run their set-up) while the stream's previous kernel
+// finishes.  Every kernel of the library therefore signals its dependents once
+// its own work is done (pdl_launch_dependents) and waits for the grids it
+// depends on (pdl_wait) before its first access to global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          int cluster_x, bool pdl, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl && internal_pdl()) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 enum ActMode : int { kActInt8H128 = 0, kActFp8 = 1, kActFp8H128 = 2 };
 

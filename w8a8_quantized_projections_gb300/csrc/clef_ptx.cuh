@@ -45,6 +45,18 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---------------------------------------------------------------- launch order
+
+// Programmatic dependent launch: let the stream's next kernel be scheduled
+// (its CTAs then run their set-up and wait in pdl_wait), and wait until every
+// grid this one depends on has completed with its writes visible.  Both are
+// no-ops without the programmatic serialization attribute on the dependent's
+// launch.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {

@@ -1517,6 +1517,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     __syncthreads();
     if (PAIR) cluster_sync();  // both CTAs' barriers and TMEM are set up
     tc_fence_after();
+    // the set-up above touches no global memory; everything after may read
+    // what the stream's previous kernels wrote
+    pdl_wait();
 
     typename G::Ctx c;
     c.stage = smem;
@@ -1588,6 +1591,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         if (kF8Split) asm volatile("setmaxnreg.inc.sync.aligned.u32 104;");
         G::epilogue(c, args);
     }
+    // this thread's role is done: the stream's next kernel may be scheduled
+    // (signalling at the start instead measured slower on the long INT8
+    // GEMMs' steps)
+    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     if (PAIR) {
@@ -1606,6 +1613,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         else
             tmem_dealloc(own_tmem, C::kTmemCols);
     }
+}
+
+// Programmatic dependent launch for a GEMM whose CTAs (pairs) each run at
+// most 128 k-blocks: there the previous kernel's tail and this one's launch
+// and set-up are a visible share of the time (the 1,502-token FP8 layer step
+// 272 -> 260 us, the 298-token linear 34 -> 31 us), while the long INT8
+// GEMMs measured slower with it (the 24,032-token layer step +0.7%).
+// k-blocks per tile of a launch (INT8: 64 of K; bf16: 64; FP8: 128)
+inline int64_t nkb_of_op(int op, int64_t K) { return op == kOpF8 ? (K + 127) / 128 : (K + 63) / 64; }
+
+inline bool short_launch(int tiles, int64_t nkb, int ctas) {
+    return ctas > 0 && (int64_t)tiles * nkb <= 128 * (int64_t)ctas;
 }
 
 template <int OP, int EPI, int BN, bool PAIR>
@@ -1675,20 +1694,20 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
     const int num_n = (args.N + C::kOutColsPerTile - 1) / C::kOutColsPerTile;
     const int tiles = num_m * num_n;
     if (PAIR) {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.blockDim = dim3(C::kThreads, 1, 1);
-        cfg.dynamicSmemBytes = C::kSmemBytes;
-        cfg.stream = st;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
         // persistent pairs: no more than can be resident at once
         static int max_pairs = -1;
         if (max_pairs < 0) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.blockDim = dim3(C::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = C::kSmemBytes;
+            cfg.stream = st;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
             cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
             int n = 0;
             e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
@@ -1731,12 +1750,12 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
                 pairs = tail0 > 0 ? max_pairs : p2;
             }
         }
-        cfg.gridDim = dim3(2 * pairs, 1, 1);
-        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, tc, td, la);
+        e = launch_kernel(kern, dim3(2 * pairs), dim3(C::kThreads), C::kSmemBytes, st, 2,
+                          short_launch(tiles, nkb_of_op(OP, args.K) + (C::kLoraFused ? args.lora_nkb : 0), pairs), ta, tb, tb2, tc, td, la);
     } else {
         const int grid = tiles < num_sms ? tiles : num_sms;
-        kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(ta, tb, tb2, tc, td, args);
-        e = cudaGetLastError();
+        e = launch_kernel(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, st, 1,
+                          short_launch(tiles, nkb_of_op(OP, args.K) + (C::kLoraFused ? args.lora_nkb : 0), grid), ta, tb, tb2, tc, td, args);
     }
     if (e != cudaSuccess) return internal_cuda_error(e, "gemm launch");
     return 0;

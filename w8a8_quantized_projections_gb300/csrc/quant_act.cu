@@ -311,6 +311,7 @@ __global__ void __launch_bounds__(MAXT, MINB) quant_act_kernel(const uint16_t *_
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nchunk = (int)(K >> 5);
     const uint16_t *xr = x + m * ldx;
+    pdl_wait();   // the row may come from the stream's previous kernel
 
     float v[C][32];
     float amax = 0.0f;
@@ -348,6 +349,7 @@ __global__ void __launch_bounds__(MAXT, MINB) quant_act_kernel(const uint16_t *_
         if (stat) store_codes<kInt8, kInt8>(v[c], r, false, qr + 32 * (int64_t)ch);
         else store_codes<kInt8>(v[c], r, zero_row, qr + 32 * (int64_t)ch);
     }
+    pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------- staged kernel
@@ -401,6 +403,7 @@ quant_staged_kernel(const __grid_constant__ CUtensorMap tmx, int M, int K, int n
         fence_barrier_init();
     }
     __syncthreads();
+    pdl_wait();   // the rows may come from the stream's previous kernel
     WaitCtx w;
     w.limit_ns = limit_ns;
     w.abort = &abort_flag;
@@ -499,6 +502,7 @@ quant_staged_kernel(const __grid_constant__ CUtensorMap tmx, int M, int K, int n
             src += slot_stride;
         }
     }
+    pdl_launch_dependents();   // this CTA's rows are done
     if (abort_flag && tid == 0) {
         // let the copies already issued into the ring land before the CTA exits
         for (int k = it; k < it + nslot; ++k) {
@@ -582,10 +586,9 @@ cudaError_t launch_staged(const StagedPlan &p, const uint16_t *x, int64_t M, int
     const int per_sm = resident < p.ctas_per_sm ? resident : p.ctas_per_sm;
     const int64_t want = (int64_t)per_sm * env.num_sms;
     const int grid = (int)(M < want ? M : want);
-    kern<<<grid, p.threads, p.smem, st>>>(tm, (int)M, (int)K, p.nslot, p.slot_stride, p.nbox,
-                                          p.box_rows, q, scale, env.status, env.wait_limit_ns,
-                                          env.static_r, env.static_s);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(p.threads), p.smem, st, 1, true, tm, (int)M, (int)K, p.nslot,
+                         p.slot_stride, p.nbox, p.box_rows, q, scale, env.status, env.wait_limit_ns,
+                         env.static_r, env.static_s);
 }
 
 template <int MODE>
@@ -608,19 +611,18 @@ cudaError_t launch_mode(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, ui
     const int64_t nchunk = K / 32;
     if (nchunk <= 576) {
         const int T = (int)((nchunk + 31) / 32 * 32);
-        quant_act_kernel<MODE, 1, 576, 2><<<(unsigned)M, T, 0, st>>>(x, K, ldx, q, scale, env.static_r,
-                                                                      env.static_s);
-    } else if (nchunk <= 1024) {
-        const int T = (int)((nchunk + 31) / 32 * 32);
-        quant_act_kernel<MODE, 1, 1024, 1><<<(unsigned)M, T, 0, st>>>(x, K, ldx, q, scale, env.static_r,
-                                                                      env.static_s);
-    } else {
-        const int64_t per = (nchunk + 1) / 2;
-        const int T = (int)((per + 31) / 32 * 32);
-        quant_act_kernel<MODE, 2, 1024, 1><<<(unsigned)M, T, 0, st>>>(x, K, ldx, q, scale, env.static_r,
-                                                                      env.static_s);
+        return launch_kernel(quant_act_kernel<MODE, 1, 576, 2>, dim3((unsigned)M), dim3(T), 0, st, 1, true, x, K, ldx,
+                             q, scale, env.static_r, env.static_s);
     }
-    return cudaGetLastError();
+    if (nchunk <= 1024) {
+        const int T = (int)((nchunk + 31) / 32 * 32);
+        return launch_kernel(quant_act_kernel<MODE, 1, 1024, 1>, dim3((unsigned)M), dim3(T), 0, st, 1, true, x, K,
+                             ldx, q, scale, env.static_r, env.static_s);
+    }
+    const int64_t per = (nchunk + 1) / 2;
+    const int T = (int)((per + 31) / 32 * 32);
+    return launch_kernel(quant_act_kernel<MODE, 2, 1024, 1>, dim3((unsigned)M), dim3(T), 0, st, 1, true, x, K, ldx, q,
+                         scale, env.static_r, env.static_s);
 }
 
 }  // namespace

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "clef_kernels.h"
+#include "clef_ptx.cuh"
 
 namespace clef {
 
@@ -36,6 +37,7 @@ __global__ void __launch_bounds__(256) swiglu_bf16_kernel(const uint16_t *__rest
                                                           uint16_t *__restrict__ h, int64_t ldh) {
     const int64_t groups_per_row = N / 8;
     const int64_t total = M * groups_per_row;
+    pdl_wait();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t m = i / groups_per_row, n = (i - m * groups_per_row) * 8;
@@ -48,6 +50,7 @@ __global__ void __launch_bounds__(256) swiglu_bf16_kernel(const uint16_t *__rest
             o[k] = pack(silu_mul(lo16(gw[k]), lo16(uw[k])), silu_mul(hi16(gw[k]), hi16(uw[k])));
         *reinterpret_cast<uint4 *>(h + m * ldh + n) = make_uint4(o[0], o[1], o[2], o[3]);
     }
+    pdl_launch_dependents();
 }
 
 }  // namespace
@@ -62,8 +65,8 @@ cudaError_t launch_swiglu_bf16(const uint16_t *y_gu, int64_t M, int64_t N, int64
     const int64_t cap = (int64_t)sms * 8;  // 8 resident blocks of 256 threads per SM
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    swiglu_bf16_kernel<<<(unsigned)blocks, 256, 0, st>>>(y_gu, M, N, ldg, h, ldh);
-    return cudaGetLastError();
+    return launch_kernel(swiglu_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1, true, y_gu, M, N, ldg, h,
+                         ldh);
 }
 
 }  // namespace clef
