@@ -116,6 +116,10 @@ struct GemmArgs {
     // tile order: 0 = M fastest (running CTAs share weight tiles), 1 = N
     // fastest (running CTAs share activation row blocks: LoRA x A^T)
     int n_fastest;
+    // M fastest: tiles are ordered in bands of band_m row blocks, all of a
+    // band's column blocks before the next band, so that a band's A rows stay
+    // in L2 while the weights stream past (0 = one band; the launcher sets it)
+    int band_m;
     // kEpiStoreBF16 with two stacked B factors: rows from b2_row0 on come from
     // the second operand (its row b2_row0 less); 0 = one B operand
     int b2_row0;

@@ -444,20 +444,27 @@ struct Gemm {
         int slot, nslots;    // tile-loop start and stride
         int num_m, num_n, num_tiles, nkb;
         int n_fastest;       // tile order: 0 = M fastest, 1 = N fastest
+        int band_m;          // M fastest: row blocks per band (1 .. num_m)
         int force_timeout;   // test knob: this CTA's MMA issuer waits on a barrier nothing signals
         int nl;              // fused LoRA: bf16 k-blocks per tile (0 = none)
         WaitCtx w;
     };
 
-    // M-fastest: the CTAs running at the same time share B (weight) tiles;
+    // M-fastest: the CTAs running at the same time share B (weight) tiles,
+    // within bands of band_m row blocks (a band's every column block before
+    // the next band), so that the band's A rows are read from DRAM once;
     // N-fastest: they share A row blocks (x A^T, where x is the large operand).
     static __device__ __forceinline__ void tile_coords(const Ctx &c, int t, int &mb, int &nb) {
         if (c.n_fastest) {
             nb = t % c.num_n;
             mb = t / c.num_n;
         } else {
-            mb = t % c.num_m;
-            nb = t / c.num_m;
+            const int band = t / (c.band_m * c.num_n);
+            const int m0 = band * c.band_m;
+            const int rows = min(c.band_m, c.num_m - m0);
+            const int local = t - band * c.band_m * c.num_n;
+            mb = m0 + local % rows;
+            nb = local / rows;
         }
     }
 
@@ -1549,6 +1556,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     c.num_tiles = c.num_m * c.num_n;
     c.nkb = C::kI8 ? (args.K + 63) / 64 : (args.K + C::BK - 1) / C::BK;
     c.n_fastest = args.n_fastest;
+    c.band_m = (args.band_m > 0 && args.band_m < c.num_m) ? args.band_m : c.num_m;
 
     c.force_timeout = args.force_timeout == 1 || (args.force_timeout >= 2 && args.force_timeout - 2 == c.slot);
     c.nl = C::kLoraFused ? args.lora_nkb : 0;
@@ -1620,6 +1628,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 // and set-up are a visible share of the time (the 1,502-token FP8 layer step
 // 272 -> 260 us, the 298-token linear 34 -> 31 us), while the long INT8
 // GEMMs measured slower with it (the 24,032-token layer step +0.7%).
+// Row blocks per band of the M-fastest tile order: as many as keep the band's
+// A rows (the activations) within 40 MB, a third of L2, so that they are read
+// from DRAM once while the weight tiles stream past; bands of even size.
+// Without bands a launch whose activations exceed L2 re-reads them for every
+// column block (24,032 x 34,816 x 5,120 INT8: 17.8 GB of DRAM reads).
+inline int band_rows(int num_m, int tile_rows, int64_t K, int a_bytes) {
+    const int64_t per = (int64_t)tile_rows * K * a_bytes;
+    int64_t band = ((int64_t)40 << 20) / (per > 0 ? per : 1);
+    if (band < 1) band = 1;
+    if (band >= num_m) return num_m;
+    const int64_t nbands = (num_m + band - 1) / band;
+    return (int)((num_m + nbands - 1) / nbands);
+}
+
 // k-blocks per tile of a launch (INT8: 64 of K; bf16: 64; FP8: 128)
 inline int64_t nkb_of_op(int op, int64_t K) { return op == kOpF8 ? (K + 127) / 128 : (K + 63) / 64; }
 
@@ -1717,6 +1739,7 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
         GemmArgs la = args;
         la.sk = 0;
         la.sk_tail0 = 0;
+        la.band_m = band_rows(num_m, C::kTileRows, args.K, OP == kOpBF16 ? 2 : 1);
         if (C::kStreamK && args.sk_ws && args.sk_cnt) {
             // Stream-K where the last wave of whole tiles would leave more
             // than 8% of the pairs' time idle (the GEMM time follows the count
@@ -1754,8 +1777,10 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
                           short_launch(tiles, nkb_of_op(OP, args.K) + (C::kLoraFused ? args.lora_nkb : 0), pairs), ta, tb, tb2, tc, td, la);
     } else {
         const int grid = tiles < num_sms ? tiles : num_sms;
+        GemmArgs la = args;
+        la.band_m = band_rows(num_m, C::kTileRows, args.K, OP == kOpBF16 ? 2 : 1);
         e = launch_kernel(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, st, 1,
-                          short_launch(tiles, nkb_of_op(OP, args.K) + (C::kLoraFused ? args.lora_nkb : 0), grid), ta, tb, tb2, tc, td, args);
+                          short_launch(tiles, nkb_of_op(OP, args.K) + (C::kLoraFused ? args.lora_nkb : 0), grid), ta, tb, tb2, tc, td, la);
     }
     if (e != cudaSuccess) return internal_cuda_error(e, "gemm launch");
     return 0;
