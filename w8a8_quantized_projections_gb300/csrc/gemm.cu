@@ -1629,13 +1629,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 // 272 -> 260 us, the 298-token linear 34 -> 31 us), while the long INT8
 // GEMMs measured slower with it (the 24,032-token layer step +0.7%).
 // Row blocks per band of the M-fastest tile order: as many as keep the band's
-// A rows (the activations) within 40 MB, a third of L2, so that they are read
-// from DRAM once while the weight tiles stream past; bands of even size.
-// Without bands a launch whose activations exceed L2 re-reads them for every
-// column block (24,032 x 34,816 x 5,120 INT8: 17.8 GB of DRAM reads).
+// A rows (the activations) within 24 MB of L2, so that they are read from DRAM
+// once while the weight tiles stream past; bands of even size.  Without bands
+// a launch whose activations exceed L2 re-reads them for every column block
+// (24,032 x 34,816 x 5,120 INT8: 17.8 GB of DRAM reads).  The 24,032-token
+// layer step with bands of 16 / 24 / 40 / 64 / 96 MB: 11.83 / 11.84 / 11.87 /
+// 11.97 / 12.01 ms (12.59 unbanded).
 inline int band_rows(int num_m, int tile_rows, int64_t K, int a_bytes) {
     const int64_t per = (int64_t)tile_rows * K * a_bytes;
-    int64_t band = ((int64_t)40 << 20) / (per > 0 ? per : 1);
+    int64_t band = ((int64_t)24 << 20) / (per > 0 ? per : 1);
     if (band < 1) band = 1;
     if (band >= num_m) return num_m;
     const int64_t nbands = (num_m + band - 1) / band;
