@@ -139,3 +139,28 @@ def test_stream_k_swiglu_equals_unsplit(M, N, K):
     finally:
         clef.bind_workspace(None)
     assert torch.equal(split.view(torch.int16), plain.view(torch.int16))
+
+
+# Banded tile order (row blocks ordered in bands whose activations fit 24 MB
+# of L2, every column block of a band before the next band): K = 17408 gives
+# bands of at most 5 row blocks; M = 2800 has 11 row blocks (bands 4, 4, 3),
+# M = 6000 24 (5, 5, 5, 5, 4) and 24,032 rows 94 (bands of 5, the last of 4;
+# the full-size workload tests).  With N =
+# 2048 the 2,800-row launch has 88 tiles for 76 pairs (stream-K splits the
+# last 12); every row block's first and last row and both rows at each CTA
+# pair boundary are compared with the oracle's exact int32 sums.
+@pytest.mark.parametrize("M,N,K,split", [(2800, 2048, 17408, False), (2800, 2048, 17408, True),
+                                         (6000, 512, 17408, False)])
+def test_banded_order_s32_equals_oracle(orc, M, N, K, split):
+    qx, qw = codes(M + 7, M, K), codes(K + 7, N, K)
+    qx_d, qw_d = dev(qx), dev(qw)
+    ws = bound_workspace() if split else None
+    try:
+        got = host(clef.w8a8_gemm_s32(qx_d, qw_d))
+    finally:
+        if split:
+            clef.bind_workspace(None)
+    rows = np.unique(np.r_[np.arange(0, M, 128), np.minimum(np.arange(127, M + 127, 128), M - 1),
+                           np.arange(255, M, 256), np.arange(256, M, 256)])
+    ref = par_rows(lambda a, b: orc.int8_gemm_acc(qx[rows][a:b], qw), len(rows))
+    assert np.array_equal(got[rows], ref)
