@@ -139,7 +139,11 @@ int clef_w8a8_gateup_swiglu(const int8_t *qx, const float *sx, const int8_t *qw_
 /*
  * clef_fp8_linear -- FP8 e4m3 W8A8 dynamic linear [FP8: Quantization table,
  * "Weights FP8, per-channel; Activations FP8, per-token, dynamic"].
- *   acc = sum_k qx[m][k] * qw[n][k] in fp32 (tensor-core accumulation order)
+ *   acc = sum_k qx[m][k] * qw[n][k] in fp32 (tensor-core accumulation order;
+ *         for K >= 8192, K is cut into three fixed parts of ceil(ceil(K/128)
+ *         / 3) * 128 elements (the last the rest), each summed apart, the
+ *         three added in K order, for every M, so that a row's bits never
+ *         depend on the call's row count or on a split)
  *   y[m][n] = bf16(((float)acc * sx[m]) * sw[n] + bias[n])
  * qx: e4m3 [M][K]; qw: e4m3 [N][K]; other arguments as clef_w8a8_linear.
  */
@@ -330,13 +334,16 @@ int clef_lora_add_noalloc(const void *x, int64_t ldx, const void *A, const void 
  * x 17408 take the same time unsplit), so a shape with a partly empty last
  * wave gains up to the idle fraction.  A launch of less than one wave is
  * split only when its tiles would keep under an eighth of the pairs busy
- * (small M, long K); the gate/up SwiGLU call and the FP8 calls (whose fp32
- * sums would change with the split) never split.
+ * (small M, long K); the gate/up SwiGLU calls never split.  clef_fp8_linear
+ * with K >= 8192 sums every tile's K as three fixed parts whatever M is (see
+ * there); with a workspace bound, the tiles of a last wave that fits three
+ * times in the pairs run as their parts on three pairs each, the same bytes
+ * as unsplit.  Other FP8 calls never split.
  * clef_gemm_workspace_bytes: the size needed on the current device (about
  * 38 MB on a 152-SM GB300), written to *bytes.
  * clef_bind_workspace: binds a caller-owned device buffer of that size to
- * `stream` on the current device (ws = NULL unbinds); INT8 GEMM calls on that
- * stream may then use it, calls on unbound streams never split.  The buffer
+ * `stream` on the current device (ws = NULL unbinds); INT8 and FP8 linear
+ * calls on that stream may then use it, calls on unbound streams never split.  The buffer
  * must be zero-filled when bound; every launch leaves its counter block
  * zeroed again (after a CLEF_ERR_TIMEOUT, refill the buffer with zeros before
  * further use).  Launches that use one buffer must not run concurrently: bind

@@ -164,3 +164,42 @@ def test_banded_order_s32_equals_oracle(orc, M, N, K, split):
                            np.arange(255, M, 256), np.arange(256, M, 256)])
     ref = par_rows(lambda a, b: orc.int8_gemm_acc(qx[rows][a:b], qw), len(rows))
     assert np.array_equal(got[rows], ref)
+
+
+# FP8 linear with K >= 8192: every tile sums its K as two fixed halves; with a
+# workspace bound, a last wave that fits twice in the pairs runs as halves on
+# two pairs (1502 x 4096 x 12288: 96 tiles for 76 pairs, 20 halved; 257 x
+# 4096 x 8192: 32 tiles under one wave, all halved).  The bytes equal the
+# unsplit launch's, and a call's rows equal the same rows called alone (100
+# rows: single CTAs, the same halves), and sampled rows meet the oracle's FP8
+# bar.
+@pytest.mark.parametrize("M,N,K", [(1502, 4096, 12288), (257, 4096, 8192)])
+def test_fp8_halves_split_equals_unsplit_and_rows(orc, M, N, K):
+    import clef_synth as S
+    from gpu_util import bf16_dev, bf16_host
+    from test_gpu_parity import assert_rms_close
+    x = S.activation(0, f"t/f8h/{M}x{N}x{K}/x", M, K)
+    w = S.weight(0, f"t/f8h/{M}x{N}x{K}/w", N, K)
+    b = S.bias(0, f"t/f8h/{M}x{N}x{K}/b", N)
+    qx, sx = clef.quant_act(bf16_dev(x), "fp8")
+    qw, sw = clef.quant_act(bf16_dev(w), "fp8")
+    bd = bf16_dev(b)
+    plain = clef.fp8_linear(qx, sx, qw, sw, bd)
+    ws = bound_workspace()
+    try:
+        for _ in range(3):
+            split = clef.fp8_linear(qx, sx, qw, sw, bd)
+            assert torch.equal(split.view(torch.int16), plain.view(torch.int16))
+        torch.cuda.synchronize()
+        assert int(ws[:COUNTER_BYTES].count_nonzero()) == 0
+    finally:
+        clef.bind_workspace(None)
+    full = host(plain.view(torch.int16))
+    for a in (0, M // 2, M - 100):
+        part = clef.fp8_linear(qx[a:a + 100].contiguous(), sx[a:a + 100].contiguous(), qw, sw, bd)
+        assert np.array_equal(host(part.view(torch.int16)), full[a:a + 100]), a
+    rows = np.unique(np.r_[0:2, M // 2, M - 2:M])
+    qxr, sxr = orc.quant_fp8(x[rows])
+    qwh, swh = par_rows(lambda a, c: orc.quant_fp8(w[a:c]), N)
+    ref = orc.fp8_linear(qxr, sxr, qwh, swh, b)
+    assert_rms_close(full[rows].view(np.uint16), ref, 1e-2, "fp8_linear halves")

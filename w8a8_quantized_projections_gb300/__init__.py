@@ -319,8 +319,8 @@ def gemm_workspace_bytes() -> int:
 
 def bind_workspace(ws, stream=None):
     """Bind a zero-filled uint8 CUDA buffer of gemm_workspace_bytes() to
-    `stream` (default: the current stream) so that INT8 GEMMs launched on it
-    may split tiles across SMs; ws = None unbinds.  The buffer is kept alive
+    `stream` (default: the current stream) so that INT8 GEMMs and FP8 linears
+    launched on it may split tiles across SMs; ws = None unbinds.  The buffer is kept alive
     while bound."""
     s = stream if stream is not None else torch.cuda.current_stream()
     key = (torch.cuda.current_device(), s.cuda_stream)

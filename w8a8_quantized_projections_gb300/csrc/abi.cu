@@ -221,7 +221,8 @@ int run_w8a8(int op, int epi, const void *qx, const float *sx, const void *qw, c
     a.bias = static_cast<const uint16_t *>(bias);
     a.out = out;
     a.ldo = ldo;
-    if (op == kOpI8) {   // a workspace bound to this stream lets tiles be split across SMs
+    if (op == kOpI8 || (op == kOpF8 && epi == kEpiScaleBias)) {
+        // a workspace bound to this stream lets tiles be split across SMs
         std::lock_guard<std::mutex> lk(g_mu);
         for (size_t i = 0; i < g_ws_count; ++i)
             if (g_ws[i].dev == d->index && g_ws[i].stream == stream) {

@@ -135,7 +135,18 @@ struct Cfg {
     // but not the SwiGLU one: the gate/up launches of the workloads fill at
     // least 94% of their last wave, and with the split path compiled in the
     // unsplit gate/up kernel ran 1.2% slower (352.7 against 344.5 us)
-    static constexpr bool kStreamK = kI8 && PAIR && !kSwiGLU && !kLoraFused;
+    //
+    // FP8 linear: a launch with K of at least 64 k-blocks (8,192) sums each
+    // tile's K as kKParts fixed parts (ceil(nkb / kKParts) k-blocks each, the
+    // last the rest), accumulator chunks that the epilogue adds in fp32 in K
+    // order.  The cut depends on K alone and the parts are added in the same
+    // order whether a tile runs whole or its parts run on several CTA pairs
+    // (stream-K over a partly empty last wave, the parts meeting in the
+    // workspace), so a row's bits do not depend on M.
+    static constexpr bool kHalves = (OP == kOpF8 && EPI == kEpiScaleBias);
+    static constexpr int kHalvesMinKBlocks = 64;
+    static constexpr int kKParts = 3;
+    static constexpr bool kStreamK = PAIR && ((kI8 && !kSwiGLU && !kLoraFused) || kHalves);
     static constexpr int kOutColsPerTile = kSwiGLU ? BN / 2 : BN;
     // full[s]: TMA (native) or the local converter warps (INT8); in pair mode
     // the leader's barrier also counts the peer's forwarded readiness.
@@ -447,6 +458,7 @@ struct Gemm {
         int band_m;          // M fastest: row blocks per band (1 .. num_m)
         int force_timeout;   // test knob: this CTA's MMA issuer waits on a barrier nothing signals
         int nl;              // fused LoRA: bf16 k-blocks per tile (0 = none)
+        int chunk;           // k-blocks per accumulator chunk
         WaitCtx w;
     };
 
@@ -829,8 +841,8 @@ struct Gemm {
         const Segs sp = seg_plan(c);
         for (int si = 0; si < sp.total; ++si) {
             const Seg sg = seg_at(c, sp, si);
-            for (int kb0 = sg.kb0; kb0 < sg.kb1; kb0 += C::kChunkKBlocks) {
-                const int kb1 = min(sg.kb1, kb0 + C::kChunkKBlocks);
+            for (int kb0 = sg.kb0; kb0 < sg.kb1; kb0 += c.chunk) {
+                const int kb1 = min(sg.kb1, kb0 + c.chunk);
                 if (!wait_pair(&c.bar->acc_empty[acc], aph ^ 1u, c, kSiteMmaAccEmpty)) return;
                 tc_fence_after();
                 const uint32_t d = c.tmem + acc * BN;
@@ -1259,15 +1271,19 @@ struct Gemm {
         const int first = sk_bound(c, q) >= (tile - sk_tail0(c)) * c.nkb ? 0 : 1;
         return ((q * 2 + first) * 2 + (int)c.rank) * C::kEpiWarps + e;
     }
+    // (T = int32_t: exact integer sums, in any order; T = uint32_t: the fp32
+    // bit patterns of an FP8 tile's K parts, added in K order)
+    template <class T>
     static __device__ bool sk_combine(const Ctx &c, const GemmArgs &a, const Seg &sg, int e, int lane,
-                                      int32_t (&tot)[C::kColsPerThread]) {
+                                      T (&tot)[C::kColsPerThread]) {
         constexpr int kV = C::kColsPerThread / 4;   // int4 per lane per block
         static_assert(32 * kV * 16 == 16384, "workspace block");
         {
             int4 *mine = a.sk_ws + (int64_t)sk_block(c, c.slot, sg.tile, e) * (32 * kV) + lane;
 #pragma unroll
             for (int j = 0; j < kV; ++j)
-                mine[j * 32] = make_int4(tot[4 * j], tot[4 * j + 1], tot[4 * j + 2], tot[4 * j + 3]);
+                mine[j * 32] = make_int4((int)tot[4 * j], (int)tot[4 * j + 1], (int)tot[4 * j + 2],
+                                         (int)tot[4 * j + 3]);
         }
         __threadfence();
         __syncwarp();
@@ -1279,6 +1295,36 @@ struct Gemm {
         old = __shfl_sync(0xFFFFFFFFu, old, 0);
         if (old != q1 - q0) return false;
         __threadfence();
+        if constexpr (!(sizeof(T) == 4 && T(-1) < T(0))) {
+            // fp32 parts: summed in K order from the workspace, this piece's
+            // own included, as a whole tile sums its chunks
+            {
+                const int4 *o = a.sk_ws + (int64_t)sk_block(c, q0, sg.tile, e) * (32 * kV) + lane;
+#pragma unroll
+                for (int j = 0; j < kV; ++j) {
+                    const int4 v = __ldcg(o + j * 32);
+                    tot[4 * j] = (T)v.x;
+                    tot[4 * j + 1] = (T)v.y;
+                    tot[4 * j + 2] = (T)v.z;
+                    tot[4 * j + 3] = (T)v.w;
+                }
+            }
+#pragma unroll 1
+            for (int q = q0 + 1; q <= q1; ++q) {
+                const int4 *o = a.sk_ws + (int64_t)sk_block(c, q, sg.tile, e) * (32 * kV) + lane;
+#pragma unroll
+                for (int j = 0; j < kV; ++j) {
+                    const int4 v = __ldcg(o + j * 32);
+                    const int vs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        tot[4 * j + i] =
+                            __float_as_uint(__fadd_rn(__uint_as_float(tot[4 * j + i]), __int_as_float(vs[i])));
+                }
+            }
+            if (lane == 0) atomicExch(cnt, 0);   // zero again for the next launch
+            return true;
+        }
 #pragma unroll 1
         for (int q = q0; q <= q1; ++q) {
             if (q == c.slot) continue;
@@ -1330,7 +1376,7 @@ struct Gemm {
                 int32_t tot[C::kColsPerThread];
 #pragma unroll
                 for (int i = 0; i < C::kColsPerThread; ++i) tot[i] = 0;
-                for (int kb0 = sg.kb0; kb0 < sg.kb1; kb0 += C::kChunkKBlocks) {
+                for (int kb0 = sg.kb0; kb0 < sg.kb1; kb0 += c.chunk) {
                     if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
                     tc_fence_after();
                     const uint32_t tbase = c.tmem + acc * BN + lane_off;
@@ -1443,6 +1489,37 @@ struct Gemm {
                     y_tile_store(c, a, t, b);
                 }
                 ++yiter;
+            } else if constexpr (C::kHalves) {
+                // FP8 linear: the tile's (or the stream-K piece's) accumulator
+                // chunks, the first as it is, the later K parts added in fp32 in
+                // K order; a split tile's parts meet in the workspace, where the
+                // piece arriving last sums them all in K order
+                uint32_t v[C::kColsPerThread];
+                for (int kb0 = sg.kb0; kb0 < sg.kb1; kb0 += c.chunk) {
+                    if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
+                    tc_fence_after();
+                    const uint32_t tbase = c.tmem + acc * BN + lane_off;
+                    if (kb0 == sg.kb0) {
+#pragma unroll
+                        for (int j = 0; j < C::kChunks32; ++j)
+                            tmem_ld32(tbase + chunk_col(j, half), *reinterpret_cast<uint32_t(*)[32]>(v + 32 * j));
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < C::kChunks32; ++j) {
+                            uint32_t r[32];
+                            tmem_ld32(tbase + chunk_col(j, half), r);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                v[32 * j + i] = __float_as_uint(
+                                    __fadd_rn(__uint_as_float(v[32 * j + i]), __uint_as_float(r[i])));
+                        }
+                    }
+                    release_acc(c, acc, lane);
+                    if (++acc == (uint32_t)C::kAccBufs) { acc = 0; aph ^= 1u; }
+                }
+                if (sg.part < 0 || sk_combine(c, a, sg, e, lane, v)) finish_row(a, row, row_ok, nb, half, v);
             } else {
                 if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
                 tc_fence_after();
@@ -1560,6 +1637,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 
     c.force_timeout = args.force_timeout == 1 || (args.force_timeout >= 2 && args.force_timeout - 2 == c.slot);
     c.nl = C::kLoraFused ? args.lora_nkb : 0;
+    c.chunk = C::kI8 ? C::kChunkKBlocks
+                     : ((C::kHalves && c.nkb >= C::kHalvesMinKBlocks) ? (c.nkb + C::kKParts - 1) / C::kKParts
+                                                                       : (1 << 30));
     c.w.limit_ns = args.wait_limit_ns;
     c.w.abort = &bar->abort;
     c.w.status = args.status;
@@ -1571,11 +1651,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     // warps, 4 x 32 x 56 + 16 x 32 x 104 = 60,416 of 61,440 (removes the
     // epilogue's spill; the 1502 x 24576 x 4096 call 104.0 -> 102.4 us)
     constexpr bool kF8Split = OP == kOpF8 && C::kEpiWarps == 16 && C::kEpiWarp0 == 4;
+    // FP8 linear (8 epilogue warps; 12 launched at 168 registers), whose
+    // epilogue holds a tile row's first K half while it adds the second:
+    // 4 x 32 x 56 + 8 x 32 x 224 = 64,512 of 64,512
+    constexpr bool kF8LinSplit = C::kHalves && C::kEpiWarps == 8 && C::kEpiWarp0 == 4;
     if (warp < C::kEpiWarp0) {
         // INT8: control and converter warps hand registers to the epilogue
         // warps, which hold the int32 totals
         if (C::kI8) asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
-        if (kF8Split) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+        if (kF8Split || kF8LinSplit) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
         if (warp == 0) {
             if (lane == 0) {
                 G::producer(c, &tmA, &tmB, &tmB2, args, fills);
@@ -1597,6 +1681,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     } else {
         if (C::kI8) asm volatile("setmaxnreg.inc.sync.aligned.u32 192;");
         if (kF8Split) asm volatile("setmaxnreg.inc.sync.aligned.u32 104;");
+        if (kF8LinSplit) asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
         G::epilogue(c, args);
     }
     // this thread's role is done: the stream's next kernel may be scheduled
@@ -1742,7 +1827,23 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
         la.sk = 0;
         la.sk_tail0 = 0;
         la.band_m = band_rows(num_m, C::kTileRows, args.K, OP == kOpBF16 ? 2 : 1);
-        if (C::kStreamK && args.sk_ws && args.sk_cnt) {
+        const int nkb_h = (args.K + C::BK - 1) / C::BK;
+        if (C::kStreamK && C::kHalves && args.sk_ws && args.sk_cnt) {
+            // FP8 linear with K parts: when the tiles left after the whole
+            // waves fit kKParts times in the pairs, each runs as its parts (its
+            // own accumulator chunks, cut by K alone) on kKParts pairs, so the
+            // last wave takes a part's time: pair p < kKParts R runs part
+            // p % kKParts of tail tile p / kKParts.
+            const int tail0 = (tiles / max_pairs) * max_pairs;
+            const int rest = tiles - tail0;
+            if (nkb_h >= C::kHalvesMinKBlocks && nkb_h % C::kKParts == 0 && rest > 0 &&
+                C::kKParts * rest <= max_pairs && tiles <= kSkMaxTiles &&
+                args.sk_ws_bytes >= (int64_t)max_pairs * kSkBytesPerPair) {
+                la.sk = C::kKParts * rest;
+                la.sk_tail0 = tail0;
+                pairs = tail0 > 0 ? max_pairs : la.sk;
+            }
+        } else if (C::kStreamK && args.sk_ws && args.sk_cnt) {
             // Stream-K where the last wave of whole tiles would leave more
             // than 8% of the pairs' time idle (the GEMM time follows the count
             // of waves: 1502 x 5120 x 17408 and 1502 x 6400 x 17408 both take

@@ -80,11 +80,11 @@ class QuantizedLayer:
                 self.w[p.name] = (qw[r0:r1], sw[r0:r1], None if b is None else b[r0:r1])
                 r0 = r1
         torch.cuda.synchronize()
-        # INT8: a stream-K workspace, bound to whichever stream runs a step
-        # (tiles of a GEMM whose last wave would be mostly idle are split
-        # across SMs; the outputs are the same bytes)
-        self.ws = None if self.fp8 else torch.zeros(gemm_workspace_bytes(), dtype=torch.uint8,
-                                                     device=device)
+        # a stream-K workspace, bound to whichever stream runs a step (tiles of
+        # a GEMM whose last wave would be mostly idle are split across SMs: the
+        # INT8 GEMMs' exact int32 pieces, the FP8 linear's fixed K halves; the
+        # outputs are the same bytes)
+        self.ws = torch.zeros(gemm_workspace_bytes(), dtype=torch.uint8, device=device)
         self._ws_stream = None   # the stream the workspace was last bound to
         # fused LoRA (INT8): per adapted launch unit, its stacked A factors, its
         # t, its stacked B factor(s) and the column segments of its adapters
