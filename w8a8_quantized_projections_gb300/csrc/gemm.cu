@@ -143,10 +143,10 @@ struct Cfg {
     // order whether a tile runs whole or its parts run on several CTA pairs
     // (stream-K over a partly empty last wave, the parts meeting in the
     // workspace), so a row's bits do not depend on M.
-    static constexpr bool kHalves = (OP == kOpF8 && EPI == kEpiScaleBias);
-    static constexpr int kHalvesMinKBlocks = 64;
+    static constexpr bool kKSplit = (OP == kOpF8 && EPI == kEpiScaleBias);
+    static constexpr int kKSplitMinKBlocks = 64;
     static constexpr int kKParts = 3;
-    static constexpr bool kStreamK = PAIR && ((kI8 && !kSwiGLU && !kLoraFused) || kHalves);
+    static constexpr bool kStreamK = PAIR && ((kI8 && !kSwiGLU && !kLoraFused) || kKSplit);
     static constexpr int kOutColsPerTile = kSwiGLU ? BN / 2 : BN;
     // full[s]: TMA (native) or the local converter warps (INT8); in pair mode
     // the leader's barrier also counts the peer's forwarded readiness.
@@ -1489,7 +1489,7 @@ struct Gemm {
                     y_tile_store(c, a, t, b);
                 }
                 ++yiter;
-            } else if constexpr (C::kHalves) {
+            } else if constexpr (C::kKSplit) {
                 // FP8 linear: the tile's (or the stream-K piece's) accumulator
                 // chunks, the first as it is, the later K parts added in fp32 in
                 // K order; a split tile's parts meet in the workspace, where the
@@ -1638,7 +1638,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     c.force_timeout = args.force_timeout == 1 || (args.force_timeout >= 2 && args.force_timeout - 2 == c.slot);
     c.nl = C::kLoraFused ? args.lora_nkb : 0;
     c.chunk = C::kI8 ? C::kChunkKBlocks
-                     : ((C::kHalves && c.nkb >= C::kHalvesMinKBlocks) ? (c.nkb + C::kKParts - 1) / C::kKParts
+                     : ((C::kKSplit && c.nkb >= C::kKSplitMinKBlocks) ? (c.nkb + C::kKParts - 1) / C::kKParts
                                                                        : (1 << 30));
     c.w.limit_ns = args.wait_limit_ns;
     c.w.abort = &bar->abort;
@@ -1652,9 +1652,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     // epilogue's spill; the 1502 x 24576 x 4096 call 104.0 -> 102.4 us)
     constexpr bool kF8Split = OP == kOpF8 && C::kEpiWarps == 16 && C::kEpiWarp0 == 4;
     // FP8 linear (8 epilogue warps; 12 launched at 168 registers), whose
-    // epilogue holds a tile row's first K half while it adds the second:
-    // 4 x 32 x 56 + 8 x 32 x 224 = 64,512 of 64,512
-    constexpr bool kF8LinSplit = C::kHalves && C::kEpiWarps == 8 && C::kEpiWarp0 == 4;
+    // epilogue holds a tile row's running sum of the K parts while it reads
+    // the next part: 4 x 32 x 56 + 8 x 32 x 224 = 64,512 of 64,512
+    constexpr bool kF8LinSplit = C::kKSplit && C::kEpiWarps == 8 && C::kEpiWarp0 == 4;
     if (warp < C::kEpiWarp0) {
         // INT8: control and converter warps hand registers to the epilogue
         // warps, which hold the int32 totals
@@ -1827,8 +1827,8 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
         la.sk = 0;
         la.sk_tail0 = 0;
         la.band_m = band_rows(num_m, C::kTileRows, args.K, OP == kOpBF16 ? 2 : 1);
-        const int nkb_h = (args.K + C::BK - 1) / C::BK;
-        if (C::kStreamK && C::kHalves && args.sk_ws && args.sk_cnt) {
+        const int nkb_k = (args.K + C::BK - 1) / C::BK;
+        if (C::kStreamK && C::kKSplit && args.sk_ws && args.sk_cnt) {
             // FP8 linear with K parts: when the tiles left after the whole
             // waves fit kKParts times in the pairs, each runs as its parts (its
             // own accumulator chunks, cut by K alone) on kKParts pairs, so the
@@ -1836,7 +1836,7 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
             // p % kKParts of tail tile p / kKParts.
             const int tail0 = (tiles / max_pairs) * max_pairs;
             const int rest = tiles - tail0;
-            if (nkb_h >= C::kHalvesMinKBlocks && nkb_h % C::kKParts == 0 && rest > 0 &&
+            if (nkb_k >= C::kKSplitMinKBlocks && nkb_k % C::kKParts == 0 && rest > 0 &&
                 C::kKParts * rest <= max_pairs && tiles <= kSkMaxTiles &&
                 args.sk_ws_bytes >= (int64_t)max_pairs * kSkBytesPerPair) {
                 la.sk = C::kKParts * rest;
