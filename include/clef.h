@@ -111,7 +111,8 @@ int clef_quant_act_static(const void *x, int64_t M, int64_t K, int64_t ldx, int 
  *   y[m][n]   = bf16(((float)acc * sx[m]) * sw[n] + bias[n])
  * qx: int8 [M][K] dense; sx: fp32 [M]; qw: int8 [N][K] dense; sw: fp32 [N];
  * bias: bf16 [N] or NULL; y: bf16 [M][N], row pitch ldy elements.
- * Requirements: K % 16 == 0, N % 8 == 0, ldy >= N, ldy % 8 == 0.  The
+ * Requirements: K % 16 == 0, N % 8 == 0, ldy >= N, ldy % 8 == 0; qx, qw,
+ * sw, bias and y 16-byte aligned, sx 4-byte.  The
  * library receives bare pointers and cannot check buffer lengths: sx must
  * hold M values and sw and bias N (the packed gate/up calls: 2N), else the
  * kernels read past their ends.

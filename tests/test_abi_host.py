@@ -66,7 +66,7 @@ def test_quant_act_static_rotated_needs_whole_blocks(mode):
 
 @pytest.mark.parametrize("name", ["clef_w8a8_linear", "clef_fp8_linear", "clef_w8a8_gateup_swiglu",
                                   "clef_fp8_gateup_swiglu"])
-@pytest.mark.parametrize("bad", ["null_qx", "N8", "K16", "ldy", "align", "sw_align"])
+@pytest.mark.parametrize("bad", ["null_qx", "N8", "K16", "ldy", "align", "sw_align", "bias_align"])
 def test_gemm_rejects_bad_arguments(name, bad):
     qx, sx, qw, sw, bias, M, N, K, y, ldy = FAKE, FAKE, FAKE, FAKE, NUL, 4, 256, 256, FAKE, 256
     if bad == "null_qx":
@@ -81,6 +81,8 @@ def test_gemm_rejects_bad_arguments(name, bad):
         y = ODD
     elif bad == "sw_align":
         sw = ODD
+    elif bad == "bias_align":     # the epilogue reads 8 bias columns per 16-byte load
+        bias = ODD
     assert getattr(clef.library(), name)(qx, sx, qw, sw, bias, M, N, K, y, ldy, S) == 1
 
 

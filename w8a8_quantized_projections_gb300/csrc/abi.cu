@@ -197,7 +197,7 @@ int check_gemm(const void *qx, const float *sx, const void *qw, const float *sw,
     if (!aligned16(qx) || !aligned16(qw) || !aligned16(out)) return arg_fail("operand/output not 16-byte aligned");
     if (scaled && (!aligned16(sw) || (reinterpret_cast<uintptr_t>(sx) & 3u)))
         return arg_fail("weight scales must be 16-byte aligned, row scales 4-byte aligned");
-    if (bias && (reinterpret_cast<uintptr_t>(bias) & 1u)) return arg_fail("bias not 2-byte aligned");
+    if (bias && !aligned16(bias)) return arg_fail("bias not 16-byte aligned");
     return CLEF_OK;
 }
 

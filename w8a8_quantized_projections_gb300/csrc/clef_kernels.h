@@ -102,6 +102,8 @@ struct GemmArgs {
     const uint16_t *bias;    // bf16, may be null
     void *out;               // bf16 or int32 output
     int64_t ldo;             // output row pitch (elements)
+    int out_v32;             // bf16 output whose every row starts on a 32-byte
+                             // boundary (the launcher sets it)
     unsigned int *status;    // device status word
     uint64_t wait_limit_ns;
     int *dbg;                // optional: per CTA, its own TMEM base and the one it uses

@@ -304,12 +304,57 @@ __device__ __forceinline__ float silu_mul_fast(float g, float u) {
     return __fmul_rn(__fdividef(g * sc, d * sc), u);
 }
 
-// Epilogue value of one accumulator: ((acc * sa) * sb) + bias, each rounded.
-__device__ __forceinline__ float scale_bias(float acc, float sa, float sb, const uint16_t *bias,
-                                            int n) {
-    float y = __fmul_rn(__fmul_rn(acc, sa), sb);
-    if (bias) y = __fadd_rn(y, __uint_as_float((uint32_t)__ldg(bias + n) << 16));
-    return y;
+// Epilogue value of one accumulator: ((acc * sa) * sb) + bias, each rounded
+// (no bias: no add, so a -0 product stays -0).
+__device__ __forceinline__ float scale_bias(float acc, float sa, float sb, float bias, bool has_bias) {
+    const float y = __fmul_rn(__fmul_rn(acc, sa), sb);
+    return has_bias ? __fadd_rn(y, bias) : y;
+}
+
+// Column scales and biases of output columns n .. n + 7 (n % 8 == 0; sb and
+// the bias 16-byte aligned): two 16-byte loads of sb and one of the bias.
+// Every lane of a warp reads the same columns, so each load is one L1
+// wavefront -- eight scalar loads per column group were the epilogue's
+// largest L1 cost, taken at every tile's end while the next tile's first
+// k-blocks were being widened.
+__device__ __forceinline__ void load_cols8(const float *sb, const uint16_t *bias, int n, float (&s)[8],
+                                           float (&b)[8]) {
+    const float4 s0 = __ldg(reinterpret_cast<const float4 *>(sb + n));
+    const float4 s1 = __ldg(reinterpret_cast<const float4 *>(sb + n) + 1);
+    s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
+    s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
+    if (bias) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(bias + n));
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            b[2 * i] = bf16_lo(ww[i]);
+            b[2 * i + 1] = bf16_hi(ww[i]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) b[i] = 0.0f;
+    }
+}
+
+// Output columns n .. n + 15 of one row (bf16; w: eight packed words in
+// column order).  One 32-byte store when every row of the output starts on a
+// 32-byte boundary (out_v32) and all 16 columns lie inside N, else 16-byte
+// stores of the 8-column groups inside N (N % 8 == 0).  A warp's lanes hold
+// 32 different rows, so every store instruction touches 32 lines: the wider
+// store halves the instructions and the L1 work of the epilogue's writes.
+__device__ __forceinline__ void store_bf16x16(const GemmArgs &a, int row, int n, const uint32_t (&w)[8]) {
+    if (n >= a.N) return;
+    uint16_t *p = static_cast<uint16_t *>(a.out) + (int64_t)row * a.ldo + n;
+    if (a.out_v32 && n + 16 <= a.N) {
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                     :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                        "r"(w[7])
+                     : "memory");
+    } else {
+        *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        if (n + 8 < a.N) *reinterpret_cast<uint4 *>(p + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+    }
 }
 
 // ---------------------------------------------------------------- CTA pairs
@@ -934,42 +979,44 @@ struct Gemm {
                                                     const float (&u)[32]) {
         if (!row_ok) return;
         const float sa = C::kScaled ? __ldg(a.sa + row) : 0.0f;
+        const bool hb = a.bias != nullptr;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const int n = n0 + 8 * g;
-            if (n >= a.N) break;  // N % 8 == 0: whole groups in or out
-            float y[8];
-            if (C::kScaled) {
-                const float4 s0 = __ldg(reinterpret_cast<const float4 *>(a.sb + n));
-                const float4 s1 = __ldg(reinterpret_cast<const float4 *>(a.sb + n) + 1);
-                const float sb[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        for (int h = 0; h < 2; ++h) {
+            uint32_t w[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) y[i] = scale_bias(v[8 * g + i], sa, sb[i], a.bias, n + i);
-                if (EPI == kEpiSwiGLU || EPI == kEpiSwiGLULora) {
-                    const int nu = a.n_half + n;
-                    const float4 t0 = __ldg(reinterpret_cast<const float4 *>(a.sb + nu));
-                    const float4 t1 = __ldg(reinterpret_cast<const float4 *>(a.sb + nu) + 1);
-                    const float su[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+            for (int g2 = 0; g2 < 2; ++g2) {
+                const int g = 2 * h + g2, n = n0 + 8 * g;
+                float y[8];
+                if (n >= a.N) {   // N % 8 == 0: whole groups in or out
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        y[i] = silu(y[i], scale_bias(u[8 * g + i], sa, su[i], a.bias, nu + i));
+                    for (int i = 0; i < 8; ++i) y[i] = 0.0f;
+                } else if (C::kScaled) {
+                    float sb[8], bb[8];
+                    load_cols8(a.sb, a.bias, n, sb, bb);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) y[i] = scale_bias(v[8 * g + i], sa, sb[i], bb[i], hb);
+                    if (EPI == kEpiSwiGLU || EPI == kEpiSwiGLULora) {
+                        load_cols8(a.sb, a.bias, a.n_half + n, sb, bb);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) y[i] = silu(y[i], scale_bias(u[8 * g + i], sa, sb[i], bb[i], hb));
+                    }
+                } else if (EPI == kEpiAddBF16) {
+                    const uint4 o = *reinterpret_cast<const uint4 *>(
+                        static_cast<const uint16_t *>(a.out) + (int64_t)row * a.ldo + n);
+                    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        y[2 * i] = __fadd_rn(bf16_lo(ow[i]), v[8 * g + 2 * i]);
+                        y[2 * i + 1] = __fadd_rn(bf16_hi(ow[i]), v[8 * g + 2 * i + 1]);
+                    }
+                } else {  // kEpiStoreBF16
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) y[i] = v[8 * g + i];
                 }
-            } else if (EPI == kEpiAddBF16) {
-                const uint4 o = *reinterpret_cast<const uint4 *>(
-                    static_cast<const uint16_t *>(a.out) + (int64_t)row * a.ldo + n);
-                const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    y[2 * i] = __fadd_rn(bf16_lo(ow[i]), v[8 * g + 2 * i]);
-                    y[2 * i + 1] = __fadd_rn(bf16_hi(ow[i]), v[8 * g + 2 * i + 1]);
-                }
-            } else {  // kEpiStoreBF16
-#pragma unroll
-                for (int i = 0; i < 8; ++i) y[i] = v[8 * g + i];
+                for (int i = 0; i < 4; ++i) w[4 * g2 + i] = pack_bf16x2(y[2 * i], y[2 * i + 1]);
             }
-            uint4 pk = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                                  pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
-            *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + (int64_t)row * a.ldo + n) = pk;
+            store_bf16x16(a, row, n0 + 16 * h, w);
         }
     }
 
@@ -980,23 +1027,28 @@ struct Gemm {
     static __device__ __forceinline__ void finish16_lora(const GemmArgs &a, int row, int n0, const int32_t *tot,
                                                          const uint32_t (&lv)[16]) {
         const float sa = __ldg(a.sa + row);
+        const bool hb = a.bias != nullptr;
+        uint32_t w[8];
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
             const int n = n0 + 8 * g;
-            if (n >= a.N) break;   // N % 8 == 0: whole groups in or out
-            const float4 s0 = __ldg(reinterpret_cast<const float4 *>(a.sb + n));
-            const float4 s1 = __ldg(reinterpret_cast<const float4 *>(a.sb + n) + 1);
-            const float sb[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
             float y[8];
+            if (n < a.N) {   // N % 8 == 0: whole groups in or out
+                float sb[8], bb[8];
+                load_cols8(a.sb, a.bias, n, sb, bb);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float base = bf16_round(scale_bias(__int2float_rn(tot[8 * g + i]), sa, sb[i], a.bias, n + i));
-                y[i] = __fadd_rn(base, __uint_as_float(lv[8 * g + i]));
+                for (int i = 0; i < 8; ++i) {
+                    const float base = bf16_round(scale_bias(__int2float_rn(tot[8 * g + i]), sa, sb[i], bb[i], hb));
+                    y[i] = __fadd_rn(base, __uint_as_float(lv[8 * g + i]));
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) y[i] = 0.0f;
             }
-            uint4 pk = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                                  pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
-            *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + (int64_t)row * a.ldo + n) = pk;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[4 * g + i] = pack_bf16x2(y[2 * i], y[2 * i + 1]);
         }
+        store_bf16x16(a, row, n0, w);
     }
 
     // Fused LoRA, SwiGLU: 16 gate columns n0.. from the gate and up totals and
@@ -1008,24 +1060,32 @@ struct Gemm {
                                                                 const uint32_t (&lg)[16],
                                                                 const uint32_t (&lu)[16]) {
         const float sa = __ldg(a.sa + row);
+        const bool hb = a.bias != nullptr;
+        uint32_t w[8];
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
             const int n = n0 + 8 * g;
-            if (n >= a.N) break;
-            const int nu = a.n_half + n;
             float h[8];
+            if (n < a.N) {
+                float sg[8], bg[8], su[8], bu[8];
+                load_cols8(a.sb, a.bias, n, sg, bg);
+                load_cols8(a.sb, a.bias, a.n_half + n, su, bu);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float gb = bf16_round(scale_bias(__int2float_rn(tg[8 * g + i]), sa, __ldg(a.sb + n + i), a.bias, n + i));
-                const float ub = bf16_round(scale_bias(__int2float_rn(tu[8 * g + i]), sa, __ldg(a.sb + nu + i), a.bias, nu + i));
-                const float gv = bf16_round(__fadd_rn(gb, __uint_as_float(lg[8 * g + i])));
-                const float uv = bf16_round(__fadd_rn(ub, __uint_as_float(lu[8 * g + i])));
-                h[i] = silu_mul_fast(gv, uv);
+                for (int i = 0; i < 8; ++i) {
+                    const float gb = bf16_round(scale_bias(__int2float_rn(tg[8 * g + i]), sa, sg[i], bg[i], hb));
+                    const float ub = bf16_round(scale_bias(__int2float_rn(tu[8 * g + i]), sa, su[i], bu[i], hb));
+                    const float gv = bf16_round(__fadd_rn(gb, __uint_as_float(lg[8 * g + i])));
+                    const float uv = bf16_round(__fadd_rn(ub, __uint_as_float(lu[8 * g + i])));
+                    h[i] = silu_mul_fast(gv, uv);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) h[i] = 0.0f;
             }
-            uint4 pk = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]),
-                                  pack_bf16x2(h[4], h[5]), pack_bf16x2(h[6], h[7]));
-            *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + (int64_t)row * a.ldo + n) = pk;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[4 * g + i] = pack_bf16x2(h[2 * i], h[2 * i + 1]);
         }
+        store_bf16x16(a, row, n0, w);
     }
 
     // Fused LoRA: finish this thread's row from its int32 totals and the LoRA
@@ -1708,11 +1768,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
 }
 
-// Programmatic dependent launch for a GEMM whose CTAs (pairs) each run at
-// most 128 k-blocks: there the previous kernel's tail and this one's launch
-// and set-up are a visible share of the time (the 1,502-token FP8 layer step
-// 272 -> 260 us, the 298-token linear 34 -> 31 us), while the long INT8
-// GEMMs measured slower with it (the 24,032-token layer step +0.7%).
 // Row blocks per band of the M-fastest tile order: as many as keep the band's
 // A rows (the activations) within 24 MB of L2, so that they are read from DRAM
 // once while the weight tiles stream past; bands of even size.  Without bands
@@ -1729,9 +1784,20 @@ inline int band_rows(int num_m, int tile_rows, int64_t K, int a_bytes) {
     return (int)((num_m + nbands - 1) / nbands);
 }
 
+// Every row of the output starts on a 32-byte boundary (bf16 outputs): the
+// epilogue may store 16 columns of a row at once.
+inline int out_rows_v32(const GemmArgs &a) {
+    return ((reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 && a.ldo % 16 == 0) ? 1 : 0;
+}
+
 // k-blocks per tile of a launch (INT8: 64 of K; bf16: 64; FP8: 128)
 inline int64_t nkb_of_op(int op, int64_t K) { return op == kOpF8 ? (K + 127) / 128 : (K + 63) / 64; }
 
+// Programmatic dependent launch for a GEMM whose CTAs (pairs) each run at
+// most 128 k-blocks: there the previous kernel's tail and this one's launch
+// and set-up are a visible share of the time (the 1,502-token FP8 layer step
+// 272 -> 260 us, the 298-token linear 34 -> 31 us), while the long INT8
+// GEMMs measured slower with it (the 24,032-token layer step +0.7%).
 inline bool short_launch(int tiles, int64_t nkb, int ctas) {
     return ctas > 0 && (int64_t)tiles * nkb <= 128 * (int64_t)ctas;
 }
@@ -1824,6 +1890,7 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
         }
         int pairs = tiles < max_pairs ? tiles : max_pairs;
         GemmArgs la = args;
+        la.out_v32 = out_rows_v32(args);
         la.sk = 0;
         la.sk_tail0 = 0;
         la.band_m = band_rows(num_m, C::kTileRows, args.K, OP == kOpBF16 ? 2 : 1);
@@ -1881,6 +1948,7 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
     } else {
         const int grid = tiles < num_sms ? tiles : num_sms;
         GemmArgs la = args;
+        la.out_v32 = out_rows_v32(args);
         la.band_m = band_rows(num_m, C::kTileRows, args.K, OP == kOpBF16 ? 2 : 1);
         e = launch_kernel(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, st, 1,
                           short_launch(tiles, nkb_of_op(OP, args.K) + (C::kLoraFused ? args.lora_nkb : 0), grid), ta, tb, tb2, tc, td, la);
