@@ -1,6 +1,6 @@
 """The binding's checks of buffer lengths the C ABI cannot see (it receives
-bare pointers): short or long scale and bias vectors and an odd packed
-gate/up row count are refused before any launch."""
+bare pointers): short or long scale and bias vectors, an odd packed gate/up
+row count and an output of the wrong shape are refused before any launch."""
 import pytest
 import torch
 
@@ -58,5 +58,27 @@ def test_gateup_rows_even_and_lengths(fn):
         f(qx, sx, qw[:-1], sw[:-1])
     with pytest.raises(ValueError, match="sw"):
         f(qx, sx, qw, sw[:128])
+    torch.cuda.synchronize()
+    assert clef.poll_status() == 0
+
+
+def test_output_shape():
+    M, N, K = 64, 128, 256
+    qx, qw = _codes(M, N, K)
+    sx = torch.ones(M, device="cuda")
+    sw = torch.ones(N, device="cuda")
+    wide = torch.zeros((M, N + 8), dtype=torch.bfloat16, device="cuda")
+    clef.w8a8_linear(qx, sx, qw, sw, y=wide[:, :N])          # a window of the right shape passes
+    for bad in (wide[:, :N - 8], wide[:M - 1, :N], wide):
+        with pytest.raises(ValueError, match="shape"):
+            clef.w8a8_linear(qx, sx, qw, sw, y=bad)
+    with pytest.raises(ValueError, match="shape"):
+        clef.w8a8_gateup_swiglu(qx, sx, qw, sw, h=wide[:, :N])   # h has N / 2 columns
+    t = torch.zeros((M, 64), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((N, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError, match="shape"):
+        clef.w8a8_linear_lora(qx, sx, qw, sw, None, t, B, y=wide[:, :N - 8])
+    with pytest.raises(ValueError, match="shape"):
+        clef.w8a8_gemm_s32(qx, qw, acc=torch.zeros((M, N - 8), dtype=torch.int32, device="cuda"))
     torch.cuda.synchronize()
     assert clef.poll_status() == 0

@@ -171,10 +171,17 @@ def _w8a8(name, codes, qx, sx, qw, sw, bias, out, n_out, stream):
     if out is None:
         out = torch.empty((M, n_out), dtype=torch.bfloat16, device=qx.device)
     _cuda(out, "out", (torch.bfloat16,))
+    _out_shape(out, M, n_out)
     ldo = _rows(out, "out")
     _call(name, _ptr(qx), _ptr(sx), _ptr(qw), _ptr(sw), _ptr(bias), M, n_out, K, _ptr(out), ldo,
           _stream(qx, stream))
     return out
+
+
+def _out_shape(out, M, n_out):
+    # the kernels write M rows of n_out columns at the output's pitch
+    if tuple(out.shape) != (M, n_out):
+        raise ValueError(f"output has shape {tuple(out.shape)}, expected ({M}, {n_out})")
 
 
 def _w8a8_checks(codes, qx, sx, qw, sw, bias):
@@ -283,6 +290,7 @@ def _w8a8_lora(name, qx, sx, qw, sw, bias, out, n_out, stream, lora_args):
     if out is None:
         out = torch.empty((M, n_out), dtype=torch.bfloat16, device=qx.device)
     _cuda(out, "out", (torch.bfloat16,))
+    _out_shape(out, M, n_out)
     ldo = _rows(out, "out")
     L = library()
     fn = getattr(L, name)
@@ -299,9 +307,12 @@ def w8a8_gemm_s32(qx, qw, acc=None, stream=None):
     _dense(qx, "qx"); _dense(qw, "qw")
     M, K = qx.shape
     N = qw.shape[0]
+    if qw.shape[1] != K:
+        raise ValueError("qx and qw disagree on K")
     if acc is None:
         acc = torch.empty((M, N), dtype=torch.int32, device=qx.device)
     _cuda(acc, "acc", (torch.int32,))
+    _out_shape(acc, M, N)
     _call("clef_w8a8_gemm_s32", _ptr(qx), _ptr(qw), M, N, K, _ptr(acc), _rows(acc, "acc"),
           _stream(qx, stream))
     return acc
