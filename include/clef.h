@@ -430,6 +430,37 @@ void clef_set_quant_staging(int mode);
  */
 void clef_set_pdl(int on);
 
+/*
+ * clef_set_sm_budget -- how many SMs the library's compute launches issued
+ * afterwards may fill (GEMMs, LoRA launches, quantizers): sms, rounded down
+ * to an even count, or every SM of the device for sms == 0 or sms at least
+ * the device's count.  Results are the same bytes under any budget (the
+ * tile order and every split follow the shapes, not the SM count; only the
+ * number of persistent CTAs changes).  A persistent GEMM CTA takes a whole
+ * SM, so work on another stream (clef_copy_sm streaming the next step's
+ * inputs) gets SMs only if the budget leaves some free.  Process-wide, like
+ * clef_set_pdl.  Returns CLEF_ERR_INVALID_ARG (budget unchanged) for a
+ * negative sms or sms == 1.
+ */
+int clef_set_sm_budget(int sms);
+
+/*
+ * clef_copy_sm -- copy bytes bytes from src to dst with loads and stores
+ * issued by ctas CTAs (one per SM; clusters of two where ctas is even)
+ * instead of a copy engine.  src and dst are any addresses the device can
+ * access: device memory, or page-locked host memory (cudaHostAlloc or
+ * cudaHostRegister), whose host address is valid on the device under
+ * unified addressing.  Copy-engine transfers from page-locked host memory
+ * were measured to stall for 20-180 ms about every half second on this GPU;
+ * SM loads over the same link ran at the same rate without stalls.  With a
+ * budget (clef_set_sm_budget) of the device's SMs less ctas, the copy runs
+ * beside the compute launches of another stream.
+ * Requirements: dst and src 16-byte aligned, bytes >= 0 and a multiple of
+ * 16, 1 <= ctas <= 64, the two ranges disjoint.  Ordered on stream like any
+ * kernel; bytes == 0 returns CLEF_OK without a launch.
+ */
+int clef_copy_sm(void *dst, const void *src, int64_t bytes, int ctas, void *stream);
+
 /* Human-readable name of a status code (static string). */
 const char *clef_status_string(int status);
 

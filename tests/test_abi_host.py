@@ -178,3 +178,29 @@ def test_mma_peak_rejects_bad_arguments(kind, iters, out):
     d = C.c_double(0.0)
     ptr = C.c_void_p(C.addressof(d)) if out else NUL
     assert clef.library().clef_mma_peak(kind, iters, ptr) == 1
+
+
+@pytest.mark.parametrize("args", [
+    (NUL, FAKE, 64, 4, S),            # null dst
+    (FAKE, NUL, 64, 4, S),            # null src
+    (ODD, C.c_void_p(0x20000), 64, 4, S),   # misaligned dst
+    (FAKE, C.c_void_p(0x20000), 40, 4, S),  # bytes not a multiple of 16
+    (FAKE, C.c_void_p(0x20000), -16, 4, S),  # negative
+    (FAKE, C.c_void_p(0x20000), 64, 0, S),   # no CTA
+    (FAKE, C.c_void_p(0x20000), 64, 65, S),  # too many CTAs
+    (FAKE, C.c_void_p(0x10010), 64, 4, S),   # overlapping ranges
+])
+def test_copy_sm_rejects_bad_arguments(args):
+    assert clef.library().clef_copy_sm(*args) == 1
+
+
+def test_copy_sm_empty_is_ok_without_launch():
+    assert clef.library().clef_copy_sm(NUL, NUL, 0, 4, S) == 0
+
+
+def test_sm_budget_arguments():
+    L = clef.library()
+    assert L.clef_set_sm_budget(-1) == 1
+    assert L.clef_set_sm_budget(1) == 1
+    assert L.clef_set_sm_budget(148) == 0
+    assert L.clef_set_sm_budget(0) == 0

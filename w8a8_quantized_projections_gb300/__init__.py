@@ -78,6 +78,8 @@ def library():
                 "clef_w8a8_gateup_swiglu_lora": [vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp, vp, i64, vp,
                                                  i64, vp],
                 "clef_mma_peak": [i32, i64, vp],
+                "clef_set_sm_budget": [i32],
+                "clef_copy_sm": [vp, vp, i64, i32, vp],
                 "clef_poll_status": [],
                 "clef_abi_version": [],
             }
@@ -496,6 +498,34 @@ def set_pdl(on: bool) -> None:
     L.clef_set_pdl.argtypes = [C.c_int]
     L.clef_set_pdl.restype = None
     L.clef_set_pdl(1 if on else 0)
+
+
+def set_sm_budget(sms: int) -> None:
+    """SMs the library's later compute launches may fill (0: all of them;
+    rounded down to an even count).  The bytes computed do not depend on it;
+    SMs outside the budget stay free for work on other streams, such as
+    copy_sm moving the next step's inputs."""
+    _call("clef_set_sm_budget", int(sms))
+
+
+def copy_sm(dst: torch.Tensor, src: torch.Tensor, ctas: int = 4, stream=None) -> torch.Tensor:
+    """Copy src into dst (same byte count, both contiguous) with loads and
+    stores issued by `ctas` CTAs instead of a copy engine.  Each side is a
+    CUDA tensor or a page-locked CPU tensor.  Returns dst."""
+    for t, n in ((dst, "dst"), (src, "src")):
+        if not isinstance(t, torch.Tensor):
+            raise ValueError(f"{n} must be a tensor")
+        _dense(t, n)
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{n} must be a CUDA tensor or a page-locked CPU tensor")
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError("dst and src differ in size")
+    dev = dst if dst.is_cuda else src
+    if not dev.is_cuda:
+        raise ValueError("one side must be a CUDA tensor (its device runs the copy)")
+    _call("clef_copy_sm", _ptr(dst), _ptr(src), nbytes, int(ctas), _stream(dev, stream))
+    return dst
 
 
 def test_force_timeout(on) -> None:

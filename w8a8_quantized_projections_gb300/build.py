@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libclef.so")
 ROOT = os.path.dirname(HERE)
-SOURCES = ["abi.cu", "quant_act.cu", "gemm.cu", "swiglu.cu", "lora_noalloc.cu", "mma_peak.cu"]
+SOURCES = ["abi.cu", "quant_act.cu", "gemm.cu", "swiglu.cu", "lora_noalloc.cu", "mma_peak.cu", "copy_sm.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 

@@ -47,6 +47,7 @@ std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
 std::atomic<int> g_force_timeout{0};
 std::atomic<int> g_quant_staging{1};
 std::atomic<int> g_pdl{1};
+std::atomic<int> g_sm_budget{0};   // SMs the compute launches may fill (0: all)
 thread_local char g_last_err[256] = "";
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -133,6 +134,13 @@ int make_tmap(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t
     return CLEF_OK;
 }
 
+// SMs a compute launch may fill: the device's, or the caller's budget
+// (clef_set_sm_budget) where that is fewer.
+int launch_sms(const DeviceState *d) {
+    const int b = g_sm_budget.load();
+    return (b > 0 && b < d->num_sms) ? b : d->num_sms;
+}
+
 GemmArgs base_args(const DeviceState *d, int64_t M, int64_t N, int64_t K) {
     GemmArgs a;
     memset(&a, 0, sizeof a);
@@ -158,9 +166,9 @@ int lora_shrink_launch(DeviceState *d, const void *x, int64_t ldx, const void *A
     a1.out = t;
     a1.ldo = ldt;
     a1.n_fastest = 1;
-    return launch_gemm(kOpBF16, kEpiStoreBF16, lora_shrink_width(M, r_pad, d->num_sms, 0),
+    return launch_gemm(kOpBF16, kEpiStoreBF16, lora_shrink_width(M, r_pad, launch_sms(d), 0),
                        Operand{x, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2},
-                       Operand{A, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2}, a1, d->num_sms, st);
+                       Operand{A, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2}, a1, launch_sms(d), st);
 }
 
 // LoRA stage 2 (arguments already checked): y = bf16(y + t B^T) over K =
@@ -176,7 +184,7 @@ int lora_expand_launch(DeviceState *d, const void *t, int64_t ldt, const void *B
     // the same rows of y (q adapter at 24,032 tokens: 96.5 -> 93.1 us)
     a2.n_fastest = 1;
     return launch_gemm(kOpBF16, kEpiAddBF16, 128, Operand{t, (uint64_t)r_pad, (uint64_t)M, (uint64_t)ldt * 2},
-                       Operand{B, (uint64_t)r, (uint64_t)N, (uint64_t)r * 2}, a2, d->num_sms, st);
+                       Operand{B, (uint64_t)r, (uint64_t)N, (uint64_t)r * 2}, a2, launch_sms(d), st);
 }
 
 // Shared checks of the W8A8 GEMM entry points.  b_rows is the row count of
@@ -232,7 +240,7 @@ int run_w8a8(int op, int epi, const void *qx, const float *sx, const void *qw, c
                 break;
             }
     }
-    return launch_gemm(op, epi, 256, A, B, a, d->num_sms, static_cast<cudaStream_t>(stream));
+    return launch_gemm(op, epi, 256, A, B, a, launch_sms(d), static_cast<cudaStream_t>(stream));
 }
 
 // The INT8 linear or gate/up SwiGLU with the LoRA expand fused (checks,
@@ -298,7 +306,7 @@ int run_w8a8_lora(bool gateup, const void *qx, const float *sx, const void *qw, 
     a.lora_nkb = (int)((gateup ? 2 : 1) * r_pad / 64);
     const Operand A = {qx, (uint64_t)K, (uint64_t)M, (uint64_t)K};
     const Operand W = {qw, (uint64_t)K, (gateup ? 2 : 1) * (uint64_t)N, (uint64_t)K};
-    return launch_gemm(kOpI8, gateup ? kEpiSwiGLULora : kEpiScaleBiasLora, 256, A, W, a, d->num_sms,
+    return launch_gemm(kOpI8, gateup ? kEpiSwiGLULora : kEpiScaleBiasLora, 256, A, W, a, launch_sms(d),
                        static_cast<cudaStream_t>(stream));
 }
 
@@ -387,7 +395,7 @@ int quant_common(const void *x, int64_t M, int64_t K, int64_t ldx, int mode, voi
     int rc = device_state(&d);
     if (rc) return rc;
     QuantEnv env;
-    env.num_sms = d->num_sms;
+    env.num_sms = launch_sms(d);
     env.status = d->status;
     env.wait_limit_ns = g_wait_limit_ns.load();
     env.staging = g_quant_staging.load();
@@ -542,9 +550,9 @@ int clef_lora_gateup_swiglu(const void *x, int64_t ldx, const void *A_gate, cons
         a1.n_fastest = 1;
         a1.b2_row0 = (int)r_pad;
         const Operand Au{A_up, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2};
-        rc = launch_gemm(kOpBF16, kEpiStoreBF16, lora_shrink_width(M, 2 * r_pad, d->num_sms, r_pad),
+        rc = launch_gemm(kOpBF16, kEpiStoreBF16, lora_shrink_width(M, 2 * r_pad, launch_sms(d), r_pad),
                          Operand{x, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2},
-                         Operand{A_gate, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2}, a1, d->num_sms, st, &Au);
+                         Operand{A_gate, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2}, a1, launch_sms(d), st, &Au);
         if (rc) return rc;
     }
     // stage 2: one GEMM over K = 2 r_pad; gate rows see B_gate in the first
@@ -562,7 +570,7 @@ int clef_lora_gateup_swiglu(const void *x, int64_t ldx, const void *A_gate, cons
     const Operand Bu{B_up, (uint64_t)r, (uint64_t)N, (uint64_t)r * 2};
     return launch_gemm(kOpBF16, kEpiLoraSwiGLU, 256,
                        Operand{t_scratch, (uint64_t)(2 * r_pad), (uint64_t)M, (uint64_t)(2 * r_pad) * 2},
-                       Operand{B_gate, (uint64_t)r, (uint64_t)N, (uint64_t)r * 2}, a2, d->num_sms, st, &Bu);
+                       Operand{B_gate, (uint64_t)r, (uint64_t)N, (uint64_t)r * 2}, a2, launch_sms(d), st, &Bu);
 }
 
 int clef_swiglu_bf16(const void *y_gu, int64_t M, int64_t N, int64_t ldg, void *h, int64_t ldh,
@@ -629,6 +637,12 @@ void clef_test_force_timeout(int on) { g_force_timeout.store(on < 0 ? 0 : on); }
 void clef_set_quant_staging(int mode) { g_quant_staging.store(mode < 0 ? 0 : (mode > 2 ? 2 : mode)); }
 
 void clef_set_pdl(int on) { g_pdl.store(on ? 1 : 0); }
+
+int clef_set_sm_budget(int sms) {
+    if (sms < 0 || sms == 1) return arg_fail("sms must be 0 (all) or at least 2");
+    g_sm_budget.store(sms & ~1);
+    return CLEF_OK;
+}
 
 const char *clef_status_string(int status) {
     switch (status) {

@@ -1883,12 +1883,18 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
             cfg.stream = st;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+            // on the whole device, whatever SM budget the first call had
+            int dev = 0, all_sms = num_sms;
+            if (cudaGetDevice(&dev) == cudaSuccess)
+                cudaDeviceGetAttribute(&all_sms, cudaDevAttrMultiProcessorCount, dev);
+            cfg.gridDim = dim3(2 * (all_sms / 2), 1, 1);
             int n = 0;
             e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-            max_pairs = (e == cudaSuccess && n > 0) ? n : num_sms / 2;
+            max_pairs = (e == cudaSuccess && n > 0) ? n : all_sms / 2;
         }
-        int pairs = tiles < max_pairs ? tiles : max_pairs;
+        // the pairs this launch may use: the SM budget leaves the rest free
+        const int cap = std::min(max_pairs, num_sms / 2);
+        int pairs = tiles < cap ? tiles : cap;
         GemmArgs la = args;
         la.out_v32 = out_rows_v32(args);
         la.sk = 0;
@@ -1901,14 +1907,14 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
             // own accumulator chunks, cut by K alone) on kKParts pairs, so the
             // last wave takes a part's time: pair p < kKParts R runs part
             // p % kKParts of tail tile p / kKParts.
-            const int tail0 = (tiles / max_pairs) * max_pairs;
+            const int tail0 = (tiles / cap) * cap;
             const int rest = tiles - tail0;
             if (nkb_k >= C::kKSplitMinKBlocks && nkb_k % C::kKParts == 0 && rest > 0 &&
-                C::kKParts * rest <= max_pairs && tiles <= kSkMaxTiles &&
-                args.sk_ws_bytes >= (int64_t)max_pairs * kSkBytesPerPair) {
+                C::kKParts * rest <= cap && tiles <= kSkMaxTiles &&
+                args.sk_ws_bytes >= (int64_t)cap * kSkBytesPerPair) {
                 la.sk = C::kKParts * rest;
                 la.sk_tail0 = tail0;
-                pairs = tail0 > 0 ? max_pairs : la.sk;
+                pairs = tail0 > 0 ? cap : la.sk;
             }
         } else if (C::kStreamK && args.sk_ws && args.sk_cnt) {
             // Stream-K where the last wave of whole tiles would leave more
@@ -1924,23 +1930,23 @@ int launch_one(const Operand &A, const Operand &B, const GemmArgs &args, int num
             // pairs busy (200 x 2048 x 8192, 8 tiles: 59.4 -> 45.2 us; 130 x
             // 1024 x 4096, 4 tiles: 39.4 -> 35.1 us).
             const int nkb = (args.K + 63) / 64;
-            const int64_t waves = (tiles + max_pairs - 1) / max_pairs;
-            const double fill = (double)tiles / (double)(waves * max_pairs);
-            const int tail0 = tiles >= max_pairs ? (tiles / max_pairs) * max_pairs : 0;
+            const int64_t waves = (tiles + cap - 1) / cap;
+            const double fill = (double)tiles / (double)(waves * cap);
+            const int tail0 = tiles >= cap ? (tiles / cap) * cap : 0;
             const int64_t rest = (int64_t)(tiles - tail0) * nkb;
             // runs of at least 16 k-blocks, or 8 when a launch of under an
             // eighth of a wave is split (small M, long K)
             const int minrun = tail0 > 0 ? C::kChunkKBlocks : 8;
-            const int p2 = (int)std::min<int64_t>(max_pairs, rest / minrun);
+            const int p2 = (int)std::min<int64_t>(cap, rest / minrun);
             // (the device splits runs with 32-bit products of a slot index and
             // the remaining k-block count)
-            const bool fits32 = rest * (int64_t)max_pairs < ((int64_t)1 << 32);
-            if (fill < 0.92 && (tail0 > 0 || 8 * tiles <= max_pairs) && p2 > tiles - tail0 &&
+            const bool fits32 = rest * (int64_t)cap < ((int64_t)1 << 32);
+            if (fill < 0.92 && (tail0 > 0 || 8 * tiles <= cap) && p2 > tiles - tail0 &&
                 tiles <= kSkMaxTiles && fits32 &&
-                args.sk_ws_bytes >= (int64_t)max_pairs * kSkBytesPerPair) {
+                args.sk_ws_bytes >= (int64_t)cap * kSkBytesPerPair) {
                 la.sk = p2;
                 la.sk_tail0 = tail0;
-                pairs = tail0 > 0 ? max_pairs : p2;
+                pairs = tail0 > 0 ? cap : p2;
             }
         }
         e = launch_kernel(kern, dim3(2 * pairs), dim3(C::kThreads), C::kSmemBytes, st, 2,
