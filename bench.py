@@ -679,7 +679,7 @@ def e2e(args, layer, acts, acts_np, cfg, dev, stream, world, torch):
     ctas = E2E_COPY_CTAS
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
-    def h2d(dst, src):
+    def move(dst, src):
         clef.copy_sm(dst, src, ctas, stream=copy)
 
     def run(n):
@@ -688,7 +688,7 @@ def e2e(args, layer, acts, acts_np, cfg, dev, stream, world, torch):
         read_back = None             # the previous step's output has been read
         with torch.cuda.stream(copy):
             for k in dev_in[0]:
-                h2d(dev_in[0][k], host_in[k])
+                move(dev_in[0][k], host_in[k])
             in_ready[0].record(copy)
         for i in range(n):
             b = i % 2
@@ -697,7 +697,7 @@ def e2e(args, layer, acts, acts_np, cfg, dev, stream, world, torch):
                     if used[1 - b] is not None:
                         copy.wait_event(used[1 - b])
                     for k in dev_in[1 - b]:
-                        h2d(dev_in[1 - b][k], host_in[k])
+                        move(dev_in[1 - b][k], host_in[k])
                     in_ready[1 - b].record(copy)
             stream.wait_event(in_ready[b])
             layer.step(dev_in[b], final_wait=read_back)
@@ -706,7 +706,7 @@ def e2e(args, layer, acts, acts_np, cfg, dev, stream, world, torch):
             used[b] = done
             with torch.cuda.stream(copy):
                 copy.wait_event(done)
-                h2d(host_out, out_dev)
+                move(host_out, out_dev)
                 read_back = ev()
                 read_back.record(copy)
         stream.wait_event(read_back)
