@@ -84,7 +84,9 @@ struct Cfg {
     // lookahead and four fp16 stages absorb the converters' per-k-block
     // latency (measured against 3 + 8 and 5 + 4: 1502 x 34816 x 5120 in 414
     // against 432 and 426 us).
-    static constexpr int NRAW = kI8 ? (PAIR ? 6 : 5) : 0;
+    // Single CTAs: 4 raw stages, a multiple of their 2 converter groups (see
+    // kConvGroups: 5 let a group's raw-stage waits skip a phase).
+    static constexpr int NRAW = kI8 ? (PAIR ? 6 : 4) : 0;
     // Epilogue warps: 16 for the FP8 SwiGLU epilogue (exp and an IEEE
     // division per output must keep pace with a k-loop less than half as long
     // as INT8's: 120 -> 102 us on 1502 x 24576 x 4096), 8 otherwise (the
@@ -154,10 +156,19 @@ struct Cfg {
     // widens k-blocks g, g + kConvGroups, ... of the CTA's k-block sequence, so
     // a warp pays its per-k-block waits, fence and arrives once every
     // kConvGroups k-blocks (1, 2, 3 groups: 1502 x 34816 x 5120 in 399, 381,
-    // 359 us).  A group's successive k-blocks may lie no more than NSTAGE
-    // apart: each of its waits on a stage barrier then targets the phase just
-    // after one it has seen complete, never two ahead (the parity test of an
-    // mbarrier wait cannot tell those apart).
+    // 359 us).  Each of a group's waits on a stage barrier must target the
+    // phase just after one it already knows complete, never two ahead (the
+    // parity test of an mbarrier wait cannot tell those apart):
+    // - fp16 stages: the group's successive k-blocks lie at most NSTAGE
+    //   apart.  Their "empty" phases complete in k-block order (the MMAs
+    //   release the stages in order), so the wait for a k-block's stage
+    //   follows the release its previous k-block waited for, which is at
+    //   least the stage's preceding phase;
+    // - raw stages: NRAW a multiple of kConvGroups.  Their "full" phases
+    //   complete when copies land, in no guaranteed order, so the stage's
+    //   preceding phase must be one of the group's own k-blocks (with 5
+    //   stages and 2 groups a group's next use of a stage came two phases
+    //   after its last one).
     static constexpr int kConvGroups = PAIR ? 3 : 2;   // single CTAs have 2 fp16 stages
     static constexpr int kGroupWarps = kConvWarps / kConvGroups;
     static constexpr int kFullArrivals = kI8 ? kGroupWarps : 1;
@@ -168,7 +179,7 @@ struct Cfg {
     static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
     static_assert(kSmemBytes <= 232448, "shared memory");
     static_assert(NSTAGE >= 2, "pipeline depth");
-    static_assert(!kI8 || (kConvWarps % kConvGroups == 0 && kConvGroups <= NSTAGE && kConvGroups <= NRAW),
+    static_assert(!kI8 || (kConvWarps % kConvGroups == 0 && kConvGroups <= NSTAGE && NRAW % kConvGroups == 0),
                   "converter groups");
     // stream-K counters and pieces are laid out for eight epilogue warps of
     // 128 int32 columns each
