@@ -439,8 +439,10 @@ void clef_set_pdl(int on);
  * number of persistent CTAs changes).  A persistent GEMM CTA takes a whole
  * SM, so work on another stream (clef_copy_sm streaming the next step's
  * inputs) gets SMs only if the budget leaves some free.  Process-wide, like
- * clef_set_pdl.  Returns CLEF_ERR_INVALID_ARG (budget unchanged) for a
- * negative sms or sms == 1.
+ * clef_set_pdl; launches captured into a CUDA graph keep the budget that was
+ * in force when they were captured.  Stream-K tails (clef_bind_workspace)
+ * are dealt over the CTA pairs the budget allows.  Returns
+ * CLEF_ERR_INVALID_ARG (budget unchanged) for a negative sms or sms == 1.
  */
 int clef_set_sm_budget(int sms);
 
