@@ -235,7 +235,12 @@ int clef_w8a8_gateup_swiglu_lora(const int8_t *qx, const float *sx, const int8_t
  * exactly clef_lora_shrink into t_scratch (ldt = r_pad) followed by
  * clef_lora_expand_add from it.
  * clef_lora_shrink: t[m][j] = bf16(sum_k x[m][k] * A[j][k]) for j < r_pad
- *   (rows j >= r of A read as zeros, so those columns of t are 0).
+ *   (rows j >= r of A read as zeros, so those columns of t are 0).  The fp32
+ *   sum runs in the tensor core's order; for K >= 6144 it is taken as four
+ *   fixed parts of ceil(K / 256) x 64 elements (the last the rest), added in
+ *   K order, whatever M is, so a row's bits never depend on the call's row
+ *   count.  With a workspace bound to the stream (clef_bind_workspace), the
+ *   parts of a partly empty last wave of tiles run on several SMs.
  *   x: bf16 [M][K], pitch ldx; A: bf16 [r][K] dense; t: bf16 [M][r_pad],
  *   pitch ldt (only columns 0 .. r_pad - 1 written).
  * clef_lora_expand_add: y[m][n] = bf16((float)y[m][n] + sum_{j<r} t[m][j] * B[n][j])
@@ -339,7 +344,9 @@ int clef_lora_add_noalloc(const void *x, int64_t ldx, const void *A, const void 
  * with K >= 8192 sums every tile's K as three fixed parts whatever M is (see
  * there); with a workspace bound, the tiles of a last wave that fits three
  * times in the pairs run as their parts on three pairs each, the same bytes
- * as unsplit.  Other FP8 calls never split.
+ * as unsplit.  Other FP8 calls never split.  The LoRA x A^T of
+ * clef_lora_shrink, clef_lora_add and clef_lora_gateup_swiglu does the same
+ * with four parts for K >= 6144 (see clef_lora_shrink).
  * clef_gemm_workspace_bytes: the size needed on the current device (about
  * 38 MB on a 152-SM GB300), written to *bytes.
  * clef_bind_workspace: binds a caller-owned device buffer of that size to

@@ -203,3 +203,42 @@ def test_fp8_halves_split_equals_unsplit_and_rows(orc, M, N, K):
     qwh, swh = par_rows(lambda a, c: orc.quant_fp8(w[a:c]), N)
     ref = orc.fp8_linear(qxr, sxr, qwh, swh, b)
     assert_rms_close(full[rows].view(np.uint16), ref, 1e-2, "fp8_linear halves")
+
+
+# LoRA x A^T with K >= 6144: every tile sums its K as four fixed parts, in
+# CTA-pair and single-CTA tiles alike; with a workspace bound, a last wave that
+# fits four times in the pairs runs as parts on four pairs each (1,502 x 17408
+# -> 256: 6 tiles under one wave, split into 24 parts; 19,712 x 6144 -> 256:
+# 77 tiles, one whole wave and one tile in parts; 300 x 8192 -> 64: 64-wide
+# single-CTA tiles).  The bytes equal the unsplit launch's, a call's rows equal
+# the same rows called alone (100 rows: single CTAs), and sampled rows meet the
+# oracle within the fp32 accumulation bound.
+@pytest.mark.parametrize("M,K,r", [(1502, 17408, 256), (19712, 6144, 256), (300, 8192, 64)])
+def test_lora_shrink_parts_split_equals_unsplit_and_rows(orc, M, K, r):
+    import clef_synth as S
+    from gpu_util import bf16_dev, bf16_ulp
+    from test_gpu_parity import lora_bound
+    x = S.activation(0, f"t/lsp/{M}x{K}/x", M, K)
+    A, _ = S.lora_pair(0, f"t/lsp/{M}x{K}", r, K, 8)
+    xd, Ad = bf16_dev(x), bf16_dev(A)
+    plain = clef.lora_shrink(xd, Ad)
+    ws = bound_workspace()
+    try:
+        for _ in range(3):
+            split = clef.lora_shrink(xd, Ad)
+            assert torch.equal(split.view(torch.int16), plain.view(torch.int16))
+        torch.cuda.synchronize()
+        assert int(ws[:COUNTER_BYTES].count_nonzero()) == 0
+    finally:
+        clef.bind_workspace(None)
+    full = host(plain.view(torch.int16))
+    for a in (0, M // 2, M - 100):
+        part = clef.lora_shrink(xd[a:a + 100].contiguous(), Ad)
+        assert np.array_equal(host(part.view(torch.int16)), full[a:a + 100]), a
+    rows = np.unique(np.r_[0:2, M // 2, M - 2:M])
+    t_ref = orc.lora_t(x[rows], A)
+    t = full[rows].view(np.uint16)[:, :r]
+    tol = bf16_ulp(S.bf16_bits_to_f64(t_ref[:, :r])) + 2 * lora_bound(x[rows], A, K)
+    d = np.abs(S.bf16_bits_to_f64(t) - S.bf16_bits_to_f64(t_ref[:, :r]))
+    assert np.all(d <= tol), f"t: worst excess {(d - tol).max():.3g}"
+    assert np.all(full[:, r:clef.lora_pad(r)] == 0), "padding columns of t must be exact zeros"

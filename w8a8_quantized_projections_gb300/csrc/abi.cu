@@ -141,6 +141,20 @@ int launch_sms(const DeviceState *d) {
     return (b > 0 && b < d->num_sms) ? b : d->num_sms;
 }
 
+// The workspace bound to this device and stream, if any, which lets a launch
+// split tiles across CTA pairs (INT8 stream-K, the K parts of the FP8 linear
+// and of the LoRA x A^T).
+void attach_workspace(GemmArgs &a, const DeviceState *d, const void *stream) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (size_t i = 0; i < g_ws_count; ++i)
+        if (g_ws[i].dev == d->index && g_ws[i].stream == stream) {
+            a.sk_cnt = static_cast<int *>(g_ws[i].ptr);
+            a.sk_ws = reinterpret_cast<int4 *>(static_cast<char *>(g_ws[i].ptr) + kSkCounterBytes);
+            a.sk_ws_bytes = g_ws[i].bytes - kSkCounterBytes;
+            return;
+        }
+}
+
 GemmArgs base_args(const DeviceState *d, int64_t M, int64_t N, int64_t K) {
     GemmArgs a;
     memset(&a, 0, sizeof a);
@@ -166,6 +180,7 @@ int lora_shrink_launch(DeviceState *d, const void *x, int64_t ldx, const void *A
     a1.out = t;
     a1.ldo = ldt;
     a1.n_fastest = 1;
+    attach_workspace(a1, d, st);
     return launch_gemm(kOpBF16, kEpiStoreBF16, lora_shrink_width(M, r_pad, launch_sms(d), 0),
                        Operand{x, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2},
                        Operand{A, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2}, a1, launch_sms(d), st);
@@ -229,17 +244,7 @@ int run_w8a8(int op, int epi, const void *qx, const float *sx, const void *qw, c
     a.bias = static_cast<const uint16_t *>(bias);
     a.out = out;
     a.ldo = ldo;
-    if (op == kOpI8 || (op == kOpF8 && epi == kEpiScaleBias)) {
-        // a workspace bound to this stream lets tiles be split across SMs
-        std::lock_guard<std::mutex> lk(g_mu);
-        for (size_t i = 0; i < g_ws_count; ++i)
-            if (g_ws[i].dev == d->index && g_ws[i].stream == stream) {
-                a.sk_cnt = static_cast<int *>(g_ws[i].ptr);
-                a.sk_ws = reinterpret_cast<int4 *>(static_cast<char *>(g_ws[i].ptr) + kSkCounterBytes);
-                a.sk_ws_bytes = g_ws[i].bytes - kSkCounterBytes;
-                break;
-            }
-    }
+    if (op == kOpI8 || (op == kOpF8 && epi == kEpiScaleBias)) attach_workspace(a, d, stream);
     return launch_gemm(op, epi, 256, A, B, a, launch_sms(d), static_cast<cudaStream_t>(stream));
 }
 
@@ -549,6 +554,7 @@ int clef_lora_gateup_swiglu(const void *x, int64_t ldx, const void *A_gate, cons
         a1.ldo = 2 * r_pad;
         a1.n_fastest = 1;
         a1.b2_row0 = (int)r_pad;
+        attach_workspace(a1, d, st);
         const Operand Au{A_up, (uint64_t)K, (uint64_t)r, (uint64_t)K * 2};
         rc = launch_gemm(kOpBF16, kEpiStoreBF16, lora_shrink_width(M, 2 * r_pad, launch_sms(d), r_pad),
                          Operand{x, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2},

@@ -145,9 +145,18 @@ struct Cfg {
     // order whether a tile runs whole or its parts run on several CTA pairs
     // (stream-K over a partly empty last wave, the parts meeting in the
     // workspace), so a row's bits do not depend on M.
-    static constexpr bool kKSplit = (OP == kOpF8 && EPI == kEpiScaleBias);
-    static constexpr int kKSplitMinKBlocks = 64;
-    static constexpr int kKParts = 3;
+    //
+    // LoRA x A^T (bf16 store): the same with 4 parts from 96 k-blocks (K =
+    // 6,144) on, for the adapters of the 24,032-token layer's o (K = 6,144)
+    // and down (K = 17,408) projections, whose 94 row blocks leave a second
+    // wave of 18 tiles on 76 pairs: 4 parts divide both k-block counts (96,
+    // 272), and 18 x 4 pieces fit in one wave.  Single-CTA tiles (calls of
+    // at most 128 rows, narrow ranks) sum the same parts, so a row's bits do
+    // not depend on the call's row count.
+    static constexpr bool kKSplit =
+        (OP == kOpF8 && EPI == kEpiScaleBias) || (OP == kOpBF16 && EPI == kEpiStoreBF16);
+    static constexpr int kKSplitMinKBlocks = (OP == kOpF8) ? 64 : 96;
+    static constexpr int kKParts = (OP == kOpF8) ? 3 : 4;
     static constexpr bool kStreamK = PAIR && ((kI8 && !kSwiGLU && !kLoraFused) || kKSplit);
     static constexpr int kOutColsPerTile = kSwiGLU ? BN / 2 : BN;
     // full[s]: TMA (native) or the local converter warps (INT8); in pair mode
@@ -1590,7 +1599,11 @@ struct Gemm {
                     release_acc(c, acc, lane);
                     if (++acc == (uint32_t)C::kAccBufs) { acc = 0; aph ^= 1u; }
                 }
-                if (sg.part < 0 || sk_combine(c, a, sg, e, lane, v)) finish_row(a, row, row_ok, nb, half, v);
+                bool whole = sg.part < 0;   // always, where tiles are never split
+                if constexpr (C::kStreamK) {
+                    if (!whole) whole = sk_combine(c, a, sg, e, lane, v);
+                }
+                if (whole) finish_row(a, row, row_ok, nb, half, v);
             } else {
                 if (!wait_pair(&c.bar->acc_full[acc], aph, c, kSiteEpiAccFull)) return;
                 tc_fence_after();
@@ -1722,15 +1735,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     // warps, 4 x 32 x 56 + 16 x 32 x 104 = 60,416 of 61,440 (removes the
     // epilogue's spill; the 1502 x 24576 x 4096 call 104.0 -> 102.4 us)
     constexpr bool kF8Split = OP == kOpF8 && C::kEpiWarps == 16 && C::kEpiWarp0 == 4;
-    // FP8 linear (8 epilogue warps; 12 launched at 168 registers), whose
-    // epilogue holds a tile row's running sum of the K parts while it reads
-    // the next part: 4 x 32 x 56 + 8 x 32 x 224 = 64,512 of 64,512
-    constexpr bool kF8LinSplit = C::kKSplit && C::kEpiWarps == 8 && C::kEpiWarp0 == 4;
+    // FP8 linear and LoRA x A^T (8 epilogue warps; 12 launched at 168
+    // registers), whose epilogue holds a tile row's running sum of the K parts
+    // while it reads the next part: FP8 4 x 32 x 56 + 8 x 32 x 224 = 64,512
+    // of 64,512; bf16 4 x 32 x 80 + 8 x 32 x 208 = 63,488 (its TMA producer,
+    // which also serves stacked B factors, spilled at 56 and 64)
+    constexpr bool kKSplitRegs = C::kKSplit && C::kEpiWarps == 8 && C::kEpiWarp0 == 4;
     if (warp < C::kEpiWarp0) {
         // INT8: control and converter warps hand registers to the epilogue
         // warps, which hold the int32 totals
         if (C::kI8) asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
-        if (kF8Split || kF8LinSplit) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+        if (kF8Split || (kKSplitRegs && OP == kOpF8)) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+        if (kKSplitRegs && OP == kOpBF16) asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
         if (warp == 0) {
             if (lane == 0) {
                 G::producer(c, &tmA, &tmB, &tmB2, args, fills);
@@ -1752,7 +1768,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     } else {
         if (C::kI8) asm volatile("setmaxnreg.inc.sync.aligned.u32 192;");
         if (kF8Split) asm volatile("setmaxnreg.inc.sync.aligned.u32 104;");
-        if (kF8LinSplit) asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+        if (kKSplitRegs && OP == kOpF8) asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+        if (kKSplitRegs && OP == kOpBF16) asm volatile("setmaxnreg.inc.sync.aligned.u32 208;");
         G::epilogue(c, args);
     }
     // this thread's role is done: the stream's next kernel may be scheduled
