@@ -95,8 +95,8 @@ struct Cfg {
     // kParts warps share each TMEM lane quadrant, splitting the tile's columns.
     static constexpr int kEpiWarps = (!kI8 && BN_ == 256 && (EPI == kEpiSwiGLU || EPI == kEpiLoraSwiGLU)) ? 16 : 8;
     static constexpr int kParts = kEpiWarps / 4;
-    // Read-modify-write epilogue (y += acc): a 32 x 32 fp32 transpose buffer
-    // per epilogue warp, so that y is read and written in row segments.
+    // LoRA gate/up adds then SwiGLU over base g|u tiles read by TMA (bf16
+    // operands, the unfused LoRA path)
     static constexpr bool kLoraSwi = (EPI == kEpiLoraSwiGLU);
     // y += acc: a ring of kYBufs y tiles (BM x BN bf16) that TMA loads
     // kYBufs - 1 tiles ahead and stores.  128-wide tiles keep 3, which leaves
@@ -1192,12 +1192,6 @@ struct Gemm {
         }
     }
 
-    // y = bf16(float(y) + acc) for the warp's 32 rows (row0 .. row0 + 31, one
-    // per lane in the accumulator): each 32-column chunk goes through the
-    // warp's transpose buffer (row-major, 16-byte unit u of row r at
-    // u ^ (r & 7): conflict-free both ways), after which lane l handles columns
-    // 8 (l & 3) .. + 7 of rows (l >> 2) + 8 i, so every warp access to y covers
-    // 64 contiguous bytes of eight rows instead of 16 bytes of 32 rows.
     // y += acc through TMA.  The CTA's y tile (its BM rows of the tile, BN
     // columns) moves as BN / 64 boxes of 64 columns x BM rows with the 128-byte
     // swizzle: box k of buffer b at epi + b * kYTile + k * BM * 128, row r's
