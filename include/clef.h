@@ -10,8 +10,9 @@
  * kernels on the caller's stream.
  *
  * Conventions shared by every entry point:
- *  - Pointers are DEVICE pointers to memory the caller owns; the library
- *    never allocates, frees or synchronises inside these calls.
+ *  - Pointers are DEVICE pointers to memory the caller owns (clef_copy_sm
+ *    also takes page-locked host memory); the library never allocates, frees
+ *    or synchronises inside these calls.
  *  - Matrices are row-major.  x/activations are [M][K]; weights are [N][K]
  *    (output-channel major, the Linear convention), so the GEMMs contract
  *    both operands along their contiguous K axis.
