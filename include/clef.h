@@ -459,8 +459,9 @@ int clef_set_sm_budget(int sms);
  * issued by ctas CTAs (one per SM; clusters of two where ctas is even)
  * instead of a copy engine.  src and dst are any addresses the device can
  * access: device memory, or page-locked host memory (cudaHostAlloc or
- * cudaHostRegister), whose host address is valid on the device under
- * unified addressing.  Copy-engine transfers from page-locked host memory
+ * cudaHostRegister), read and written through its device mapping.  Pageable
+ * host memory returns CLEF_ERR_INVALID_ARG (nothing launched) unless the
+ * device reads pageable memory directly (cudaDevAttrPageableMemoryAccess).  Copy-engine transfers from page-locked host memory
  * were measured to stall for 20-180 ms about every half second on this GPU;
  * SM loads over the same link ran at the same rate without stalls.  With a
  * budget (clef_set_sm_budget) of the device's SMs less ctas, the copy runs

@@ -9,6 +9,8 @@ every split follow the shapes, only the number of persistent CTAs changes
 (INT8 stream-K pieces, FP8 K parts, the quantizer's two kernels, the fused
 LoRA and a whole layer step).  A copy running on a side stream beside a GEMM
 under a budget that leaves it room must leave both results intact."""
+import ctypes as C
+
 import numpy as np
 import pytest
 import torch
@@ -49,6 +51,25 @@ def test_copy_directions(n, ctas):
     torch.cuda.synchronize()
     assert torch.equal(dev.cpu(), src_h)
     assert torch.equal(back, src_h)
+
+
+def test_copy_from_pageable_host_memory_is_refused_or_correct():
+    """Through the C ABI, pageable host memory (a numpy buffer) is either
+    refused on the host (nothing launched) or, where the device reads
+    pageable memory directly, copied byte for byte."""
+    n = (1 << 20) + 16
+    src = np.random.default_rng(5).integers(-128, 128, n, dtype=np.int8)
+    assert src.ctypes.data % 16 == 0
+    dst = torch.zeros(n, dtype=torch.int8, device="cuda")
+    rc = clef.library().clef_copy_sm(C.c_void_p(dst.data_ptr()), C.c_void_p(src.ctypes.data), n, 4,
+                                     C.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert rc in (0, 1)
+    if rc == 0:
+        assert np.array_equal(dst.cpu().numpy(), src)
+    else:
+        assert b"page-locked" in clef.library().clef_last_error()
+        assert int(dst.count_nonzero()) == 0
 
 
 def test_copy_refuses_unpinned_and_mismatched():

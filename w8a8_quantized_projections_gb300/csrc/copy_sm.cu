@@ -13,8 +13,9 @@
 // beside it.
 //
 // Addresses are whatever the device can read or write: device memory, or
-// page-locked host memory (allocated or registered with CUDA), whose host
-// address is valid on the device under unified addressing.  The CTAs come in
+// page-locked host memory (allocated or registered with CUDA), reached
+// through its device mapping.  Other host memory is refused on the host,
+// unless the device reads pageable memory directly.  The CTAs come in
 // clusters of two where their count is even, so that they occupy whole SM
 // pairs and leave the pairs the GEMMs are launched on.
 #include <cstdint>
@@ -55,6 +56,22 @@ int fail(const char *msg) {
     return CLEF_ERR_INVALID_ARG;
 }
 
+// The address the kernel dereferences for p: device and managed memory as
+// they are, page-locked host memory through its device mapping, and other
+// host memory only where the device reads pageable memory directly.  nullptr
+// where the device cannot reach p (the call is then refused instead of
+// faulting on the GPU).
+const void *device_address(const void *p, bool pageable_ok) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();   // a failed query leaves its error behind: clear it
+        return pageable_ok ? p : nullptr;
+    }
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return p;
+    if (at.type == cudaMemoryTypeHost) return at.devicePointer;
+    return pageable_ok ? p : nullptr;
+}
+
 }  // namespace
 
 }  // namespace clef
@@ -75,6 +92,15 @@ extern "C" int clef_copy_sm(void *dst, const void *src, int64_t bytes, int ctas,
     unsigned int *status = nullptr;
     int rc = internal_device(&num_sms, &status);   // device checks (sm_103) first
     if (rc) return rc;
+    int dev = 0, pageable = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev);
+    const void *dsrc = device_address(src, pageable != 0);
+    void *ddst = const_cast<void *>(device_address(dst, pageable != 0));
+    if (!dsrc || !ddst)
+        return fail("invalid argument: host memory must be page-locked (cudaHostAlloc or cudaHostRegister)");
+    if ((reinterpret_cast<uintptr_t>(ddst) | reinterpret_cast<uintptr_t>(dsrc)) & 15u)
+        return fail("invalid argument: the device addresses must be 16-byte aligned");
     const int64_t n16 = bytes / 16;
     // no more CTAs than 16-byte words per thread-round, and clusters of two
     // where the count allows
@@ -82,8 +108,8 @@ extern "C" int clef_copy_sm(void *dst, const void *src, int64_t bytes, int ctas,
     if ((int64_t)grid * kCopyThreads > n16) grid = (int)((n16 + kCopyThreads - 1) / kCopyThreads);
     const int cluster = (grid % 2 == 0) ? 2 : 1;
     cudaError_t e = launch_kernel(copy_sm_kernel, dim3(grid), dim3(kCopyThreads), 0,
-                                  static_cast<cudaStream_t>(stream), cluster, false, static_cast<uint4 *>(dst),
-                                  static_cast<const uint4 *>(src), n16);
+                                  static_cast<cudaStream_t>(stream), cluster, false, static_cast<uint4 *>(ddst),
+                                  static_cast<const uint4 *>(dsrc), n16);
     if (e != cudaSuccess) return internal_cuda_error(e, "copy launch");
     return CLEF_OK;
 }
