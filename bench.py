@@ -663,8 +663,10 @@ def e2e(args, layer, acts, acts_np, cfg, dev, stream, world, torch):
     output buffer).  The copies are the library's clef_copy_sm on
     E2E_COPY_CTAS CTAs, and the compute runs under an SM budget that leaves
     them those SMs: copy-engine transfers from pinned host memory stalled
-    for 20-180 ms about every half second here (200 steps at 14.8-17.5 ms
-    against 11.8 ms without the stalls), SM loads over the same link do not."""
+    for 20-180 ms about every half second on some boxes (200 steps at
+    14.8-17.5 ms against 11.8 ms without the stalls) and rarely on others
+    (1,000 steps at 12.01 ms against 12.35 ms with the SM copies); SM loads
+    over the same link did not stall on any box tried."""
     host_in = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).pin_memory()
                for k, v in acts_np.items()}
     last = cfg.projections[-1].name

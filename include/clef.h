@@ -461,11 +461,12 @@ int clef_set_sm_budget(int sms);
  * access: device memory, or page-locked host memory (cudaHostAlloc or
  * cudaHostRegister), read and written through its device mapping.  Pageable
  * host memory returns CLEF_ERR_INVALID_ARG (nothing launched) unless the
- * device reads pageable memory directly (cudaDevAttrPageableMemoryAccess).  Copy-engine transfers from page-locked host memory
- * were measured to stall for 20-180 ms about every half second on this GPU;
- * SM loads over the same link ran at the same rate without stalls.  With a
- * budget (clef_set_sm_budget) of the device's SMs less ctas, the copy runs
- * beside the compute launches of another stream.
+ * device reads pageable memory directly (cudaDevAttrPageableMemoryAccess).
+ * Copy-engine transfers from page-locked host memory were measured to stall
+ * for 20-180 ms, on some GB300 machines about every half second and on others
+ * rarely; SM loads over the same link ran at the same rate without stalls on
+ * every box tried.  With a budget (clef_set_sm_budget) of the device's SMs
+ * less ctas, the copy runs beside the compute launches of another stream.
  * Requirements: dst and src 16-byte aligned, bytes >= 0 and a multiple of
  * 16, 1 <= ctas <= 64, the two ranges disjoint.  Ordered on stream like any
  * kernel; bytes == 0 returns CLEF_OK without a launch.

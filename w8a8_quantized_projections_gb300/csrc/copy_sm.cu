@@ -3,10 +3,11 @@
 //
 // A step that takes its activations from host memory moves them over the
 // CPU-GPU link while the previous step computes.  Copy-engine transfers from
-// page-locked host memory were measured to stall for 20-180 ms about every
-// half second on this GPU, with or without other work running, in whole or
-// in 16-64 MB pieces, on one stream or two; loads issued by SMs over the same
-// link ran at the same 211 GB/s without a stall.  The copy therefore runs as
+// page-locked host memory were measured to stall for 20-180 ms, on some GB300
+// boxes about every half second (with or without other work running, in
+// whole or in 16-64 MB pieces, on one stream or two) and on others rarely;
+// loads issued by SMs over the same link ran at the same 211 GB/s without a
+// stall on every box tried.  The copy therefore runs as
 // a kernel on a few SMs, beside the compute: the compute launches leave those
 // SMs free when the caller sets an SM budget (clef_set_sm_budget), because a
 // persistent GEMM CTA takes a whole SM and no copy CTA could be resident
